@@ -1,0 +1,39 @@
+/*
+ * CPU oracle for C = A * B over row-major fp32 matrices. Test
+ * infrastructure only: the product library never includes this header.
+ * All routines return 0 on success and nonzero on a bad argument.
+ */
+#ifndef SGEMM_ORACLE_H
+#define SGEMM_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* The CPU loop of the source pages: float accumulator, k ascending. */
+int oracle_sgemm_f32(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda,
+                     const float *B, int64_t ldb, float *C, int64_t ldc);
+
+/* Same loop in double; S (may be NULL) receives sum_k |A[i][k]|*|B[k][j]|. */
+int oracle_sgemm_f64(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda,
+                     const float *B, int64_t ldb, double *C64, double *S, int64_t ldc);
+
+/* Rows [row_begin, row_end) of the double product, i-k-j order, threaded by rows.
+ * Output row r of C64 / S is product row row_begin + r. Bit-identical to
+ * oracle_sgemm_f64 on those rows. */
+int oracle_sgemm_f64_rows(int64_t row_begin, int64_t row_end, int64_t N, int64_t K,
+                          const float *A, int64_t lda, const float *B, int64_t ldb,
+                          double *C64, double *S, int64_t ldc, int nthreads);
+
+/* Double product and S at n_samples (rows[t], cols[t]) positions. */
+int oracle_sgemm_f64_at(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda,
+                        const float *B, int64_t ldb, int64_t n_samples, const int64_t *rows,
+                        const int64_t *cols, double *c64, double *s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif
