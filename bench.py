@@ -1,0 +1,438 @@
+#!/usr/bin/env python3
+"""Benchmark of the GB300 SGEMM: GFLOP/s (2MNK / time) and the roofline fraction.
+
+One step = one C = A * B over the workload's seeded synthetic inputs, already
+resident in HBM. Default workload: M = 2048, K = 4096, N = 3072, N(0, 1)
+entries, seed 4 (the benchmark shape of "CUDA算子优化(4)：矩阵乘法"). Its
+inputs and output (109 MB) fit in the 129 MB L2, so a 256 MiB buffer is
+written between timed steps to flush L2; only the product is inside the
+CUDA events.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--variant auto|ffma|tf32x3] [--workload NAME] [--all-configs]
+
+Prints one JSON line (rank 0). With N > 1 (torchrun, one process per GPU)
+every rank runs its own replica of the workload: the product does not shard
+with a data-path exchange, so there is no collective beyond the timing
+barrier and the max-over-ranks reduction. ``--impl reference`` times the CPU
+oracle (the pages' float triple loop) on a bounded row sample instead.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from dense_fp32_matrix_major_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "SGEMM GFLOP/s (2MNK/s) on 1 GB300 and % of FP32 roofline peak"
+UNIT = "GFLOP/s"
+L2_FLUSH_BYTES = 256 << 20
+# FP32 lanes per SM and the maximum SM clock of a GB300 (the profiling
+# recipe's unit counts): the FFMA peak is SMs x 128 x 2 flops x clock.
+FP32_LANES_PER_SM = 128
+GB300_MAX_SM_MHZ = 2070.0
+# Fallback denominators (no measured-peaks file): dense bf16 1.9 PFLOP/s burst,
+# HBM 6.8 TB/s; TF32 runs at 1.1 / 2.25 of the bf16 rate (nominal ratio).
+FALLBACK_BF16_TFLOPS = 1900.0
+TF32_OVER_BF16 = 1.1 / 2.25
+
+
+def _dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ------------------------------------------------------------------ clocks
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.lines: list[str] = []
+        self._thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu_index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self._thread = threading.Thread(target=self._read, daemon=True)
+        self._thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self._thread:
+            self._thread.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- peaks
+
+
+def _measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        with open(path) as f:
+            return json.load(f)
+    except (OSError, ValueError):
+        return None
+
+
+def _tf32x3_peak_tflops():
+    """fp32-equivalent ceiling of the three-product TF32 path: TF32 dense / 3."""
+    peaks = _measured_peaks()
+    if peaks and peaks.get("bf16_tflops"):
+        return float(peaks["bf16_tflops"]) * TF32_OVER_BF16 / 3.0, "measured bf16 x 1.1/2.25 / 3"
+    return FALLBACK_BF16_TFLOPS * TF32_OVER_BF16 / 3.0, "fallback bf16 1.9 PF x 1.1/2.25 / 3"
+
+
+def _traffic_record(kernel_key: str):
+    """Per-launch DRAM bytes from the committed ncu summary, if the kernel is unchanged."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            recs = json.load(f)
+    except (OSError, ValueError):
+        return None
+    rec = recs.get(kernel_key)
+    if not rec:
+        return None
+    src = os.path.join(ROOT, rec["source"])
+    try:
+        with open(src, "rb") as f:
+            digest = hashlib.sha256(f.read()).hexdigest()[:16]
+    except OSError:
+        return None
+    return rec["dram_bytes_per_launch"] if digest == rec["source_sha256_16"] else None
+
+
+# -------------------------------------------------------------- our arm
+
+
+def _device_inputs(w, torch, device):
+    A, B = _host_inputs(w)
+    dA = torch.from_numpy(np.ascontiguousarray(A)).to(device)
+    dB = torch.from_numpy(np.ascontiguousarray(B)).to(device)
+    dC = torch.empty((w.M, w.N), dtype=torch.float32, device=device)
+    return A, B, dA, dB, dC
+
+
+def run_ours(args, w, torch, dist):
+    from dense_fp32_matrix_major_gb300 import sgemm
+
+    ws, rank, local = _dist_env()
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    sgemm.set_variant(args.variant)
+    A, B, dA, dB, dC = _device_inputs(w, torch, device)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream()
+    sh = stream.cuda_stream
+
+    def step():
+        rc = sgemm.sgemm_f32_raw(w.M, w.N, w.K, dA.data_ptr(), w.K, dB.data_ptr(), w.N,
+                                 dC.data_ptr(), w.N, sh)
+        if rc:
+            raise sgemm.SgemmError(rc, "sgemm_f32")
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    variant_used = sgemm.variant_name(sgemm.last_variant_used())
+    launches_per_step = sgemm.last_launch_count()
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)  # let the sampler start before the timed region
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()  # L2 flush between timed steps, outside the events
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    wall = time.perf_counter() - wall0
+    sampler.stop()
+    per_step = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms = sum(per_step) / len(per_step)
+    ms_max = ms
+    if dist is not None:
+        t = torch.tensor([ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_max = float(t.item())
+    value = ws * w.flops / (ms_max * 1e-3) / 1e9
+
+    # Parity spot check of the timed output (cheap, sampled; not timed).
+    import oracle  # test infrastructure: used here only to spot-check the result
+    r, c = wl.sample_positions(w.M, w.N, 64, seed=99)
+    c64, s = oracle.sgemm_f64_at(A, B, r, c)
+    err = oracle.normalized_error(dC.cpu().numpy()[r, c], c64, s)
+
+    # End to end: host buffers through the C ABI, copies inside the timed region.
+    e2e = run_e2e(args, w, torch, sgemm, A, B, device, dist, ws)
+
+    clocks = sampler.summary()
+    sm_max = clocks["sm_max_mhz"] or GB300_MAX_SM_MHZ
+    sm_count = torch.cuda.get_device_properties(device).multi_processor_count
+    if variant_used == "tf32x3":
+        peak, peak_src = _tf32x3_peak_tflops()
+        bound = "tensor"
+        kernel_key = "tf32x3"
+    else:
+        peak = sm_count * FP32_LANES_PER_SM * 2 * sm_max * 1e6 / 1e12
+        peak_src = f"{sm_count} SMs x 128 FP32 lanes x 2 x {sm_max:.0f} MHz (recipe unit counts)"
+        bound = "alu"
+        kernel_key = "ffma"
+    achieved = w.flops / (ms * 1e-3) / 1e12
+    roofline = {
+        "bound": bound, "achieved": round(achieved, 3), "peak": round(peak, 3), "unit": "TFLOP/s",
+        "frac": round(achieved / peak, 4), "traffic": _traffic_record(kernel_key),
+        "peak_source": peak_src,
+        "algorithmic_flops_per_launch": w.flops,
+        "timing": "CUDA events around each sgemm_f32 call on its stream (includes the small "
+                  "zeroing kernel when stream-K tiles exist), mean over the timed steps",
+    }
+    return {
+        "value": value, "ms_per_step": ms_max, "wall_s": wall, "variant": variant_used,
+        "launches_per_step": launches_per_step, "per_step_ms_min": min(per_step),
+        "per_step_ms_median": statistics.median(per_step), "roofline": roofline, "e2e": e2e,
+        "clocks": clocks, "parity_sampled_err": err,
+    }
+
+
+def run_e2e(args, w, torch, sgemm, A, B, device, dist, ws):
+    Ah = torch.from_numpy(np.ascontiguousarray(A)).pin_memory()
+    Bh = torch.from_numpy(np.ascontiguousarray(B)).pin_memory()
+    Ch = torch.empty((w.M, w.N), dtype=torch.float32).pin_memory()
+    dA = torch.empty_like(Ah, device=device)
+    dB = torch.empty_like(Bh, device=device)
+    dC = torch.empty_like(Ch, device=device)
+    stream = torch.cuda.current_stream()
+    steps = max(3, min(args.steps, args.e2e_steps))
+    for _ in range(2):
+        sgemm.sgemm_f32_from_host(Ah, Bh, Ch, dA, dB, dC, stream)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(steps):
+        sgemm.sgemm_f32_from_host(Ah, Bh, Ch, dA, dB, dC, stream)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    ms = ev0.elapsed_time(ev1) / steps
+    if dist is not None:
+        t = torch.tensor([ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return {
+        "value": round(ws * w.flops / (ms * 1e-3) / 1e9, 2), "unit": UNIT,
+        "h2d_bytes_per_step": 4 * (w.M * w.K + w.K * w.N), "d2h_bytes_per_step": 4 * w.M * w.N,
+        "ms_per_step": round(ms, 4), "steps": steps,
+        "path": "sgemm_f32_from_host: pinned host A, B -> device, product, device C -> pinned host",
+    }
+
+
+# ------------------------------------------------------------ CPU oracle
+
+
+_INPUT_CACHE = {}
+
+
+def _host_inputs(w):
+    if w.name not in _INPUT_CACHE:
+        _INPUT_CACHE[w.name] = wl.make_inputs(w)
+    return _INPUT_CACHE[w.name]
+
+
+def cpu_oracle_sample(w, budget_s: float):
+    """Time the oracle's float loop (one thread) on the first rows of the workload."""
+    import oracle  # test infrastructure: timed here as the CPU baseline
+
+    A, B = _host_inputs(w)
+    rows = 1
+    t0 = time.perf_counter()
+    oracle.sgemm_f32(np.ascontiguousarray(A[:rows]), B)
+    t1 = time.perf_counter() - t0
+    rows = int(max(1, min(w.M, budget_s / max(t1, 1e-6))))
+    t0 = time.perf_counter()
+    oracle.sgemm_f32(np.ascontiguousarray(A[:rows]), B)
+    secs = time.perf_counter() - t0
+    flops = 2 * rows * w.N * w.K
+    return {
+        "value": round(flops / secs / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+        "sample": f"rows 0..{rows - 1} of A ({rows} x {w.K}) times all of B ({w.K} x {w.N}): "
+                  f"the float i-j-k loop, one thread, {secs:.1f} s",
+        "seconds": round(secs, 2),
+    }
+
+
+def run_reference(args, w):
+    ws, rank, _ = _dist_env()
+    if rank != 0:
+        return None
+    budget = args.ref_step_seconds
+    for _ in range(args.warmup):
+        cpu_oracle_sample(w, budget / 4)
+    vals, secs = [], 0.0
+    for _ in range(args.steps):
+        r = cpu_oracle_sample(w, budget)
+        vals.append(r["value"])
+        secs += r["seconds"]
+    value = statistics.mean(vals)
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(2 * w.M * w.N * w.K / (value * 1e9) * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic", "config": _config(w, "oracle"),
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": r["sample"]},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "note": "the CPU oracle (float triple loop of the source pages), timed on a bounded row "
+                "sample each step; ms_per_step is the full workload extrapolated from the rate",
+    }
+
+
+def _config(w, variant):
+    return {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "dist": w.dist, "seed": w.seed,
+            "layout": "row-major fp32, lda=K, ldb=N, ldc=N", "variant": variant,
+            "l2": "flushed between timed steps (256 MiB write); inputs+output 109 MB < 129 MB L2",
+            "parallelism": "replicas (one independent product per GPU)"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--variant", default="auto", choices=["auto", "ffma", "tf32x3"])
+    ap.add_argument("--workload", default=wl.C5_HEAD.name, choices=sorted(wl.BY_NAME))
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--ref-step-seconds", type=float, default=4.0)
+    ap.add_argument("--all-configs", action="store_true",
+                    help="also print one extra line per workload (not the headline line)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    w = wl.BY_NAME[args.workload]
+    ws, rank, local = _dist_env()
+
+    if args.impl == "reference":
+        res = run_reference(args, w)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return
+
+    import torch
+
+    dist = None
+    if ws > 1:
+        import torch.distributed as tdist
+        torch.cuda.set_device(local)
+        tdist.init_process_group("nccl")
+        dist = tdist
+    res = run_ours(args, w, torch, dist)
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(res["value"], 2), "unit": UNIT, "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(res["ms_per_step"], 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded numpy PCG64, N(0,1))",
+            "config": _config(w, res["variant"]),
+            "roofline": res["roofline"],
+            "e2e": res["e2e"],
+            "gpu_launches": res["launches_per_step"] * args.steps,
+            "clocks": res["clocks"],
+            "per_step_ms": {"mean": round(res["ms_per_step"], 5), "min": round(res["per_step_ms_min"], 5),
+                            "median": round(res["per_step_ms_median"], 5)},
+            "parity_sampled_err": res["parity_sampled_err"],
+        }
+        line["cpu_baseline"] = cpu_oracle_sample(w, args.cpu_seconds) if ws == 1 else None
+        print(json.dumps(line), flush=True)
+        if args.all_configs:
+            for other in wl.ALL:
+                if other is w:
+                    continue
+                sub = argparse.Namespace(**vars(args))
+                sub.steps = min(args.steps, 200)
+                r = run_ours(sub, other, torch, None)
+                print(json.dumps({"workload": other.name, "value": round(r["value"], 2), "unit": UNIT,
+                                  "ms_per_step": round(r["ms_per_step"], 5), "variant": r["variant"],
+                                  "roofline_frac": r["roofline"]["frac"],
+                                  "parity_sampled_err": r["parity_sampled_err"]}), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,258 @@
+// C ABI of libsgemm_gb300: argument checks, variant selection and dispatch.
+// The declarations and the contract of every entry point are in sgemm.h.
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "sgemm.h"
+#include "sgemm_internal.h"
+
+namespace sgemm {
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+std::once_flag g_env_once;
+std::atomic<int> g_variant{SGEMM_AUTO};
+std::atomic<int> g_last_variant{SGEMM_AUTO};
+std::atomic<int> g_last_launches{0};
+std::atomic<int64_t> g_tune_tile{0};
+std::atomic<int64_t> g_tune_sk{0};
+
+struct DevCache {
+    std::once_flag once[kMaxDevices];
+    DeviceInfo info[kMaxDevices];
+    int status[kMaxDevices];
+};
+DevCache g_dev;
+
+int parse_variant(const char *s) {
+    if (!s || !*s) return -1;
+    if (!strcmp(s, "0") || !strcmp(s, "auto")) return SGEMM_AUTO;
+    if (!strcmp(s, "1") || !strcmp(s, "ffma")) return SGEMM_FFMA;
+    if (!strcmp(s, "2") || !strcmp(s, "tf32x3")) return SGEMM_TF32X3;
+    return -1;
+}
+
+void read_env() {
+    std::call_once(g_env_once, [] {
+        const int v = parse_variant(getenv("SGEMM_VARIANT"));
+        if (v >= 0) g_variant.store(v);
+    });
+}
+
+// Byte range [lo, hi) spanned by a rows x cols matrix with row stride ld.
+void span(const void *p, int64_t rows, int64_t cols, int64_t ld, uintptr_t *lo, uintptr_t *hi) {
+    *lo = reinterpret_cast<uintptr_t>(p);
+    *hi = *lo + static_cast<uintptr_t>(((rows - 1) * ld + cols) * static_cast<int64_t>(sizeof(float)));
+}
+
+bool overlaps(const void *x, int64_t xr, int64_t xc, int64_t xld, const void *y, int64_t yr, int64_t yc,
+              int64_t yld) {
+    if (xr == 0 || xc == 0 || yr == 0 || yc == 0) return false;
+    uintptr_t a0, a1, b0, b1;
+    span(x, xr, xc, xld, &a0, &a1);
+    span(y, yr, yc, yld, &b0, &b1);
+    return a0 < b1 && b0 < a1;
+}
+
+int check_args(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, const float *B, int64_t ldb,
+               const float *C, int64_t ldc) {
+    if (M < 0 || N < 0 || K < 0) return SGEMM_ERR_INVALID_ARG;
+    if (lda < K || ldb < N || ldc < N) return SGEMM_ERR_INVALID_ARG;
+    if (lda < 1 || ldb < 1 || ldc < 1) return SGEMM_ERR_INVALID_ARG;
+    // Element offsets must fit in int64 with room to spare.
+    const int64_t lim = INT64_C(1) << 60;
+    if ((M > 0 && lda > lim / M) || (K > 0 && ldb > lim / K) || (M > 0 && ldc > lim / M))
+        return SGEMM_ERR_INVALID_ARG;
+    if (M > 0 && K > 0 && !A) return SGEMM_ERR_INVALID_ARG;
+    if (K > 0 && N > 0 && !B) return SGEMM_ERR_INVALID_ARG;
+    if (M > 0 && N > 0 && !C) return SGEMM_ERR_INVALID_ARG;
+    if (M > 0 && N > 0) {
+        if (overlaps(C, M, N, ldc, A, M, K, lda) || overlaps(C, M, N, ldc, B, K, N, ldb))
+            return SGEMM_ERR_INVALID_ARG;
+    }
+    return SGEMM_OK;
+}
+
+int enqueue(const Problem &p, cudaStream_t stream) {
+    read_env();
+    DeviceInfo dev;
+    int rc = current_device(&dev);
+    if (rc != SGEMM_OK) return rc;
+    int launches = 0;
+    if (p.M == 0 || p.N == 0) {
+        g_last_launches.store(0);
+        return SGEMM_OK;
+    }
+    if (p.K == 0) {
+        rc = zero_launch(p.C, p.M, p.N, p.ldc, dev, stream, &launches);
+        if (rc == SGEMM_OK) {
+            g_last_variant.store(SGEMM_FFMA);
+            g_last_launches.store(launches);
+        }
+        return rc;
+    }
+    int variant = g_variant.load();
+    if (variant == SGEMM_AUTO) variant = tf32x3_supports(p, dev) ? SGEMM_TF32X3 : SGEMM_FFMA;
+    if (variant == SGEMM_TF32X3) {
+        if (!tf32x3_supports(p, dev)) return SGEMM_ERR_UNSUPPORTED;
+        rc = tf32x3_launch(p, dev, stream, &launches);
+    } else {
+        rc = ffma_launch(p, dev, static_cast<int>(g_tune_tile.load()), static_cast<int>(g_tune_sk.load()),
+                         stream, &launches);
+    }
+    if (rc == SGEMM_OK) {
+        g_last_variant.store(variant);
+        g_last_launches.store(launches);
+    }
+    return rc;
+}
+
+}  // namespace
+
+int current_device(DeviceInfo *info) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return SGEMM_ERR_DEVICE;
+    }
+    std::call_once(g_dev.once[dev], [dev] {
+        DeviceInfo d{};
+        d.device = dev;
+        int optin = 0;
+        bool ok = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
+                  cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev) == cudaSuccess &&
+                  cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev) == cudaSuccess &&
+                  cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) == cudaSuccess;
+        d.smem_optin = static_cast<size_t>(optin);
+        g_dev.info[dev] = d;
+        if (!ok) {
+            cudaGetLastError();
+            g_dev.status[dev] = SGEMM_ERR_DEVICE;
+        } else {
+            // The kernels are built for sm_103a only.
+            g_dev.status[dev] = (d.cc_major == 10 && d.cc_minor == 3) ? SGEMM_OK : SGEMM_ERR_DEVICE;
+        }
+    });
+    *info = g_dev.info[dev];
+    return g_dev.status[dev];
+}
+
+}  // namespace sgemm
+
+using sgemm::Problem;
+
+extern "C" {
+
+int sgemm_f32(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, const float *B, int64_t ldb,
+              float *C, int64_t ldc, sgemm_stream_t stream) {
+    int rc = sgemm::check_args(M, N, K, A, lda, B, ldb, C, ldc);
+    if (rc != SGEMM_OK) return rc;
+    Problem p{M, N, K, A, lda, B, ldb, C, ldc};
+    return sgemm::enqueue(p, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int sgemm_f32_from_host(int64_t M, int64_t N, int64_t K, const float *A_host, int64_t lda,
+                        const float *B_host, int64_t ldb, float *C_host, int64_t ldc, float *dA, float *dB,
+                        float *dC, sgemm_stream_t stream) {
+    int rc = sgemm::check_args(M, N, K, dA, lda, dB, ldb, dC, ldc);
+    if (rc != SGEMM_OK) return rc;
+    if ((M > 0 && K > 0 && !A_host) || (K > 0 && N > 0 && !B_host) || (M > 0 && N > 0 && !C_host))
+        return SGEMM_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const size_t f = sizeof(float);
+    if (M > 0 && K > 0 &&
+        cudaMemcpy2DAsync(dA, lda * f, A_host, lda * f, K * f, M, cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return cudaGetLastError(), SGEMM_ERR_LAUNCH;
+    if (K > 0 && N > 0 &&
+        cudaMemcpy2DAsync(dB, ldb * f, B_host, ldb * f, N * f, K, cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return cudaGetLastError(), SGEMM_ERR_LAUNCH;
+    Problem p{M, N, K, dA, lda, dB, ldb, dC, ldc};
+    rc = sgemm::enqueue(p, s);
+    if (rc != SGEMM_OK) return rc;
+    if (M > 0 && N > 0 &&
+        cudaMemcpy2DAsync(C_host, ldc * f, dC, ldc * f, N * f, M, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return cudaGetLastError(), SGEMM_ERR_LAUNCH;
+    return SGEMM_OK;
+}
+
+int sgemm_set_variant(int variant) {
+    sgemm::read_env();
+    if (variant < SGEMM_AUTO || variant > SGEMM_TF32X3) return SGEMM_ERR_INVALID_ARG;
+    sgemm::g_variant.store(variant);
+    return SGEMM_OK;
+}
+
+int sgemm_get_variant(void) {
+    sgemm::read_env();
+    return sgemm::g_variant.load();
+}
+
+const char *sgemm_variant_name(int variant) {
+    switch (variant) {
+        case SGEMM_AUTO: return "auto";
+        case SGEMM_FFMA: return "ffma";
+        case SGEMM_TF32X3: return "tf32x3";
+        default: return "unknown";
+    }
+}
+
+int sgemm_last_variant_used(void) { return sgemm::g_last_variant.load(); }
+
+int sgemm_last_launch_count(void) { return sgemm::g_last_launches.load(); }
+
+const char *sgemm_strerror(int status) {
+    switch (status) {
+        case SGEMM_OK: return "success";
+        case SGEMM_ERR_INVALID_ARG: return "invalid argument";
+        case SGEMM_ERR_UNSUPPORTED: return "variant does not support this shape or alignment";
+        case SGEMM_ERR_LAUNCH: return "CUDA launch or copy failed";
+        case SGEMM_ERR_DEVICE: return "no usable sm_103a device";
+        case SGEMM_ERR_TIMEOUT: return "a kernel gave up a bounded wait";
+        default: return "unknown status";
+    }
+}
+
+int sgemm_device_status(void) {
+    if (cudaDeviceSynchronize() != cudaSuccess) {
+        cudaGetLastError();
+        return SGEMM_ERR_LAUNCH;
+    }
+    int code = 0;
+    if (sgemm::watchdog_read_and_clear(&code) != 0) return SGEMM_ERR_LAUNCH;
+    return code ? SGEMM_ERR_TIMEOUT : SGEMM_OK;
+}
+
+int sgemm_set_tuning(int key, int64_t value) {
+    switch (key) {
+        case SGEMM_TUNE_FFMA_TILE:
+            if (value < 0 || value > 3) return SGEMM_ERR_INVALID_ARG;
+            sgemm::g_tune_tile.store(value);
+            return SGEMM_OK;
+        case SGEMM_TUNE_STREAM_K:
+            if (value < 0 || value > 3) return SGEMM_ERR_INVALID_ARG;
+            sgemm::g_tune_sk.store(value);
+            return SGEMM_OK;
+        case SGEMM_TUNE_WATCHDOG_POLLS:
+            return sgemm::watchdog_set_polls(value);
+        default: return SGEMM_ERR_INVALID_ARG;
+    }
+}
+
+int64_t sgemm_get_tuning(int key) {
+    switch (key) {
+        case SGEMM_TUNE_FFMA_TILE: return sgemm::g_tune_tile.load();
+        case SGEMM_TUNE_STREAM_K: return sgemm::g_tune_sk.load();
+        case SGEMM_TUNE_WATCHDOG_POLLS: return sgemm::watchdog_polls();
+        default: return -1;
+    }
+}
+
+const char *sgemm_version(void) { return "0.1.0"; }
+
+}  // extern "C"

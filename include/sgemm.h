@@ -1,0 +1,151 @@
+/*
+ * sgemm.h — C ABI of the GB300 (sm_103a) dense fp32 matrix multiplication
+ * library, libsgemm_gb300.so.
+ *
+ * The operation is the plain product of row-major single-precision matrices
+ *
+ *     C[i][j] = sum over k = 0 .. K-1 of A[i][k] * B[k][j]
+ *
+ * with A of M x K, B of K x N and C of M x N. This is the definition stated
+ * in "CUDA算子优化(4)：矩阵乘法", section "矩阵乘法的数学定义", and in
+ * "CUDA内存优化入门：从Naive到Tiled矩阵乘法", section 三 (formula block);
+ * both index row-major storage as A[i*K + k], B[k*N + j], C[i*N + j]. This
+ * ABI adds a row stride per matrix: element (r, c) of a matrix with row
+ * stride ld sits at offset r*ld + c (in elements, not bytes).
+ *
+ * Conventions shared by every entry point
+ *   - Sizes and strides are int64_t element counts.
+ *   - Matrix pointers are device pointers (memory that the current CUDA
+ *     device can read and write), except where an entry point says "host".
+ *   - The caller owns every buffer. The library allocates no device or host
+ *     memory in any call, keeps no pointer after a call returns, and never
+ *     synchronises the stream.
+ *   - Calls are asynchronous: they enqueue work on `stream` and return. A
+ *     NULL stream means the legacy default stream. Errors raised by a kernel
+ *     while it runs surface on the stream (cudaStreamSynchronize), not here.
+ *   - The library runs only on devices of compute capability 10.3 (sm_103a).
+ *   - No entry point ever calls exit() or falls back to the CPU.
+ */
+#ifndef DENSE_FP32_SGEMM_GB300_H
+#define DENSE_FP32_SGEMM_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t, declared here so the header needs no CUDA include. */
+typedef struct CUstream_st *sgemm_stream_t;
+
+/* Status codes returned by every int-returning entry point. */
+enum sgemm_status {
+    SGEMM_OK = 0,
+    SGEMM_ERR_INVALID_ARG = 1, /* negative size, stride shorter than a row, NULL
+                                  pointer with a non-empty extent, C overlapping
+                                  A or B, unknown variant or tuning key */
+    SGEMM_ERR_UNSUPPORTED = 2, /* a forced variant cannot run this shape or
+                                  alignment (SGEMM_AUTO never returns this) */
+    SGEMM_ERR_LAUNCH = 3,      /* a CUDA call failed while enqueueing */
+    SGEMM_ERR_DEVICE = 4,      /* no usable device, or not compute capability 10.3 */
+    SGEMM_ERR_TIMEOUT = 5      /* a kernel gave up a bounded wait (see sgemm_device_status) */
+};
+
+/* Kernel variants. */
+enum sgemm_variant {
+    SGEMM_AUTO = 0,   /* pick per shape and alignment */
+    SGEMM_FFMA = 1,   /* register-blocked fp32 fused multiply-add on the CUDA cores */
+    SGEMM_TF32X3 = 2  /* tensor cores (tcgen05) with the three-term TF32 split */
+};
+
+/*
+ * C = A * B.
+ *   M, N, K   sizes; each >= 0.
+ *   A, lda    M x K, row stride lda >= K; read only.
+ *   B, ldb    K x N, row stride ldb >= N; read only.
+ *   C, ldc    M x N, row stride ldc >= N; every element of the M x N box is
+ *             overwritten (no alpha, no beta: C's old contents are not read).
+ *             Elements between column N and the next row start are never
+ *             written. C must not overlap A or B.
+ *   stream    CUDA stream to enqueue on.
+ * M == 0 or N == 0: nothing is enqueued, SGEMM_OK. K == 0: C is set to zero
+ * (the empty sum). A NULL pointer is accepted only for a matrix with no
+ * elements. Results: every output is the exact sum rounded with fp32
+ * arithmetic in an order the library chooses; the acceptance bound is
+ * max |C - C_exact| / sum_k |A[i][k]| |B[k][j]| <= 1e-5, and inputs whose
+ * products and partial sums are integers below 2^24 give exact results.
+ * Returns SGEMM_OK or an sgemm_status code; on error nothing is enqueued.
+ */
+int sgemm_f32(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, const float *B,
+              int64_t ldb, float *C, int64_t ldc, sgemm_stream_t stream);
+
+/*
+ * C = A * B for matrices that live in HOST memory, through caller-owned
+ * device buffers. Enqueues, on `stream`: the copy of A_host into dA and of
+ * B_host into dB (row strides kept), the product into dC, and the copy of
+ * dC back into C_host. dA, dB, dC are device buffers with the same row
+ * strides as the host matrices (lda, ldb, ldc) and at least that many rows.
+ * Host buffers should be page-locked (cudaHostAlloc) for the copies to be
+ * asynchronous; the caller synchronises the stream before reading C_host.
+ * Same sizes, strides, errors and results as sgemm_f32.
+ */
+int sgemm_f32_from_host(int64_t M, int64_t N, int64_t K, const float *A_host, int64_t lda,
+                        const float *B_host, int64_t ldb, float *C_host, int64_t ldc, float *dA,
+                        float *dB, float *dC, sgemm_stream_t stream);
+
+/* Variant selection, process-wide (all threads, all devices). Returns SGEMM_OK
+ * or SGEMM_ERR_INVALID_ARG for an unknown value. The initial value is
+ * SGEMM_AUTO, or the value of the environment variable SGEMM_VARIANT (0, 1, 2
+ * or a variant name) read at the first call. */
+int sgemm_set_variant(int variant);
+int sgemm_get_variant(void);
+/* Name of a variant ("auto", "ffma", "tf32x3"), or "unknown". Static storage. */
+const char *sgemm_variant_name(int variant);
+/* Variant that the most recent successful sgemm_f32 call in this process
+ * enqueued (SGEMM_AUTO before any call). For reporting only. */
+int sgemm_last_variant_used(void);
+/* Number of kernel launches that the most recent successful sgemm_f32 call
+ * enqueued (0 for an empty product). For reporting only. */
+int sgemm_last_launch_count(void);
+
+/* Human-readable text of a status code. Static storage. */
+const char *sgemm_strerror(int status);
+
+/*
+ * Bounded waits. Kernels that wait on an mbarrier or a flag give up after a
+ * fixed number of polls, record the event in a per-device flag and return
+ * without writing their tile. This call waits for all work on the current
+ * device (cudaDeviceSynchronize), then returns SGEMM_ERR_TIMEOUT if a kernel
+ * gave up since the last call (and clears the flag), SGEMM_ERR_LAUNCH if the
+ * device reported an error, else SGEMM_OK.
+ */
+int sgemm_device_status(void);
+
+/*
+ * Tuning keys for sgemm_set_tuning / sgemm_get_tuning (process-wide).
+ *   SGEMM_TUNE_FFMA_TILE     0 = choose per shape; 1 = 128x256; 2 = 128x128;
+ *                            3 = 64x64 (FFMA block tile, M x N)
+ *   SGEMM_TUNE_STREAM_K      0 = choose per shape; 1 = data-parallel only;
+ *                            2 = data-parallel waves plus a stream-K remainder;
+ *                            3 = stream-K over all tiles
+ *   SGEMM_TUNE_WATCHDOG_POLLS  polls before a bounded wait gives up (>= 1024)
+ * Returns SGEMM_OK or SGEMM_ERR_INVALID_ARG. sgemm_get_tuning returns the
+ * value, or -1 for an unknown key.
+ */
+enum sgemm_tuning_key {
+    SGEMM_TUNE_FFMA_TILE = 1,
+    SGEMM_TUNE_STREAM_K = 2,
+    SGEMM_TUNE_WATCHDOG_POLLS = 3
+};
+int sgemm_set_tuning(int key, int64_t value);
+int64_t sgemm_get_tuning(int key);
+
+/* Library version as "major.minor.patch". Static storage. */
+const char *sgemm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DENSE_FP32_SGEMM_GB300_H */

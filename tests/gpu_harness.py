@@ -1,0 +1,80 @@
+"""Helpers for the GPU parity tests: place matrices in device memory with
+chosen row strides and pointer offsets, guard bands around C, and compare
+with the CPU oracle."""
+
+from __future__ import annotations
+
+import numpy as np
+
+import oracle
+
+CANARY = np.float32(7777.25)  # every float of C's buffer outside the M x N box
+GUARD = 67                    # floats of guard band after each buffer
+TOL = 1e-5                    # max |C - C64| / sum_k |A||B|
+
+
+def device_matrix(values: np.ndarray, ld: int | None = None, offset: int = 0, fill=CANARY):
+    """(flat, view): a flat CUDA buffer and a rows x cols strided view into it.
+
+    The view starts ``offset`` floats into the buffer, rows sit ``ld`` floats
+    apart; everything else in the buffer holds ``fill``.
+    """
+    import torch
+
+    rows, cols = values.shape
+    ld = cols if ld is None else ld
+    assert ld >= cols
+    size = offset + max(rows, 1) * ld + GUARD
+    flat = torch.full((size,), float(fill), dtype=torch.float32)
+    if rows and cols:
+        box = flat[offset:offset + rows * ld].view(rows, ld)[:, :cols]
+        box.copy_(torch.from_numpy(np.ascontiguousarray(values)))
+    flat = flat.cuda()
+    view = flat.as_strided((rows, cols), (ld, 1), offset)
+    return flat, view
+
+
+def run_sgemm(A: np.ndarray, B: np.ndarray, *, lda=None, ldb=None, ldc=None, offsets=(0, 0, 0),
+              prefill=np.nan):
+    """Run the library on numpy inputs; return (C as numpy, C's flat buffer on host, status)."""
+    import torch
+    from dense_fp32_matrix_major_gb300 import sgemm
+
+    M, K = A.shape
+    N = B.shape[1]
+    lda = max(K, 1) if lda is None else lda
+    ldb = max(N, 1) if ldb is None else ldb
+    ldc = max(N, 1) if ldc is None else ldc
+    fa, vA = device_matrix(A, lda, offsets[0])
+    fb, vB = device_matrix(B, ldb, offsets[1])
+    cvals = np.full((M, N), prefill, dtype=np.float32)
+    fc, vC = device_matrix(cvals, ldc, offsets[2])
+    stream = torch.cuda.current_stream()
+    rc = sgemm.sgemm_f32_raw(M, N, K, vA.data_ptr(), lda, vB.data_ptr(), ldb, vC.data_ptr(), ldc,
+                             stream.cuda_stream)
+    torch.cuda.synchronize()
+    flat = fc.cpu().numpy()
+    box = vC.cpu().numpy() if M and N else np.zeros((M, N), np.float32)
+    return box, flat, rc
+
+
+def outside_box_intact(flat: np.ndarray, M: int, N: int, ldc: int, offset: int) -> bool:
+    """True if every float of C's buffer outside the M x N box still holds CANARY."""
+    mask = np.ones(flat.shape[0], dtype=bool)
+    for i in range(M):
+        mask[offset + i * ldc: offset + i * ldc + N] = False
+    return bool(np.all(flat[mask].view(np.uint32) == np.float32(CANARY).view(np.uint32)))
+
+
+def oracle_error(C: np.ndarray, A: np.ndarray, B: np.ndarray, nthreads=None) -> float:
+    """Normalised error of C against the double-accumulating oracle (full product)."""
+    if A.shape[0] * A.shape[1] * B.shape[1] <= 2_000_000:
+        C64, S = oracle.sgemm_f64(A, B)
+    else:
+        C64, S = oracle.sgemm_f64_rows(A, B, nthreads=nthreads)
+    return oracle.normalized_error(C, C64, S)
+
+
+def sampled_error(C: np.ndarray, A: np.ndarray, B: np.ndarray, rows, cols) -> float:
+    c64, s = oracle.sgemm_f64_at(A, B, rows, cols)
+    return oracle.normalized_error(C[rows, cols], c64, s)

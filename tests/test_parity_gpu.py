@@ -1,0 +1,202 @@
+"""GPU parity: the CUDA library against the CPU oracle, element by element.
+
+Acceptance: max |C_gpu - C64| / sum_k |A||B| <= 1e-5 (C64 = the oracle's
+double-accumulating product), bit-exact where every product and partial sum
+is an integer below 2^24, and no write outside the M x N box of C.
+"""
+
+import itertools
+
+import numpy as np
+import pytest
+
+import oracle
+from dense_fp32_matrix_major_gb300 import workloads as wl
+from tests.gpu_harness import TOL, outside_box_intact, oracle_error, run_sgemm, sampled_error
+
+pytestmark = pytest.mark.gpu
+
+# (variant, ffma tile, stream-K mode) settings every small-shape test runs under.
+SETTINGS = [
+    ("auto", 0, 0),
+    ("ffma", 1, 1), ("ffma", 1, 3), ("ffma", 2, 2), ("ffma", 3, 0), ("ffma", 2, 3),
+]
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import torch
+
+    assert torch.cuda.is_available()
+    from dense_fp32_matrix_major_gb300 import sgemm
+
+    yield sgemm
+    sgemm.set_variant(0)
+    sgemm.set_tuning(sgemm.SGEMM_TUNE_FFMA_TILE, 0)
+    sgemm.set_tuning(sgemm.SGEMM_TUNE_STREAM_K, 0)
+
+
+def _apply(lib, setting):
+    variant, tile, sk = setting
+    lib.set_variant(variant)
+    lib.set_tuning(lib.SGEMM_TUNE_FFMA_TILE, tile)
+    lib.set_tuning(lib.SGEMM_TUNE_STREAM_K, sk)
+
+
+def _check(A, B, C, flat, ldc, offset=0, exact=False):
+    M, N = C.shape
+    assert outside_box_intact(flat, M, N, ldc, offset), "write outside the M x N box"
+    if exact:
+        ref = (A.astype(np.int64) @ B.astype(np.int64)).astype(np.float32)
+        assert np.array_equal(C, ref)
+    else:
+        err = oracle_error(C, A, B)
+        assert err <= TOL, err
+
+
+TINY = [1, 2, 3, 5, 8, 13, 16, 17]
+
+
+@pytest.mark.parametrize("setting", SETTINGS, ids=lambda s: f"{s[0]}-t{s[1]}-sk{s[2]}")
+def test_tiny_shape_sweep(lib, setting):
+    _apply(lib, setting)
+    for M, N, K in itertools.product(TINY, TINY, TINY):
+        A, B = wl.make_pair(M, N, K, "normal", M * 1000 + N * 10 + K)
+        C, flat, rc = run_sgemm(A, B)
+        assert rc == 0, (M, N, K)
+        _check(A, B, C, flat, max(N, 1))
+
+
+TILE_EDGES = [(63, 65, 15), (64, 64, 16), (65, 63, 17), (127, 255, 31), (128, 256, 33),
+              (129, 257, 47), (1, 300, 100), (300, 1, 100), (200, 3, 1), (33, 257, 513)]
+
+
+@pytest.mark.parametrize("setting", SETTINGS, ids=lambda s: f"{s[0]}-t{s[1]}-sk{s[2]}")
+@pytest.mark.parametrize("M,N,K", TILE_EDGES)
+def test_tile_boundary_crossings(lib, setting, M, N, K):
+    _apply(lib, setting)
+    A, B = wl.make_pair(M, N, K, "uniform", M + N + K)
+    C, flat, rc = run_sgemm(A, B)
+    assert rc == 0
+    _check(A, B, C, flat, N)
+
+
+@pytest.mark.parametrize("setting", SETTINGS, ids=lambda s: f"{s[0]}-t{s[1]}-sk{s[2]}")
+def test_integer_inputs_bit_exact(lib, setting):
+    _apply(lib, setting)
+    for (M, N, K) in [(257, 129, 1000), (64, 300, 4096), (1000, 40, 77)]:
+        A, B = wl.make_pair(M, N, K, "int4", K)
+        C, flat, rc = run_sgemm(A, B)
+        assert rc == 0
+        _check(A, B, C, flat, N, exact=True)
+
+
+@pytest.mark.parametrize("setting", SETTINGS, ids=lambda s: f"{s[0]}-t{s[1]}-sk{s[2]}")
+def test_padded_strides_and_unaligned_pointers(lib, setting):
+    _apply(lib, setting)
+    M, N, K = 150, 270, 90
+    A, B = wl.make_pair(M, N, K, "normal", 21)
+    cases = [
+        dict(lda=K + 6, ldb=N + 2, ldc=N + 10, offsets=(0, 0, 0)),   # padded rows
+        dict(lda=K + 1, ldb=N + 1, ldc=N + 3, offsets=(1, 3, 1)),   # no 16-byte alignment anywhere
+        dict(lda=K, ldb=N + 4, ldc=N + 4, offsets=(2, 4, 8)),        # aligned B and C, odd A
+    ]
+    for case in cases:
+        C, flat, rc = run_sgemm(A, B, **case)
+        assert rc == 0, case
+        _check(A, B, C, flat, case["ldc"], case["offsets"][2])
+
+
+def test_special_cases(lib):
+    _apply(lib, ("auto", 0, 0))
+    # K = 0: the empty sum, C becomes zero.
+    A = np.zeros((5, 0), np.float32)
+    B = np.zeros((0, 7), np.float32)
+    C, flat, rc = run_sgemm(A, B)
+    assert rc == 0 and np.all(C == 0) and outside_box_intact(flat, 5, 7, 7, 0)
+    # M = 0 and N = 0: nothing is written.
+    for (M, N, K) in [(0, 7, 3), (4, 0, 3), (0, 0, 0)]:
+        A = np.ones((M, K), np.float32)
+        B = np.ones((K, N), np.float32)
+        C, flat, rc = run_sgemm(A, B, prefill=np.float32(7777.25))
+        assert rc == 0
+        assert np.all(flat == np.float32(7777.25))
+    # Single nonzero term: one scaled row of B, exactly.
+    A = np.zeros((70, 40), np.float32)
+    A[33, 17] = -0.5
+    B = np.random.default_rng(5).standard_normal((40, 90)).astype(np.float32)
+    C, flat, rc = run_sgemm(A, B)
+    exp = np.zeros((70, 90), np.float32)
+    exp[33] = -0.5 * B[17]
+    assert rc == 0 and np.array_equal(C, exp)
+    # Identity: C == B bit for bit.
+    I = np.eye(300, dtype=np.float32)
+    B = np.random.default_rng(6).standard_normal((300, 200)).astype(np.float32)
+    C, flat, rc = run_sgemm(I, B)
+    assert rc == 0 and np.array_equal(C, B)
+
+
+def test_status_codes_on_device(lib):
+    import torch
+
+    a = torch.zeros(16, device="cuda")
+    # C overlapping A is rejected.
+    assert lib.sgemm_f32_raw(2, 2, 2, a.data_ptr(), 2, a.data_ptr() + 64, 2, a.data_ptr() + 4, 2, 0) == 1
+    assert lib.device_status() == 0
+
+
+# ------------------------------------------------------------- benchmark configs
+
+
+def _config_error(C, A, B, w):
+    if w.M * w.N * w.K <= 1024 ** 3:
+        return oracle_error(C, A, B)
+    # Full sizes beyond the oracle's budget: a band of full rows (every column
+    # tile and the last, ragged one) plus seeded samples over the whole box.
+    band = 32
+    C64, S = oracle.sgemm_f64_rows(A, B, w.M - band, w.M)
+    err_band = oracle.normalized_error(C[w.M - band:], C64, S)
+    r, c = wl.sample_positions(w.M, w.N, 4000, seed=w.seed)
+    return max(err_band, sampled_error(C, A, B, r, c))
+
+
+@pytest.mark.parametrize("w", wl.ALL, ids=lambda w: w.name)
+@pytest.mark.parametrize("variant", ["auto", "ffma"])
+def test_benchmark_configs(lib, w, variant):
+    _apply(lib, (variant, 0, 0))
+    A, B = wl.make_inputs(w)
+    C, flat, rc = run_sgemm(A, B, lda=w.lda, ldb=w.ldb, ldc=w.ldc)
+    assert rc == 0
+    assert outside_box_intact(flat, w.M, w.N, w.ldc or w.N, 0)
+    if w.dist == "ones":
+        assert np.all(C == np.float32(w.K))  # the page's closed form: every output is K
+    else:
+        err = _config_error(C, A, B, w)
+        assert err <= TOL, err
+
+
+def test_from_host_entry_point(lib):
+    import torch
+
+    w = wl.C3_RAGGED
+    A, B = wl.make_inputs(w)
+    Ah = torch.from_numpy(A).pin_memory()
+    Bh = torch.from_numpy(B).pin_memory()
+    Ch = torch.full((w.M, w.N), float("nan")).pin_memory()
+    dA, dB, dC = (torch.empty_like(t, device="cuda") for t in (Ah, Bh, Ch))
+    lib.set_variant(0)
+    lib.sgemm_f32_from_host(Ah, Bh, Ch, dA, dB, dC)
+    torch.cuda.synchronize()
+    r, c = wl.sample_positions(w.M, w.N, 2000, seed=1)
+    assert sampled_error(Ch.numpy(), A, B, r, c) <= TOL
+
+
+def test_repeat_calls_are_stable(lib):
+    """Stream-K adds partial sums with atomics: repeated runs stay within the bound."""
+    _apply(lib, ("ffma", 1, 3))
+    A, B = wl.make_pair(256, 512, 2048, "normal", 77)
+    C64, S = oracle.sgemm_f64_rows(A, B)
+    for _ in range(3):
+        C, flat, rc = run_sgemm(A, B)
+        assert rc == 0
+        assert oracle.normalized_error(C, C64, S) <= TOL
