@@ -79,6 +79,17 @@ int check_args(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, con
     return SGEMM_OK;
 }
 
+// AUTO: the tensor-core path once the product is large enough to fill the
+// GPU with 128 x 256 tiles (measured crossover between 1024^3 and
+// 1023 x 2049 x 1537 on GB300), and only up to K = 8192: its accumulation
+// rounds toward zero, so its error grows with K (2.7e-6 of the 1e-5 bound at
+// K = 4096); beyond that the FFMA path keeps the bound at any K.
+int auto_variant(const Problem &p, const DeviceInfo &dev) {
+    const double work = static_cast<double>(p.M) * static_cast<double>(p.N) * static_cast<double>(p.K);
+    if (work >= 2147483648.0 && p.K <= 8192 && tf32x3_supports(p, dev)) return SGEMM_TF32X3;
+    return SGEMM_FFMA;
+}
+
 int enqueue(const Problem &p, cudaStream_t stream) {
     read_env();
     DeviceInfo dev;
@@ -98,10 +109,10 @@ int enqueue(const Problem &p, cudaStream_t stream) {
         return rc;
     }
     int variant = g_variant.load();
-    if (variant == SGEMM_AUTO) variant = tf32x3_supports(p, dev) ? SGEMM_TF32X3 : SGEMM_FFMA;
+    if (variant == SGEMM_AUTO) variant = auto_variant(p, dev);
     if (variant == SGEMM_TF32X3) {
         if (!tf32x3_supports(p, dev)) return SGEMM_ERR_UNSUPPORTED;
-        rc = tf32x3_launch(p, dev, stream, &launches);
+        rc = tf32x3_launch(p, dev, static_cast<int>(g_tune_sk.load()), stream, &launches);
     } else {
         rc = ffma_launch(p, dev, static_cast<int>(g_tune_tile.load()), static_cast<int>(g_tune_sk.load()),
                          stream, &launches);
@@ -238,8 +249,8 @@ int sgemm_set_tuning(int key, int64_t value) {
             if (value < 0 || value > 3) return SGEMM_ERR_INVALID_ARG;
             sgemm::g_tune_sk.store(value);
             return SGEMM_OK;
-        case SGEMM_TUNE_WATCHDOG_POLLS:
-            return sgemm::watchdog_set_polls(value);
+        case SGEMM_TUNE_WATCHDOG_MS:
+            return sgemm::watchdog_set_ms(value);
         default: return SGEMM_ERR_INVALID_ARG;
     }
 }
@@ -248,7 +259,7 @@ int64_t sgemm_get_tuning(int key) {
     switch (key) {
         case SGEMM_TUNE_FFMA_TILE: return sgemm::g_tune_tile.load();
         case SGEMM_TUNE_STREAM_K: return sgemm::g_tune_sk.load();
-        case SGEMM_TUNE_WATCHDOG_POLLS: return sgemm::watchdog_polls();
+        case SGEMM_TUNE_WATCHDOG_MS: return sgemm::watchdog_ms();
         default: return -1;
     }
 }

@@ -345,16 +345,7 @@ int launch_cfg(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStream_
     const int tiles = static_cast<int>(tiles64);
     const int slots = dev.sm_count * per_sm;
     // A stream-K share below this many k-steps costs more in fix-up than it saves.
-    const int64_t min_share = 8;
-
-    int mode = sk_mode;
-    if (mode == SK_AUTO) {
-        const int rem = tiles % slots;
-        if (tiles >= slots)
-            mode = (rem != 0 && static_cast<int64_t>(rem) * k_tiles >= min_share * slots) ? SK_HYBRID : SK_DP_ONLY;
-        else
-            mode = (tiles * 2 <= slots && k_tiles >= 2 * min_share) ? SK_ALL : SK_DP_ONLY;
-    }
+    const Schedule sch = make_schedule(tiles, k_tiles, slots, sk_mode, 8);
 
     FfmaArgs a;
     a.M = p.M;
@@ -369,23 +360,14 @@ int launch_cfg(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStream_
     a.tiles_n = static_cast<int>(tiles_n);
     a.k_tiles = static_cast<int>(k_tiles);
     a.total_tiles = tiles;
-    int grid = 0;
-    if (mode == SK_DP_ONLY) {
-        a.dp_tiles = tiles;
-        a.sk_iters = 0;
-        a.sk_ctas = 0;
-        grid = std::min(tiles, slots);
-    } else {
-        a.dp_tiles = (mode == SK_ALL) ? 0 : (tiles / slots) * slots;
-        const int split = tiles - a.dp_tiles;
-        a.sk_iters = static_cast<int64_t>(split) * k_tiles;
-        a.sk_ctas = static_cast<int>(std::max<int64_t>(1, min64(slots, a.sk_iters / min_share)));
-        grid = std::max(std::min(a.dp_tiles, slots), a.sk_ctas);
-        if (split > 0) {
-            zero_tiles_kernel<<<split, 256, 0, stream>>>(p.C, p.M, p.N, p.ldc, C::BM, C::BN, a.tiles_n,
-                                                         a.dp_tiles);
-            ++*launches;
-        }
+    a.dp_tiles = sch.dp_tiles;
+    a.sk_iters = sch.sk_iters;
+    a.sk_ctas = sch.sk_ctas;
+    const int grid = sch.grid;
+    if (tiles > sch.dp_tiles) {
+        rc = zero_tiles_launch(p.C, p.M, p.N, p.ldc, C::BM, C::BN, a.tiles_n, sch.dp_tiles, tiles - sch.dp_tiles,
+                               stream, launches);
+        if (rc != SGEMM_OK) return rc;
     }
     ffma_kernel<C, VEC_B, VEC_C><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(a);
     ++*launches;
@@ -424,6 +406,14 @@ int ffma_launch(const Problem &p, const DeviceInfo &dev, int tile, int sk_mode, 
         case FFMA_TILE_64x64: return launch_aligned<CfgSmall>(p, dev, sk_mode, stream, launches);
         default: return SGEMM_ERR_INVALID_ARG;
     }
+}
+
+int zero_tiles_launch(float *C, int64_t M, int64_t N, int64_t ldc, int bm, int bn, int tiles_n, int first_tile,
+                      int count, cudaStream_t stream, int *launches) {
+    if (count <= 0) return SGEMM_OK;
+    zero_tiles_kernel<<<count, 256, 0, stream>>>(C, M, N, ldc, bm, bn, tiles_n, first_tile);
+    ++*launches;
+    return cudaGetLastError() == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
 }
 
 int zero_launch(float *C, int64_t M, int64_t N, int64_t ldc, const DeviceInfo &dev, cudaStream_t stream,

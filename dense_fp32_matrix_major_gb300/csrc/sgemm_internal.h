@@ -34,6 +34,53 @@ int current_device(DeviceInfo *info);
 enum FfmaTile { FFMA_TILE_AUTO = 0, FFMA_TILE_128x256 = 1, FFMA_TILE_128x128 = 2, FFMA_TILE_64x64 = 3 };
 enum StreamKMode { SK_AUTO = 0, SK_DP_ONLY = 1, SK_HYBRID = 2, SK_ALL = 3 };
 
+// Work split of a persistent grid over a tiles x k_steps iteration space:
+// tiles [0, dp_tiles) go whole, round-robin over the CTAs; the rest are split
+// along K into sk_iters (tile, k-step) iterations shared evenly by CTAs
+// [0, sk_ctas) (stream-K). A split tile's outputs are zeroed first and its
+// partial sums added with atomics.
+struct Schedule {
+    int dp_tiles;
+    int sk_ctas;
+    int grid;
+    int64_t sk_iters;
+};
+
+// slots = CTAs that can be resident at once; min_share = fewest k-steps worth
+// giving one stream-K CTA.
+inline Schedule make_schedule(int tiles, int64_t k_steps, int slots, int mode, int64_t min_share) {
+    if (mode == SK_AUTO) {
+        const int rem = tiles % slots;
+        if (tiles >= slots)
+            mode = (rem != 0 && static_cast<int64_t>(rem) * k_steps >= min_share * slots) ? SK_HYBRID
+                                                                                              : SK_DP_ONLY;
+        else
+            mode = (tiles * 2 <= slots && k_steps >= 2 * min_share) ? SK_ALL : SK_DP_ONLY;
+    }
+    Schedule s{};
+    if (mode == SK_DP_ONLY) {
+        s.dp_tiles = tiles;
+        s.sk_iters = 0;
+        s.sk_ctas = 0;
+        s.grid = tiles < slots ? tiles : slots;
+        return s;
+    }
+    s.dp_tiles = (mode == SK_ALL) ? 0 : (tiles / slots) * slots;
+    s.sk_iters = static_cast<int64_t>(tiles - s.dp_tiles) * k_steps;
+    int64_t ctas = s.sk_iters / min_share;
+    if (ctas > slots) ctas = slots;
+    if (ctas < 1) ctas = 1;
+    s.sk_ctas = static_cast<int>(ctas);
+    const int dp_grid = s.dp_tiles < slots ? s.dp_tiles : slots;
+    s.grid = dp_grid > s.sk_ctas ? dp_grid : s.sk_ctas;
+    return s;
+}
+
+// Enqueue a kernel that zeroes the C region of `count` tiles starting at
+// tile `first_tile` of a bm x bn tile grid with tiles_n tiles per row.
+int zero_tiles_launch(float *C, int64_t M, int64_t N, int64_t ldc, int bm, int bn, int tiles_n, int first_tile,
+                      int count, cudaStream_t stream, int *launches);
+
 // Enqueue the FFMA product. `launches` receives the number of kernels enqueued.
 int ffma_launch(const Problem &p, const DeviceInfo &dev, int tile, int sk_mode, cudaStream_t stream,
                 int *launches);
@@ -45,12 +92,13 @@ int zero_launch(float *C, int64_t M, int64_t N, int64_t ldc, const DeviceInfo &d
 // Tensor-core three-term TF32 variant. Returns SGEMM_ERR_UNSUPPORTED when it
 // cannot run the request.
 bool tf32x3_supports(const Problem &p, const DeviceInfo &dev);
-int tf32x3_launch(const Problem &p, const DeviceInfo &dev, cudaStream_t stream, int *launches);
+int tf32x3_launch(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStream_t stream, int *launches);
 
 // Watchdog flag shared by kernels with bounded waits (one per device, in the
 // tf32x3 translation unit). Read-and-clear; returns 0 or the first recorded code.
 int watchdog_read_and_clear(int *code);
-int64_t watchdog_polls();
-int watchdog_set_polls(int64_t polls);
+int64_t watchdog_ms();
+int watchdog_set_ms(int64_t ms);
+int *watchdog_flag_device_ptr();  // device address of the current device's flag, or nullptr
 
 }  // namespace sgemm

@@ -75,6 +75,9 @@ enum sgemm_variant {
  * arithmetic in an order the library chooses; the acceptance bound is
  * max |C - C_exact| / sum_k |A[i][k]| |B[k][j]| <= 1e-5, and inputs whose
  * products and partial sums are integers below 2^24 give exact results.
+ * Non-finite inputs: SGEMM_FFMA follows IEEE arithmetic; SGEMM_TF32X3 gives
+ * NaN where IEEE gives +-inf (its split multiplies an infinite high part by
+ * a zero low part). NaN inputs give NaN in both.
  * Returns SGEMM_OK or an sgemm_status code; on error nothing is enqueued.
  */
 int sgemm_f32(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, const float *B,
@@ -113,9 +116,9 @@ int sgemm_last_launch_count(void);
 const char *sgemm_strerror(int status);
 
 /*
- * Bounded waits. Kernels that wait on an mbarrier or a flag give up after a
- * fixed number of polls, record the event in a per-device flag and return
- * without writing their tile. This call waits for all work on the current
+ * Bounded waits. Kernels that wait on an mbarrier give up after a fixed time
+ * (SGEMM_TUNE_WATCHDOG_MS), record the event in a per-device flag, stop
+ * issuing work and return; C is then incomplete. This call waits for all work on the current
  * device (cudaDeviceSynchronize), then returns SGEMM_ERR_TIMEOUT if a kernel
  * gave up since the last call (and clears the flag), SGEMM_ERR_LAUNCH if the
  * device reported an error, else SGEMM_OK.
@@ -129,14 +132,15 @@ int sgemm_device_status(void);
  *   SGEMM_TUNE_STREAM_K      0 = choose per shape; 1 = data-parallel only;
  *                            2 = data-parallel waves plus a stream-K remainder;
  *                            3 = stream-K over all tiles
- *   SGEMM_TUNE_WATCHDOG_POLLS  polls before a bounded wait gives up (>= 1024)
+ *   SGEMM_TUNE_WATCHDOG_MS   milliseconds a bounded wait polls before it gives
+ *                            up (1 .. 60000; default 2000)
  * Returns SGEMM_OK or SGEMM_ERR_INVALID_ARG. sgemm_get_tuning returns the
  * value, or -1 for an unknown key.
  */
 enum sgemm_tuning_key {
     SGEMM_TUNE_FFMA_TILE = 1,
     SGEMM_TUNE_STREAM_K = 2,
-    SGEMM_TUNE_WATCHDOG_POLLS = 3
+    SGEMM_TUNE_WATCHDOG_MS = 3
 };
 int sgemm_set_tuning(int key, int64_t value);
 int64_t sgemm_get_tuning(int key);

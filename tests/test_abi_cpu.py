@@ -71,7 +71,8 @@ def test_tuning_keys(binding):
     with pytest.raises(binding.SgemmError):
         binding.set_tuning(binding.SGEMM_TUNE_STREAM_K, 9)
     with pytest.raises(binding.SgemmError):
-        binding.set_tuning(binding.SGEMM_TUNE_WATCHDOG_POLLS, 10)
+        binding.set_tuning(binding.SGEMM_TUNE_WATCHDOG_MS, 0)
+    assert binding.get_tuning(binding.SGEMM_TUNE_WATCHDOG_MS) == 2000
 
 
 @pytest.mark.parametrize(

@@ -20,6 +20,7 @@ pytestmark = pytest.mark.gpu
 SETTINGS = [
     ("auto", 0, 0),
     ("ffma", 1, 1), ("ffma", 1, 3), ("ffma", 2, 2), ("ffma", 3, 0), ("ffma", 2, 3),
+    ("tf32x3", 0, 0), ("tf32x3", 0, 1), ("tf32x3", 0, 3),
 ]
 
 
@@ -161,7 +162,7 @@ def _config_error(C, A, B, w):
 
 
 @pytest.mark.parametrize("w", wl.ALL, ids=lambda w: w.name)
-@pytest.mark.parametrize("variant", ["auto", "ffma"])
+@pytest.mark.parametrize("variant", ["auto", "ffma", "tf32x3"])
 def test_benchmark_configs(lib, w, variant):
     _apply(lib, (variant, 0, 0))
     A, B = wl.make_inputs(w)
@@ -200,3 +201,38 @@ def test_repeat_calls_are_stable(lib):
         C, flat, rc = run_sgemm(A, B)
         assert rc == 0
         assert oracle.normalized_error(C, C64, S) <= TOL
+
+
+def test_tf32x3_long_k_margin(lib):
+    """The tensor-core path rounds each accumulation toward zero, so its error
+    grows with K; at K = 8192 it must still meet the bound."""
+    _apply(lib, ("tf32x3", 0, 0))
+    A, B = wl.make_pair(256, 512, 8192, "normal", 88)
+    C, flat, rc = run_sgemm(A, B)
+    assert rc == 0
+    r, c = wl.sample_positions(256, 512, 3000, seed=2)
+    assert sampled_error(C, A, B, r, c) <= TOL
+
+
+def test_nonfinite_inputs_propagate(lib):
+    """Non-finite inputs reach exactly the outputs that use them.
+
+    FFMA follows IEEE arithmetic: an infinity gives +-inf. The three-term TF32
+    split multiplies an infinite high part by the zero low part of the other
+    operand (inf * 0), so there the output is NaN instead of +-inf.
+    """
+    for variant in ("ffma", "tf32x3"):
+        _apply(lib, (variant, 0, 0))
+        A = np.ones((130, 40), np.float32)
+        B = np.ones((40, 260), np.float32)
+        A[5, 3] = np.inf
+        A[77, 0] = np.nan
+        C, flat, rc = run_sgemm(A, B)
+        assert rc == 0
+        if variant == "ffma":
+            assert np.all(np.isposinf(C[5]))
+        else:
+            assert np.all(~np.isfinite(C[5]))
+        assert np.all(np.isnan(C[77]))
+        rest = np.delete(C, [5, 77], axis=0)
+        assert np.all(rest == 40.0)
