@@ -7,12 +7,13 @@
 // optimisation ("CUDA内存优化入门：从Naive到Tiled矩阵乘法", section 八); they
 // give no design for them, and this kernel is not derived from their code.
 //
-// Split. Each fp32 value x becomes hi = tf32(x) (round to nearest, ties
-// away) and lo = tf32(x - hi), where x - hi is exact in fp32. Then
+// Split. Each fp32 value x becomes hi = x truncated to tf32 (sign, exponent,
+// top 10 mantissa bits) and lo = tf32(x - hi), where x - hi is exact in fp32.
+// Then
 //     a*b = hi_a*hi_b + hi_a*lo_b + lo_a*hi_b + lo_a*lo_b,
 // and the kernel sums the first three products on the tensor cores with fp32
-// accumulation. |lo| <= 2^-11 |x|, so the dropped term and the rounding of lo
-// are below 2^-21 |a*b| per product, far inside the 1e-5 acceptance bound on
+// accumulation. |lo| < 2^-10 |x|, so the dropped term (< 2^-20 |a*b|) and the
+// rounding of lo (< 2^-21 |x|) stay far inside the 1e-5 acceptance bound on
 // max |C - C_exact| / sum_k |a_ik||b_kj|. Values with at most 11 significant
 // bits (small integers) have lo = 0 and give exact products.
 //
@@ -21,7 +22,8 @@
 //     lives in TMEM (256 of the 512 columns; two buffers, so the epilogue of
 //     one tile overlaps the main loop of the next).
 //   * Warps 1-8 (producers) read a k-block of A (128 x 32) and B (32 x 256)
-//     from global memory (any alignment; 16-byte loads where A allows), split
+//     from global memory (any alignment; 16-byte loads where the rows allow,
+//     unguarded loads for k-blocks inside the matrices), split
 //     each value, and write four K-major tiles -- A_hi, A_lo, B_hi, B_lo, each
 //     row 32 values = 128 bytes -- into shared memory in the 128-byte swizzled
 //     layout that the tensor core reads (16-byte chunk c of row r stored at
@@ -213,24 +215,33 @@ __device__ __forceinline__ uint32_t tf32_rna_bits(float x) {
     return r;
 }
 
-// hi + lo split of one value (see the header comment). Non-finite inputs
-// pass through in hi with lo = 0; a hi that rounds past the largest float
-// falls back to truncation.
+// hi + lo split of one value: hi keeps the sign, the exponent and the top 10
+// mantissa bits of x (an exact tf32, so it never overflows), and lo is
+// x - hi (exact in fp32) rounded to tf32. Non-finite x gives a NaN lo, so the
+// products that use it are NaN.
 __device__ __forceinline__ void split_tf32(float x, float &hi, float &lo) {
-    if (!isfinite(x)) {
-        hi = x;
-        lo = 0.0f;
-        return;
-    }
-    float h = __uint_as_float(tf32_rna_bits(x));
-    if (!isfinite(h)) h = __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
-    hi = h;
-    lo = __uint_as_float(tf32_rna_bits(x - h));
+    hi = __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
+    lo = __uint_as_float(tf32_rna_bits(x - hi));
 }
+
+__device__ __forceinline__ void split_store(uint32_t hi_addr, uint32_t lo_addr, float a, float b, float c,
+                                            float d);
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, float a, float b, float c, float d) {
     asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
                  : "memory");
+}
+
+// Split four values and store the high parts at hi_addr, the low parts at lo_addr.
+__device__ __forceinline__ void split_store(uint32_t hi_addr, uint32_t lo_addr, float a, float b, float c,
+                                            float d) {
+    float h0, h1, h2, h3, l0, l1, l2, l3;
+    split_tf32(a, h0, l0);
+    split_tf32(b, h1, l1);
+    split_tf32(c, h2, l2);
+    split_tf32(d, h3, l3);
+    st_shared_v4(hi_addr, h0, h1, h2, h3);
+    st_shared_v4(lo_addr, l0, l1, l2, l3);
 }
 
 // Byte offset of 16-byte chunk `chunk` of row `row` in a 128-byte-swizzled tile.
@@ -260,7 +271,7 @@ __device__ __forceinline__ void for_each_unit(const Args &a, volatile int *abort
     }
 }
 
-template <bool VEC_A, bool VEC_C>
+template <bool VEC_A, bool VEC_B, bool VEC_C>
 __global__ void __launch_bounds__(THREADS, 1) tf32x3_kernel(const Args a) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -342,51 +353,102 @@ __global__ void __launch_bounds__(THREADS, 1) tf32x3_kernel(const Args a) {
     } else if (warp <= PRODUCER_WARPS) {
         // -------------------------------------------------------------- producers
         const int pt = threadIdx.x - 32;  // 0 .. PRODUCER_THREADS-1
+        // A: task r is row r*32 + pt/8, 16-byte chunk pt%8 (8 lanes = one row).
+        const int a_row0 = pt >> 3, a_ch = pt & 7;
+        const uint32_t a_off0 = sw128_offset(a_row0, a_ch);  // + r * 32 rows * 128 B
+        // B with 16-byte loads: task r covers B rows 4c..4c+3 (c = pt%8) and
+        // columns 4g..4g+3 (g = pt/8 + 32r); a quarter-warp shares g and spans
+        // the 8 chunks, so its swizzled stores hit 8 distinct bank groups.
+        const int b_c = pt & 7, b_g0 = pt >> 3;
         uint32_t it = 0;
         bool ok = true;
         for_each_unit(a, abort_flag, [&](int tile, int kb, int ke) {
             if (!ok) return;
             const int64_t m0 = static_cast<int64_t>(tile / a.tiles_n) * BM;
             const int64_t n0 = static_cast<int64_t>(tile % a.tiles_n) * BN;
+            const bool full_mn = (m0 + BM <= a.M) && (n0 + BN <= a.N);
+            const float *a_base = a.A + (m0 + a_row0) * a.lda + a_ch * 4;
+            const float *b_base = VEC_B ? a.B + static_cast<int64_t>(4 * b_c) * a.ldb + n0 + 4 * b_g0
+                                        : a.B + n0 + pt;
             for (int kblk = kb; kblk < ke; ++kblk, ++it) {
                 const int s = it & 1;
                 const int64_t k0 = static_cast<int64_t>(kblk) * BK;
+                const bool interior = full_mn && (k0 + BK <= a.K);
                 // Loads first (all in flight together), then split and store.
-                float4 av[A_TASKS / PRODUCER_THREADS];
-                float4 bv[B_TASKS / PRODUCER_THREADS];
+                float4 av[4], bv[8];
+                if (interior) {
 #pragma unroll
-                for (int r = 0; r < A_TASKS / PRODUCER_THREADS; ++r) {
-                    const int t = r * PRODUCER_THREADS + pt;
-                    const int row = t >> 3, ch = t & 7;
-                    const int64_t gm = m0 + row, gk = k0 + ch * 4;
-                    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-                    if (gm < a.M) {
-                        const float *src = a.A + gm * a.lda + gk;
-                        if (VEC_A && gk + 3 < a.K) {
-                            v = __ldg(reinterpret_cast<const float4 *>(src));
+                    for (int r = 0; r < 4; ++r) {
+                        const float *src = a_base + static_cast<int64_t>(r * 32) * a.lda + k0;
+                        if (VEC_A) {
+                            av[r] = __ldg(reinterpret_cast<const float4 *>(src));
                         } else {
+                            av[r] = make_float4(__ldg(src), __ldg(src + 1), __ldg(src + 2), __ldg(src + 3));
+                        }
+                    }
+                    if (VEC_B) {
+#pragma unroll
+                        for (int r = 0; r < 2; ++r)
+#pragma unroll
+                            for (int q = 0; q < 4; ++q)
+                                bv[r * 4 + q] = __ldg(reinterpret_cast<const float4 *>(
+                                    b_base + (k0 + q) * a.ldb + 128 * r));
+                    } else {
+#pragma unroll
+                        for (int r = 0; r < 8; ++r) {
+                            const float *src = b_base + (k0 + 4 * r) * a.ldb;
+                            bv[r] = make_float4(__ldg(src), __ldg(src + a.ldb), __ldg(src + 2 * a.ldb),
+                                                __ldg(src + 3 * a.ldb));
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        const int64_t gm = m0 + a_row0 + r * 32, gk = k0 + a_ch * 4;
+                        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                        if (gm < a.M) {
+                            const float *src = a.A + gm * a.lda + gk;
                             if (gk + 0 < a.K) v.x = __ldg(src + 0);
                             if (gk + 1 < a.K) v.y = __ldg(src + 1);
                             if (gk + 2 < a.K) v.z = __ldg(src + 2);
                             if (gk + 3 < a.K) v.w = __ldg(src + 3);
                         }
+                        av[r] = v;
                     }
-                    av[r] = v;
-                }
+                    if (VEC_B) {
 #pragma unroll
-                for (int r = 0; r < B_TASKS / PRODUCER_THREADS; ++r) {
-                    const int t = r * PRODUCER_THREADS + pt;
-                    const int n = t & (BN - 1), ch = t / BN;
-                    const int64_t gn = n0 + n, gk = k0 + ch * 4;
-                    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-                    if (gn < a.N) {
-                        const float *src = a.B + gk * a.ldb + gn;
-                        if (gk + 0 < a.K) v.x = __ldg(src);
-                        if (gk + 1 < a.K) v.y = __ldg(src + a.ldb);
-                        if (gk + 2 < a.K) v.z = __ldg(src + 2 * a.ldb);
-                        if (gk + 3 < a.K) v.w = __ldg(src + 3 * a.ldb);
+                        for (int r = 0; r < 2; ++r)
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                const int64_t gk = k0 + 4 * b_c + q, gn = n0 + 4 * (b_g0 + 32 * r);
+                                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                                if (gk < a.K) {
+                                    const float *src = a.B + gk * a.ldb + gn;
+                                    if (gn + 3 < a.N) {
+                                        v = __ldg(reinterpret_cast<const float4 *>(src));
+                                    } else {
+                                        if (gn + 0 < a.N) v.x = __ldg(src + 0);
+                                        if (gn + 1 < a.N) v.y = __ldg(src + 1);
+                                        if (gn + 2 < a.N) v.z = __ldg(src + 2);
+                                    }
+                                }
+                                bv[r * 4 + q] = v;
+                            }
+                    } else {
+#pragma unroll
+                        for (int r = 0; r < 8; ++r) {
+                            const int64_t gn = n0 + pt, gk = k0 + 4 * r;
+                            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                            if (gn < a.N) {
+                                const float *src = a.B + gk * a.ldb + gn;
+                                if (gk + 0 < a.K) v.x = __ldg(src);
+                                if (gk + 1 < a.K) v.y = __ldg(src + a.ldb);
+                                if (gk + 2 < a.K) v.z = __ldg(src + 2 * a.ldb);
+                                if (gk + 3 < a.K) v.w = __ldg(src + 3 * a.ldb);
+                            }
+                            bv[r] = v;
+                        }
                     }
-                    bv[r] = v;
                 }
                 if (!mbar_wait(bar(2 + s), ((it >> 1) & 1) ^ 1, a, abort_flag, WD_PRODUCER)) {
                     ok = false;
@@ -394,30 +456,34 @@ __global__ void __launch_bounds__(THREADS, 1) tf32x3_kernel(const Args a) {
                 }
                 const uint32_t st = base + static_cast<uint32_t>(s * STAGE_BYTES);
 #pragma unroll
-                for (int r = 0; r < A_TASKS / PRODUCER_THREADS; ++r) {
-                    const int t = r * PRODUCER_THREADS + pt;
-                    const int row = t >> 3, ch = t & 7;
-                    float h0, h1, h2, h3, l0, l1, l2, l3;
-                    split_tf32(av[r].x, h0, l0);
-                    split_tf32(av[r].y, h1, l1);
-                    split_tf32(av[r].z, h2, l2);
-                    split_tf32(av[r].w, h3, l3);
-                    const uint32_t off = sw128_offset(row, ch);
-                    st_shared_v4(st + off, h0, h1, h2, h3);
-                    st_shared_v4(st + A_TILE + off, l0, l1, l2, l3);
+                for (int r = 0; r < 4; ++r) {
+                    const uint32_t off = a_off0 + static_cast<uint32_t>(r * 32 * 128);
+                    split_store(st + off, st + A_TILE + off, av[r].x, av[r].y, av[r].z, av[r].w);
                 }
+                const uint32_t bh = st + 2 * A_TILE, bl = bh + B_TILE;
+                if (VEC_B) {
+                    // bv[r*4 + q] holds B row 4c+q, columns 4g..4g+3: column j of
+                    // that 4 x 4 block is chunk c of tile row 4g + j.
 #pragma unroll
-                for (int r = 0; r < B_TASKS / PRODUCER_THREADS; ++r) {
-                    const int t = r * PRODUCER_THREADS + pt;
-                    const int n = t & (BN - 1), ch = t / BN;
-                    float h0, h1, h2, h3, l0, l1, l2, l3;
-                    split_tf32(bv[r].x, h0, l0);
-                    split_tf32(bv[r].y, h1, l1);
-                    split_tf32(bv[r].z, h2, l2);
-                    split_tf32(bv[r].w, h3, l3);
-                    const uint32_t off = sw128_offset(n, ch);
-                    st_shared_v4(st + 2 * A_TILE + off, h0, h1, h2, h3);
-                    st_shared_v4(st + 2 * A_TILE + B_TILE + off, l0, l1, l2, l3);
+                    for (int r = 0; r < 2; ++r) {
+                        const int g = b_g0 + 32 * r;
+                        const float4 q0 = bv[r * 4 + 0], q1 = bv[r * 4 + 1], q2 = bv[r * 4 + 2], q3 = bv[r * 4 + 3];
+                        uint32_t off = sw128_offset(4 * g + 0, b_c);
+                        split_store(bh + off, bl + off, q0.x, q1.x, q2.x, q3.x);
+                        off = sw128_offset(4 * g + 1, b_c);
+                        split_store(bh + off, bl + off, q0.y, q1.y, q2.y, q3.y);
+                        off = sw128_offset(4 * g + 2, b_c);
+                        split_store(bh + off, bl + off, q0.z, q1.z, q2.z, q3.z);
+                        off = sw128_offset(4 * g + 3, b_c);
+                        split_store(bh + off, bl + off, q0.w, q1.w, q2.w, q3.w);
+                    }
+                } else {
+                    // bv[r] holds B rows 4r..4r+3 of column pt: chunk r of tile row pt.
+#pragma unroll
+                    for (int r = 0; r < 8; ++r) {
+                        const uint32_t off = sw128_offset(pt, r);
+                        split_store(bh + off, bl + off, bv[r].x, bv[r].y, bv[r].z, bv[r].w);
+                    }
                 }
                 fence_proxy_async_smem();  // generic-proxy stores -> visible to the tensor core
                 mbar_arrive(bar(s));
@@ -474,13 +540,13 @@ __global__ void __launch_bounds__(THREADS, 1) tf32x3_kernel(const Args a) {
 }
 
 constexpr int kMaxDevices = 64;
-std::once_flag g_attr_once[kMaxDevices][4];
-cudaError_t g_attr_err[kMaxDevices][4];
+std::once_flag g_attr_once[kMaxDevices][8];
+cudaError_t g_attr_err[kMaxDevices][8];
 
-template <bool VEC_A, bool VEC_C>
+template <bool VEC_A, bool VEC_B, bool VEC_C>
 int launch(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStream_t stream, int *launches) {
-    constexpr int idx = (VEC_A ? 2 : 0) + (VEC_C ? 1 : 0);
-    auto kernel = tf32x3_kernel<VEC_A, VEC_C>;
+    constexpr int idx = (VEC_A ? 4 : 0) + (VEC_B ? 2 : 0) + (VEC_C ? 1 : 0);
+    auto kernel = tf32x3_kernel<VEC_A, VEC_B, VEC_C>;
     std::call_once(g_attr_once[dev.device][idx], [&] {
         g_attr_err[dev.device][idx] =
             cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
@@ -582,11 +648,19 @@ bool tf32x3_supports(const Problem &p, const DeviceInfo &dev) {
 int tf32x3_launch(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStream_t stream, int *launches) {
     if (!tf32x3_supports(p, dev) || dev.device < 0 || dev.device >= kMaxDevices) return SGEMM_ERR_UNSUPPORTED;
     const bool va = (p.lda % 4 == 0) && (reinterpret_cast<uintptr_t>(p.A) % 16 == 0);
+    const bool vb = (p.ldb % 4 == 0) && (reinterpret_cast<uintptr_t>(p.B) % 16 == 0);
     const bool vc = (p.ldc % 4 == 0) && (reinterpret_cast<uintptr_t>(p.C) % 16 == 0);
-    if (va && vc) return launch<true, true>(p, dev, sk_mode, stream, launches);
-    if (va) return launch<true, false>(p, dev, sk_mode, stream, launches);
-    if (vc) return launch<false, true>(p, dev, sk_mode, stream, launches);
-    return launch<false, false>(p, dev, sk_mode, stream, launches);
+    const int idx = (va ? 4 : 0) + (vb ? 2 : 0) + (vc ? 1 : 0);
+    switch (idx) {
+        case 0: return launch<false, false, false>(p, dev, sk_mode, stream, launches);
+        case 1: return launch<false, false, true>(p, dev, sk_mode, stream, launches);
+        case 2: return launch<false, true, false>(p, dev, sk_mode, stream, launches);
+        case 3: return launch<false, true, true>(p, dev, sk_mode, stream, launches);
+        case 4: return launch<true, false, false>(p, dev, sk_mode, stream, launches);
+        case 5: return launch<true, false, true>(p, dev, sk_mode, stream, launches);
+        case 6: return launch<true, true, false>(p, dev, sk_mode, stream, launches);
+        default: return launch<true, true, true>(p, dev, sk_mode, stream, launches);
+    }
 }
 
 }  // namespace sgemm
