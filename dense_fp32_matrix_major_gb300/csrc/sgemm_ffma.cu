@@ -58,9 +58,10 @@ struct FfmaArgs {
     int sk_ctas;       // CTAs [0, sk_ctas) share the split iterations evenly
 };
 
-template <int WARPS_M_, int WARPS_N_, int CN_, int STAGES_, int MIN_BLOCKS_>
+template <int WARPS_M_, int WARPS_N_, int CN_, int STAGES_, int MIN_BLOCKS_, int KU_>
 struct Cfg {
     static constexpr int WARPS_M = WARPS_M_, WARPS_N = WARPS_N_, CN = CN_, STAGES = STAGES_;
+    static constexpr int KU = KU_;  // k-steps unrolled per pass of the inner loop (8 or 16)
     static constexpr int MIN_BLOCKS = MIN_BLOCKS_;  // resident CTAs per SM the registers must allow
     static constexpr int BK = 16;
     static constexpr int THREADS = 32 * WARPS_M * WARPS_N;
@@ -79,9 +80,9 @@ struct Cfg {
     static_assert(BK * BN / 4 % THREADS == 0, "B tile must split evenly over threads");
 };
 
-using CfgBig = Cfg<2, 4, 4, 4, 1>;    // 128 x 256, 256 threads, 8 x 16 per thread
-using CfgMid = Cfg<2, 4, 2, 4, 2>;    // 128 x 128, 256 threads, 8 x 8 per thread
-using CfgSmall = Cfg<1, 2, 2, 3, 6>;  // 64 x 64, 64 threads, 8 x 8 per thread
+using CfgBig = Cfg<2, 4, 4, 4, 1, 8>;     // 128 x 256, 256 threads, 8 x 16 per thread
+using CfgMid = Cfg<2, 4, 2, 4, 2, 16>;    // 128 x 128, 256 threads, 8 x 8 per thread
+using CfgSmall = Cfg<1, 2, 2, 3, 6, 16>;  // 64 x 64, 64 threads, 8 x 8 per thread
 
 __host__ __device__ __forceinline__ int64_t min64(int64_t x, int64_t y) { return x < y ? x : y; }
 
@@ -194,13 +195,19 @@ __device__ __forceinline__ void process_tile(const FfmaArgs &a, float *As, float
         }
         const float *as = As + (t % S) * C::A_STAGE;
         const float *bs = Bs + (t % S) * C::B_STAGE;
+        // Rolled passes of KU unrolled k-steps. With the 8 x 16 register tile a
+        // full unroll of BK = 16 overflows the instruction cache, so that
+        // configuration runs two passes of 8; the swizzle term
+        // ((k8 + kk) & 7 = kk & 7) stays a compile-time constant.
+#pragma unroll 1
+        for (int k8 = 0; k8 < BK; k8 += C::KU)
 #pragma unroll
-        for (int kk = 0; kk < BK; ++kk) {
+        for (int kk = 0; kk < C::KU; ++kk) {
             float av[8], bv[TN];
 #pragma unroll
             for (int g = 0; g < 2; ++g) {
-                const float4 v =
-                    *reinterpret_cast<const float4 *>(as + as_index<C>(kk, wm0 + g * 32 + tm * 4));
+                const float4 v = *reinterpret_cast<const float4 *>(
+                    as + (k8 + kk) * C::BM + ((wm0 + g * 32 + tm * 4) ^ ((kk & 7) << 2)));
                 av[g * 4 + 0] = v.x;
                 av[g * 4 + 1] = v.y;
                 av[g * 4 + 2] = v.z;
@@ -208,7 +215,8 @@ __device__ __forceinline__ void process_tile(const FfmaArgs &a, float *As, float
             }
 #pragma unroll
             for (int c = 0; c < C::CN; ++c) {
-                const float4 v = *reinterpret_cast<const float4 *>(bs + kk * C::BN + wn0 + c * 16 + tn * 4);
+                const float4 v =
+                    *reinterpret_cast<const float4 *>(bs + (k8 + kk) * C::BN + wn0 + c * 16 + tn * 4);
                 bv[c * 4 + 0] = v.x;
                 bv[c * 4 + 1] = v.y;
                 bv[c * 4 + 2] = v.z;

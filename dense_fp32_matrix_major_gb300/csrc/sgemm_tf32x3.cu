@@ -41,6 +41,8 @@
 //     records the event in a device flag and in a CTA abort flag, every role
 //     stops issuing work, the MMA thread waits (bounded) for its own MMAs to
 //     drain, and the CTA frees its TMEM and exits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -58,6 +60,7 @@ __device__ int g_watchdog_code;
 namespace {
 
 std::atomic<int64_t> g_watchdog_ms{2000};
+std::atomic<int> g_use_tma{1};  // TMA variant when the alignment allows it
 
 constexpr int BM = 128, BN = 256, BK = 32;  // BK fp32 = 128 bytes = one swizzle row
 constexpr int STAGES = 2;
@@ -108,6 +111,8 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
            (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
            (static_cast<uint64_t>(2) << 61);
 }
+
+__device__ __forceinline__ uint32_t tf32_rna_bits(float x);
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -176,6 +181,35 @@ __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a_desc, uint64_
         "}\n" ::"r"(d_tmem),
         "l"(a_desc), "l"(b_desc), "r"(kIdesc), "r"(accumulate)
         : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+// 2-D tiled TMA load of the box at (x, y) (x innermost, in elements) into
+// shared memory, completing `bytes` of transactions on the mbarrier.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
+            "r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ float4 ld_shared_v4(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+
+// Low part of a value whose high part the tensor core takes by truncation.
+__device__ __forceinline__ float lo_of(float x) {
+    const float hi = __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
+    return __uint_as_float(tf32_rna_bits(x - hi));
 }
 
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
@@ -539,6 +573,271 @@ __global__ void __launch_bounds__(THREADS, 1) tf32x3_kernel(const Args a) {
     }
 }
 
+
+// ---------------------------------------------------------------------------
+// TMA variant, for A and B whose base addresses and row strides are 16-byte
+// aligned. The tensor core reads an fp32 value of a kind::tf32 operand as its
+// truncation to tf32, so a raw tile can serve as the high part:
+//   * TMA copies the A tile (K-major, as stored) straight into the stage in
+//     the 128-byte swizzled layout: that is A's high part. Converter warps add
+//     A's low part chunk for chunk at the same offsets.
+//   * B is stored N-contiguous, and the operand must be K-major, so TMA copies
+//     the raw B tile (32 rows of K x 256 of N, unswizzled) into a staging
+//     buffer; converter warps read it in 4 x 4 blocks and write B's high and
+//     low parts transposed into the stage. Lane l of each group of eight
+//     takes column block g = g0 + l and k-chunk c = (l + s) mod 8, which keeps
+//     both the staging reads and the swizzled stores free of bank conflicts.
+//     The staging buffer is released as soon as its values are in registers.
+// Out-of-range elements arrive as zeros from TMA.
+//   warp 0: MMA issuer; warp 1: TMA issuer; warps 2-9: converters;
+//   warps 10-13: epilogue.
+// Shared memory: two 96 KB stages (A raw = hi | A lo | B hi | B lo) and the
+// 32 KB B staging buffer.
+namespace tma {
+
+constexpr int CONV_WARPS = 8;
+constexpr int CONV_THREADS = 32 * CONV_WARPS;
+constexpr int EPI_WARP0 = 2 + CONV_WARPS;
+constexpr int THREADS = 32 * (EPI_WARP0 + EPILOGUE_WARPS);
+constexpr int A_RAW = 0, A_LO = A_TILE, B_HI = 2 * A_TILE, B_LO = 2 * A_TILE + B_TILE;
+constexpr int STAGING = STAGES * STAGE_BYTES;  // B raw: BK rows x BN floats
+constexpr int STAGING_BYTES = BK * BN * 4;
+constexpr int BAR_OFFSET = STAGING + STAGING_BYTES;
+constexpr int SMEM_BYTES = BAR_OFFSET + BAR_BYTES + 1024;
+constexpr int A_CHUNKS = A_TILE / 16;
+static_assert(A_CHUNKS % CONV_THREADS == 0, "even converter split of A");
+static_assert((BN / 4) * (BK / 4) == 2 * CONV_THREADS, "two 4 x 4 B blocks per converter thread");
+static_assert(BK == 32 && BN % 32 == 0, "diagonal mapping assumes 8 k-chunks");
+
+}  // namespace tma
+
+template <bool VEC_C>
+__global__ void __launch_bounds__(tma::THREADS, 1)
+    tf32x3_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const Args a) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *smem = smem_raw + (base - raw);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + tma::BAR_OFFSET);
+    // [0..1] a_full (TMA of A), [2..3] empty (MMA done with the stage),
+    // [4..5] acc_full, [6..7] acc_empty, [8] drain, [9..10] op_full
+    // (converters done), [11] b_staged (TMA of B), [12] staging free
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + 13);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 14);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    auto bar = [&](int i) { return smem_u32(bars + i); };
+    const uint32_t staging = base + tma::STAGING;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(bar(s), 1);
+            mbar_init(bar(2 + s), 1);
+            mbar_init(bar(9 + s), tma::CONV_THREADS);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar(4 + b), 1);
+            mbar_init(bar(6 + b), 32 * EPILOGUE_WARPS);
+        }
+        mbar_init(bar(8), 1);
+        mbar_init(bar(11), 1);
+        mbar_init(bar(12), tma::CONV_THREADS);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(tmem_holder)),
+                     "r"(TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            uint32_t it = 0, unit = 0;
+            for_each_unit(a, abort_flag, [&](int, int kb, int ke) {
+                const int buf = unit & 1;
+                if (!mbar_wait(bar(6 + buf), ((unit >> 1) & 1) ^ 1, a, abort_flag, WD_MMA_ACC)) return;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
+                for (int kblk = kb; kblk < ke; ++kblk, ++it) {
+                    const int s = it & 1;
+                    const uint32_t ph = (it >> 1) & 1;
+                    if (!mbar_wait(bar(9 + s), ph, a, abort_flag, WD_MMA_FULL)) return;
+                    if (!mbar_wait(bar(s), ph, a, abort_flag, WD_MMA_FULL)) return;
+                    tc_fence_after();
+                    const uint32_t st = base + static_cast<uint32_t>(s * STAGE_BYTES);
+                    const uint64_t a_hi = sw128_desc(st + tma::A_RAW), a_lo = sw128_desc(st + tma::A_LO);
+                    const uint64_t b_hi = sw128_desc(st + tma::B_HI), b_lo = sw128_desc(st + tma::B_LO);
+#pragma unroll
+                    for (int ks = 0; ks < BK / 8; ++ks) {
+                        const uint64_t adv = static_cast<uint64_t>(ks * 2);  // 32 bytes along K
+                        const uint32_t first = (kblk == kb && ks == 0) ? 0u : 1u;
+                        tc_mma(d_tmem, a_lo + adv, b_hi + adv, first);
+                        tc_mma(d_tmem, a_hi + adv, b_lo + adv, 1u);
+                        tc_mma(d_tmem, a_hi + adv, b_hi + adv, 1u);
+                    }
+                    tc_commit(bar(2 + s));
+                }
+                tc_commit(bar(4 + buf));
+                ++unit;
+            });
+            tc_commit(bar(8));
+            const bool was_aborted = *abort_flag != 0;
+            if (!mbar_wait(bar(8), 0, a, abort_flag, WD_DRAIN) && was_aborted) {
+                const uint64_t t0 = global_timer();
+                while (!mbar_try_wait(bar(8), 0) && global_timer() - t0 < a.timeout_ns) {
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ TMA issuer
+        if (lane == 0) {
+            uint32_t it = 0;
+            bool ok = true;
+            for_each_unit(a, abort_flag, [&](int tile, int kb, int ke) {
+                if (!ok) return;
+                const int m0 = (tile / a.tiles_n) * BM;
+                const int n0 = (tile % a.tiles_n) * BN;
+                for (int kblk = kb; kblk < ke; ++kblk, ++it) {
+                    const int s = it & 1;
+                    const int k0 = kblk * BK;
+                    // B into the staging buffer once the converters have read the last one.
+                    if (!mbar_wait(bar(12), (it & 1) ^ 1, a, abort_flag, WD_PRODUCER)) {
+                        ok = false;
+                        return;
+                    }
+                    mbar_arrive_expect_tx(bar(11), tma::STAGING_BYTES);
+                    tma_load_2d(staging, &tmB, n0, k0, bar(11));
+                    // A straight into the stage once the MMA is done with it.
+                    if (!mbar_wait(bar(2 + s), ((it >> 1) & 1) ^ 1, a, abort_flag, WD_PRODUCER)) {
+                        ok = false;
+                        return;
+                    }
+                    mbar_arrive_expect_tx(bar(s), A_TILE);
+                    tma_load_2d(base + static_cast<uint32_t>(s * STAGE_BYTES) + tma::A_RAW, &tmA, k0, m0, bar(s));
+                }
+            });
+        }
+    } else if (warp < tma::EPI_WARP0) {
+        // ------------------------------------------------------------ converters
+        const int ct = threadIdx.x - 64;
+        const int l = ct & 7, quarter = ct >> 3;  // 32 groups of eight lanes
+        uint32_t it = 0;
+        bool ok = true;
+        for_each_unit(a, abort_flag, [&](int, int kb, int ke) {
+            if (!ok) return;
+            for (int kblk = kb; kblk < ke; ++kblk, ++it) {
+                const int s = it & 1;
+                // B: two 4 x 4 blocks per thread from the staging buffer.
+                if (!mbar_wait(bar(11), it & 1, a, abort_flag, WD_PRODUCER)) {
+                    ok = false;
+                    return;
+                }
+                float4 bv[2][4];
+                int bg[2], bc[2];
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    const int tb = quarter * 2 + r;  // 0..63
+                    const int g = (tb >> 3) * 8 + l, c = (l + tb) & 7;
+                    bg[r] = g;
+                    bc[r] = c;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        bv[r][q] = ld_shared_v4(staging + static_cast<uint32_t>((4 * c + q) * BN * 4 + g * 16));
+                }
+                // The next TMA (async proxy) overwrites what these generic loads
+                // read: order them first, then release the staging buffer.
+                fence_proxy_async_smem();
+                mbar_arrive(bar(12));
+                if (!mbar_wait(bar(s), (it >> 1) & 1, a, abort_flag, WD_PRODUCER)) {
+                    ok = false;
+                    return;
+                }
+                const uint32_t st = base + static_cast<uint32_t>(s * STAGE_BYTES);
+                float4 av[tma::A_CHUNKS / tma::CONV_THREADS];
+#pragma unroll
+                for (int r = 0; r < tma::A_CHUNKS / tma::CONV_THREADS; ++r)
+                    av[r] = ld_shared_v4(st + tma::A_RAW + (r * tma::CONV_THREADS + ct) * 16);
+#pragma unroll
+                for (int r = 0; r < tma::A_CHUNKS / tma::CONV_THREADS; ++r)
+                    st_shared_v4(st + tma::A_LO + (r * tma::CONV_THREADS + ct) * 16, lo_of(av[r].x), lo_of(av[r].y),
+                                 lo_of(av[r].z), lo_of(av[r].w));
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    // bv[r][q] = B row 4c+q, columns 4g..4g+3; column j of the block is
+                    // chunk c of operand row 4g + j.
+                    const float4 q0 = bv[r][0], q1 = bv[r][1], q2 = bv[r][2], q3 = bv[r][3];
+                    const int g = bg[r], c = bc[r];
+                    uint32_t off = sw128_offset(4 * g + 0, c);
+                    split_store(st + tma::B_HI + off, st + tma::B_LO + off, q0.x, q1.x, q2.x, q3.x);
+                    off = sw128_offset(4 * g + 1, c);
+                    split_store(st + tma::B_HI + off, st + tma::B_LO + off, q0.y, q1.y, q2.y, q3.y);
+                    off = sw128_offset(4 * g + 2, c);
+                    split_store(st + tma::B_HI + off, st + tma::B_LO + off, q0.z, q1.z, q2.z, q3.z);
+                    off = sw128_offset(4 * g + 3, c);
+                    split_store(st + tma::B_HI + off, st + tma::B_LO + off, q0.w, q1.w, q2.w, q3.w);
+                }
+                fence_proxy_async_smem();
+                mbar_arrive(bar(9 + s));
+            }
+        });
+    } else {
+        // -------------------------------------------------------------- epilogue
+        const int q = warp & 3;
+        uint32_t unit = 0;
+        for_each_unit(a, abort_flag, [&](int tile, int kb, int ke) {
+            const int buf = unit & 1;
+            if (!mbar_wait(bar(4 + buf), (unit >> 1) & 1, a, abort_flag, WD_EPILOGUE)) return;
+            tc_fence_after();
+            const int64_t m0 = static_cast<int64_t>(tile / a.tiles_n) * BM;
+            const int64_t n0 = static_cast<int64_t>(tile % a.tiles_n) * BN;
+            const int64_t row = m0 + q * 32 + lane;
+            const bool atomic = !(kb == 0 && ke == a.k_blocks);
+            float *crow = a.C + row * a.ldc;
+#pragma unroll 1
+            for (int ch = 0; ch < BN / 32; ++ch) {
+                float v[32];
+                tmem_load32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * BN + ch * 32),
+                            v);
+                const int64_t col0 = n0 + ch * 32;
+                if (row < a.M && col0 < a.N) {
+                    if (atomic) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (col0 + j < a.N) atomicAdd(crow + col0 + j, v[j]);
+                    } else if (VEC_C && col0 + 31 < a.N) {
+#pragma unroll
+                        for (int j = 0; j < 32; j += 4)
+                            *reinterpret_cast<float4 *>(crow + col0 + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (col0 + j < a.N) crow[col0 + j] = v[j];
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(bar(6 + buf));
+            ++unit;
+        });
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) {
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS)
+                     : "memory");
+    }
+}
+
 constexpr int kMaxDevices = 64;
 std::once_flag g_attr_once[kMaxDevices][8];
 cudaError_t g_attr_err[kMaxDevices][8];
@@ -588,6 +887,94 @@ int launch(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStream_t st
     a.timeout_ns = static_cast<uint64_t>(g_watchdog_ms.load()) * 1000000ull;
     a.watchdog = flag;
     kernel<<<sch.grid, THREADS, SMEM_BYTES, stream>>>(a);
+    ++*launches;
+    return cudaGetLastError() == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
+}
+
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+        else
+            cudaGetLastError();
+    });
+    return fn;
+}
+
+// Row-major rows x cols fp32 matrix with row stride ld (elements), boxes of
+// box_cols x box_rows, out-of-range elements read as zero.
+bool encode_map(CUtensorMap *map, const float *ptr, int64_t rows, int64_t cols, int64_t ld, uint32_t box_cols,
+                uint32_t box_rows, CUtensorMapSwizzle swizzle) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * sizeof(float)};
+    const cuuint32_t box[2] = {box_cols, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(ptr), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// TMA requirements: 16-byte aligned bases and row strides, coordinates that
+// fit int32.
+bool tma_ok(const Problem &p) {
+    return (reinterpret_cast<uintptr_t>(p.A) % 16 == 0) && (reinterpret_cast<uintptr_t>(p.B) % 16 == 0) &&
+           (p.lda % 4 == 0) && (p.ldb % 4 == 0) && p.M < INT32_MAX / 2 && p.N < INT32_MAX / 2 &&
+           p.K < INT32_MAX / 2 && tensor_map_encoder() != nullptr;
+}
+
+std::once_flag g_tma_attr_once[kMaxDevices][2];
+cudaError_t g_tma_attr_err[kMaxDevices][2];
+
+template <bool VEC_C>
+int launch_tma(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStream_t stream, int *launches) {
+    auto kernel = tf32x3_tma_kernel<VEC_C>;
+    std::call_once(g_tma_attr_once[dev.device][VEC_C ? 1 : 0], [&] {
+        g_tma_attr_err[dev.device][VEC_C ? 1 : 0] =
+            cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, tma::SMEM_BYTES);
+    });
+    if (g_tma_attr_err[dev.device][VEC_C ? 1 : 0] != cudaSuccess) {
+        cudaGetLastError();
+        return SGEMM_ERR_LAUNCH;
+    }
+    int *flag = watchdog_flag_device_ptr();
+    if (!flag) return SGEMM_ERR_LAUNCH;
+    alignas(64) CUtensorMap mapA, mapB;
+    if (!encode_map(&mapA, p.A, p.M, p.K, p.lda, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B)) return SGEMM_ERR_LAUNCH;
+    if (!encode_map(&mapB, p.B, p.K, p.N, p.ldb, BN, BK, CU_TENSOR_MAP_SWIZZLE_NONE)) return SGEMM_ERR_LAUNCH;
+
+    const int64_t tiles_m = (p.M + BM - 1) / BM, tiles_n = (p.N + BN - 1) / BN;
+    const int64_t k_blocks = (p.K + BK - 1) / BK;
+    if (tiles_m * tiles_n > INT32_MAX / 2) return SGEMM_ERR_UNSUPPORTED;
+    const int tiles = static_cast<int>(tiles_m * tiles_n);
+    const Schedule sch = make_schedule(tiles, k_blocks, dev.sm_count, sk_mode, 4);
+    if (tiles > sch.dp_tiles) {
+        int rc = zero_tiles_launch(p.C, p.M, p.N, p.ldc, BM, BN, static_cast<int>(tiles_n), sch.dp_tiles,
+                                   tiles - sch.dp_tiles, stream, launches);
+        if (rc != SGEMM_OK) return rc;
+    }
+    Args a{};
+    a.M = p.M;
+    a.N = p.N;
+    a.K = p.K;
+    a.C = p.C;
+    a.ldc = p.ldc;
+    a.tiles_n = static_cast<int>(tiles_n);
+    a.k_blocks = static_cast<int>(k_blocks);
+    a.dp_tiles = sch.dp_tiles;
+    a.sk_ctas = sch.sk_ctas;
+    a.sk_iters = sch.sk_iters;
+    a.timeout_ns = static_cast<uint64_t>(g_watchdog_ms.load()) * 1000000ull;
+    a.watchdog = flag;
+    kernel<<<sch.grid, tma::THREADS, tma::SMEM_BYTES, stream>>>(mapA, mapB, a);
     ++*launches;
     return cudaGetLastError() == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
 }
@@ -642,14 +1029,17 @@ int watchdog_set_ms(int64_t ms) {
 
 bool tf32x3_supports(const Problem &p, const DeviceInfo &dev) {
     return p.M > 0 && p.N > 0 && p.K > 0 && dev.cc_major == 10 && dev.cc_minor == 3 &&
-           dev.smem_optin >= static_cast<size_t>(SMEM_BYTES);
+           dev.smem_optin >= static_cast<size_t>(tma::SMEM_BYTES);
 }
 
 int tf32x3_launch(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStream_t stream, int *launches) {
     if (!tf32x3_supports(p, dev) || dev.device < 0 || dev.device >= kMaxDevices) return SGEMM_ERR_UNSUPPORTED;
+    const bool vc = (p.ldc % 4 == 0) && (reinterpret_cast<uintptr_t>(p.C) % 16 == 0);
+    if (g_use_tma.load() && tma_ok(p))
+        return vc ? launch_tma<true>(p, dev, sk_mode, stream, launches)
+                  : launch_tma<false>(p, dev, sk_mode, stream, launches);
     const bool va = (p.lda % 4 == 0) && (reinterpret_cast<uintptr_t>(p.A) % 16 == 0);
     const bool vb = (p.ldb % 4 == 0) && (reinterpret_cast<uintptr_t>(p.B) % 16 == 0);
-    const bool vc = (p.ldc % 4 == 0) && (reinterpret_cast<uintptr_t>(p.C) % 16 == 0);
     const int idx = (va ? 4 : 0) + (vb ? 2 : 0) + (vc ? 1 : 0);
     switch (idx) {
         case 0: return launch<false, false, false>(p, dev, sk_mode, stream, launches);
