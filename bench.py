@@ -181,6 +181,8 @@ def run_ours(args, w, torch, dist):
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
     sgemm.set_variant(args.variant)
+    if args.tc_kernel is not None:
+        sgemm.set_tuning(sgemm.SGEMM_TUNE_TF32X3_KERNEL, args.tc_kernel)
     A, B, dA, dB, dC = _device_inputs(w, torch, device)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
     stream = torch.cuda.current_stream()
@@ -375,6 +377,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--variant", default="auto", choices=["auto", "ffma", "tf32x3"])
     ap.add_argument("--workload", default=wl.C5_HEAD.name, choices=sorted(wl.BY_NAME))
+    ap.add_argument("--tc-kernel", type=int, default=None, choices=[0, 1, 2],
+                    help="tensor-core kernel for 16-byte-aligned operands (library tuning key)")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-step-seconds", type=float, default=4.0)

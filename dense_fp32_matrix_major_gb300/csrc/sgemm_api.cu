@@ -251,6 +251,8 @@ int sgemm_set_tuning(int key, int64_t value) {
             return SGEMM_OK;
         case SGEMM_TUNE_WATCHDOG_MS:
             return sgemm::watchdog_set_ms(value);
+        case SGEMM_TUNE_TF32X3_KERNEL:
+            return sgemm::tf32x3_set_kernel(value);
         default: return SGEMM_ERR_INVALID_ARG;
     }
 }
@@ -260,6 +262,7 @@ int64_t sgemm_get_tuning(int key) {
         case SGEMM_TUNE_FFMA_TILE: return sgemm::g_tune_tile.load();
         case SGEMM_TUNE_STREAM_K: return sgemm::g_tune_sk.load();
         case SGEMM_TUNE_WATCHDOG_MS: return sgemm::watchdog_ms();
+        case SGEMM_TUNE_TF32X3_KERNEL: return sgemm::tf32x3_get_kernel();
         default: return -1;
     }
 }

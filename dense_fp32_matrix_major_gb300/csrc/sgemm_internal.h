@@ -99,6 +99,10 @@ int tf32x3_launch(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStre
 int watchdog_read_and_clear(int *code);
 int64_t watchdog_ms();
 int watchdog_set_ms(int64_t ms);
+// Which tensor-core kernel serves TMA-compatible operands (tuning key
+// SGEMM_TUNE_TF32X3_KERNEL).
+int tf32x3_set_kernel(int64_t mode);
+int64_t tf32x3_get_kernel();
 int *watchdog_flag_device_ptr();  // device address of the current device's flag, or nullptr
 
 }  // namespace sgemm

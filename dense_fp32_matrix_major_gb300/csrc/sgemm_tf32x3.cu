@@ -60,7 +60,9 @@ __device__ int g_watchdog_code;
 namespace {
 
 std::atomic<int64_t> g_watchdog_ms{2000};
-std::atomic<int> g_use_tma{1};  // TMA variant when the alignment allows it
+// Tensor-core kernel for operands that TMA can load: 0 = LDG kernel only,
+// 1 = TMA kernel, 2 = TMA kernel with A in TMEM (fastest; the default).
+std::atomic<int> g_use_tma{2};
 
 constexpr int BM = 128, BN = 256, BK = 32;  // BK fp32 = 128 bytes = one swizzle row
 constexpr int STAGES = 2;
@@ -182,6 +184,34 @@ __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a_desc, uint64_
         "l"(a_desc), "l"(b_desc), "r"(kIdesc), "r"(accumulate)
         : "memory");
 }
+
+// MMA with the A operand in TMEM (128 lanes = rows, 8 columns = the k-slice).
+__device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t accumulate) {
+    asm volatile(
+        "{\n"
+        " .reg .pred p;\n"
+        " setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n"
+        "}\n" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(kIdesc), "r"(accumulate)
+        : "memory");
+}
+
+// 16 consecutive TMEM columns of this thread's lane.
+__device__ __forceinline__ void tmem_store16(uint32_t taddr, const float (&v)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+        "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+        "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+        "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+        "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+        "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+        "r"(__float_as_uint(v[15]))
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
@@ -838,6 +868,262 @@ __global__ void __launch_bounds__(tma::THREADS, 1)
     }
 }
 
+
+// ---------------------------------------------------------------------------
+// Variant with A in TMEM (same alignment needs as the TMA variant). A's high
+// and low parts go to TMEM, which frees the shared memory for a raw staging
+// ring two k-blocks deep, so TMA latency stays off the critical path:
+//   shared: two B operand stages (B hi | B lo, 64 KB each) and two raw slots
+//   (A tile 16 KB with 128-byte swizzle | B tile 32 KB unswizzled);
+//   TMEM: the 128 x 256 accumulator (columns 0-255) and two A stages
+//   (columns 256 + 64 s: hi in the first 32, lo in the next 32).
+// Converter warps take one TMEM lane quarter (warp mod 4) and one half of the
+// 32 k-columns each: every thread splits 16 values of one row of A and stores
+// them with tcgen05.st; B is transposed into the stage as in the TMA variant.
+// One accumulator: the MMA of the next unit waits for the epilogue to drain.
+namespace tm3 {
+
+constexpr int CONV_WARPS = 8;
+constexpr int CONV_THREADS = 32 * CONV_WARPS;
+constexpr int EPI_WARP0 = 2 + CONV_WARPS;
+constexpr int THREADS = 32 * (EPI_WARP0 + EPILOGUE_WARPS);
+constexpr int B_STAGE = 2 * B_TILE;  // hi | lo
+constexpr int SLOT = A_TILE + B_TILE;  // raw A | raw B
+constexpr int RAW0 = STAGES * B_STAGE;
+constexpr int BAR_OFFSET = RAW0 + 2 * SLOT;
+constexpr int SMEM_BYTES = BAR_OFFSET + BAR_BYTES + 1024;
+constexpr uint32_t TMEM_A = BN;  // first A column
+static_assert((BN / 4) * (BK / 4) == 2 * CONV_THREADS, "two 4 x 4 B blocks per converter thread");
+
+}  // namespace tm3
+
+template <bool VEC_C>
+__global__ void __launch_bounds__(tm3::THREADS, 1)
+    tf32x3_tmem_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const Args a) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *smem = smem_raw + (base - raw);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + tm3::BAR_OFFSET);
+    // [0..1] raw_full (TMA), [2..3] raw_free (converters read the slot),
+    // [4..5] op_full (converters wrote the stage), [6..7] empty (MMA done),
+    // [8] acc_full, [9] acc_empty, [10] drain
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + 11);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 12);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    auto bar = [&](int i) { return smem_u32(bars + i); };
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(bar(s), 1);
+            mbar_init(bar(2 + s), tm3::CONV_THREADS);
+            mbar_init(bar(4 + s), tm3::CONV_THREADS);
+            mbar_init(bar(6 + s), 1);
+        }
+        mbar_init(bar(8), 1);
+        mbar_init(bar(9), 32 * EPILOGUE_WARPS);
+        mbar_init(bar(10), 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(tmem_holder)),
+                     "r"(TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            uint32_t it = 0, unit = 0;
+            for_each_unit(a, abort_flag, [&](int, int kb, int ke) {
+                if (!mbar_wait(bar(9), (unit & 1) ^ 1, a, abort_flag, WD_MMA_ACC)) return;
+                tc_fence_after();
+                for (int kblk = kb; kblk < ke; ++kblk, ++it) {
+                    const int s = it & 1;
+                    if (!mbar_wait(bar(4 + s), (it >> 1) & 1, a, abort_flag, WD_MMA_FULL)) return;
+                    tc_fence_after();
+                    const uint32_t st = base + static_cast<uint32_t>(s * tm3::B_STAGE);
+                    const uint64_t b_hi = sw128_desc(st), b_lo = sw128_desc(st + B_TILE);
+                    const uint32_t a_hi = tmem_base + tm3::TMEM_A + static_cast<uint32_t>(64 * s);
+                    const uint32_t a_lo = a_hi + 32;
+#pragma unroll
+                    for (int ks = 0; ks < BK / 8; ++ks) {
+                        const uint64_t adv = static_cast<uint64_t>(ks * 2);
+                        const uint32_t ac = static_cast<uint32_t>(ks * 8);
+                        const uint32_t first = (kblk == kb && ks == 0) ? 0u : 1u;
+                        tc_mma_ts(tmem_base, a_lo + ac, b_hi + adv, first);
+                        tc_mma_ts(tmem_base, a_hi + ac, b_lo + adv, 1u);
+                        tc_mma_ts(tmem_base, a_hi + ac, b_hi + adv, 1u);
+                    }
+                    tc_commit(bar(6 + s));
+                }
+                tc_commit(bar(8));
+                ++unit;
+            });
+            tc_commit(bar(10));
+            const bool was_aborted = *abort_flag != 0;
+            if (!mbar_wait(bar(10), 0, a, abort_flag, WD_DRAIN) && was_aborted) {
+                const uint64_t t0 = global_timer();
+                while (!mbar_try_wait(bar(10), 0) && global_timer() - t0 < a.timeout_ns) {
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ TMA issuer
+        if (lane == 0) {
+            uint32_t it = 0;
+            bool ok = true;
+            for_each_unit(a, abort_flag, [&](int tile, int kb, int ke) {
+                if (!ok) return;
+                const int m0 = (tile / a.tiles_n) * BM;
+                const int n0 = (tile % a.tiles_n) * BN;
+                for (int kblk = kb; kblk < ke; ++kblk, ++it) {
+                    const int slot = it & 1;
+                    if (!mbar_wait(bar(2 + slot), ((it >> 1) & 1) ^ 1, a, abort_flag, WD_PRODUCER)) {
+                        ok = false;
+                        return;
+                    }
+                    const uint32_t sl = base + tm3::RAW0 + static_cast<uint32_t>(slot * tm3::SLOT);
+                    mbar_arrive_expect_tx(bar(slot), tm3::SLOT);
+                    tma_load_2d(sl, &tmA, kblk * BK, m0, bar(slot));
+                    tma_load_2d(sl + A_TILE, &tmB, n0, kblk * BK, bar(slot));
+                }
+            });
+        }
+    } else if (warp < tm3::EPI_WARP0) {
+        // ------------------------------------------------------------ converters
+        const int ct = threadIdx.x - 64;
+        const int l = ct & 7, quarter = ct >> 3;
+        const int q = warp & 3, half = (warp - 2) >> 2;  // TMEM lane quarter, k half
+        const int arow = 32 * q + lane;                   // A row this thread converts
+        uint32_t it = 0;
+        bool ok = true;
+        for_each_unit(a, abort_flag, [&](int, int kb, int ke) {
+            if (!ok) return;
+            for (int kblk = kb; kblk < ke; ++kblk, ++it) {
+                const int s = it & 1;
+                const uint32_t ph = (it >> 1) & 1;
+                if (!mbar_wait(bar(s), ph, a, abort_flag, WD_PRODUCER)) {
+                    ok = false;
+                    return;
+                }
+                const uint32_t sl = base + tm3::RAW0 + static_cast<uint32_t>(s * tm3::SLOT);
+                // A: 16 k-values of row arow (128-byte swizzled rows).
+                float4 av[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) av[j] = ld_shared_v4(sl + sw128_offset(arow, 4 * half + j));
+                // B: two 4 x 4 blocks from the unswizzled staging tile.
+                float4 bv[2][4];
+                int bg[2], bc[2];
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    const int tb = quarter * 2 + r;
+                    const int g = (tb >> 3) * 8 + l, c = (l + tb) & 7;
+                    bg[r] = g;
+                    bc[r] = c;
+#pragma unroll
+                    for (int qq = 0; qq < 4; ++qq)
+                        bv[r][qq] = ld_shared_v4(sl + A_TILE + static_cast<uint32_t>((4 * c + qq) * BN * 4 + g * 16));
+                }
+                fence_proxy_async_smem();  // order these loads before the next TMA into the slot
+                mbar_arrive(bar(2 + s));
+                // The stage (B in shared memory, A in TMEM) is free once the MMA
+                // two k-blocks back has finished.
+                if (!mbar_wait(bar(6 + s), ph ^ 1, a, abort_flag, WD_PRODUCER)) {
+                    ok = false;
+                    return;
+                }
+                tc_fence_after();
+                const uint32_t st = base + static_cast<uint32_t>(s * tm3::B_STAGE);
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    const float4 q0 = bv[r][0], q1 = bv[r][1], q2 = bv[r][2], q3 = bv[r][3];
+                    const int g = bg[r], c = bc[r];
+                    uint32_t off = sw128_offset(4 * g + 0, c);
+                    split_store(st + off, st + B_TILE + off, q0.x, q1.x, q2.x, q3.x);
+                    off = sw128_offset(4 * g + 1, c);
+                    split_store(st + off, st + B_TILE + off, q0.y, q1.y, q2.y, q3.y);
+                    off = sw128_offset(4 * g + 2, c);
+                    split_store(st + off, st + B_TILE + off, q0.z, q1.z, q2.z, q3.z);
+                    off = sw128_offset(4 * g + 3, c);
+                    split_store(st + off, st + B_TILE + off, q0.w, q1.w, q2.w, q3.w);
+                }
+                float hi[16], lo[16];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    split_tf32(av[j].x, hi[4 * j + 0], lo[4 * j + 0]);
+                    split_tf32(av[j].y, hi[4 * j + 1], lo[4 * j + 1]);
+                    split_tf32(av[j].z, hi[4 * j + 2], lo[4 * j + 2]);
+                    split_tf32(av[j].w, hi[4 * j + 3], lo[4 * j + 3]);
+                }
+                const uint32_t ta = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + tm3::TMEM_A +
+                                    static_cast<uint32_t>(64 * s + 16 * half);
+                tmem_store16(ta, hi);
+                tmem_store16(ta + 32, lo);
+                tmem_wait_st();
+                fence_proxy_async_smem();
+                tc_fence_before();
+                mbar_arrive(bar(4 + s));
+            }
+        });
+    } else {
+        // -------------------------------------------------------------- epilogue
+        const int q = warp & 3;
+        uint32_t unit = 0;
+        for_each_unit(a, abort_flag, [&](int tile, int kb, int ke) {
+            if (!mbar_wait(bar(8), unit & 1, a, abort_flag, WD_EPILOGUE)) return;
+            tc_fence_after();
+            const int64_t m0 = static_cast<int64_t>(tile / a.tiles_n) * BM;
+            const int64_t n0 = static_cast<int64_t>(tile % a.tiles_n) * BN;
+            const int64_t row = m0 + q * 32 + lane;
+            const bool atomic = !(kb == 0 && ke == a.k_blocks);
+            float *crow = a.C + row * a.ldc;
+#pragma unroll 1
+            for (int ch = 0; ch < BN / 32; ++ch) {
+                float v[32];
+                tmem_load32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(ch * 32), v);
+                if (ch == BN / 32 - 1) {
+                    tc_fence_before();
+                    mbar_arrive(bar(9));  // accumulator read out: the next unit may start
+                }
+                const int64_t col0 = n0 + ch * 32;
+                if (row < a.M && col0 < a.N) {
+                    if (atomic) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (col0 + j < a.N) atomicAdd(crow + col0 + j, v[j]);
+                    } else if (VEC_C && col0 + 31 < a.N) {
+#pragma unroll
+                        for (int j = 0; j < 32; j += 4)
+                            *reinterpret_cast<float4 *>(crow + col0 + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (col0 + j < a.N) crow[col0 + j] = v[j];
+                    }
+                }
+            }
+            ++unit;
+        });
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) {
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS)
+                     : "memory");
+    }
+}
+
 constexpr int kMaxDevices = 64;
 std::once_flag g_attr_once[kMaxDevices][8];
 cudaError_t g_attr_err[kMaxDevices][8];
@@ -931,17 +1217,20 @@ bool tma_ok(const Problem &p) {
            p.K < INT32_MAX / 2 && tensor_map_encoder() != nullptr;
 }
 
-std::once_flag g_tma_attr_once[kMaxDevices][2];
-cudaError_t g_tma_attr_err[kMaxDevices][2];
+std::once_flag g_tma_attr_once[kMaxDevices][4];
+cudaError_t g_tma_attr_err[kMaxDevices][4];
 
-template <bool VEC_C>
+// V3 = A in TMEM (tf32x3_tmem_kernel), else the TMA variant (tf32x3_tma_kernel).
+template <bool V3, bool VEC_C>
 int launch_tma(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStream_t stream, int *launches) {
-    auto kernel = tf32x3_tma_kernel<VEC_C>;
-    std::call_once(g_tma_attr_once[dev.device][VEC_C ? 1 : 0], [&] {
-        g_tma_attr_err[dev.device][VEC_C ? 1 : 0] =
-            cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, tma::SMEM_BYTES);
+    auto kernel = V3 ? tf32x3_tmem_kernel<VEC_C> : tf32x3_tma_kernel<VEC_C>;
+    constexpr int smem = V3 ? tm3::SMEM_BYTES : tma::SMEM_BYTES;
+    constexpr int threads = V3 ? tm3::THREADS : tma::THREADS;
+    constexpr int idx = (V3 ? 2 : 0) + (VEC_C ? 1 : 0);
+    std::call_once(g_tma_attr_once[dev.device][idx], [&] {
+        g_tma_attr_err[dev.device][idx] = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     });
-    if (g_tma_attr_err[dev.device][VEC_C ? 1 : 0] != cudaSuccess) {
+    if (g_tma_attr_err[dev.device][idx] != cudaSuccess) {
         cudaGetLastError();
         return SGEMM_ERR_LAUNCH;
     }
@@ -974,7 +1263,7 @@ int launch_tma(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStream_
     a.sk_iters = sch.sk_iters;
     a.timeout_ns = static_cast<uint64_t>(g_watchdog_ms.load()) * 1000000ull;
     a.watchdog = flag;
-    kernel<<<sch.grid, tma::THREADS, tma::SMEM_BYTES, stream>>>(mapA, mapB, a);
+    kernel<<<sch.grid, threads, smem, stream>>>(mapA, mapB, a);
     ++*launches;
     return cudaGetLastError() == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
 }
@@ -1021,6 +1310,14 @@ int watchdog_read_and_clear(int *code) {
 
 int64_t watchdog_ms() { return g_watchdog_ms.load(); }
 
+int tf32x3_set_kernel(int64_t mode) {
+    if (mode < 0 || mode > 2) return SGEMM_ERR_INVALID_ARG;
+    g_use_tma.store(static_cast<int>(mode));
+    return SGEMM_OK;
+}
+
+int64_t tf32x3_get_kernel() { return g_use_tma.load(); }
+
 int watchdog_set_ms(int64_t ms) {
     if (ms < 1 || ms > 60000) return SGEMM_ERR_INVALID_ARG;
     g_watchdog_ms.store(ms);
@@ -1035,9 +1332,13 @@ bool tf32x3_supports(const Problem &p, const DeviceInfo &dev) {
 int tf32x3_launch(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStream_t stream, int *launches) {
     if (!tf32x3_supports(p, dev) || dev.device < 0 || dev.device >= kMaxDevices) return SGEMM_ERR_UNSUPPORTED;
     const bool vc = (p.ldc % 4 == 0) && (reinterpret_cast<uintptr_t>(p.C) % 16 == 0);
-    if (g_use_tma.load() && tma_ok(p))
-        return vc ? launch_tma<true>(p, dev, sk_mode, stream, launches)
-                  : launch_tma<false>(p, dev, sk_mode, stream, launches);
+    const int mode = g_use_tma.load();
+    if (mode == 2 && tma_ok(p))
+        return vc ? launch_tma<true, true>(p, dev, sk_mode, stream, launches)
+                  : launch_tma<true, false>(p, dev, sk_mode, stream, launches);
+    if (mode >= 1 && tma_ok(p))
+        return vc ? launch_tma<false, true>(p, dev, sk_mode, stream, launches)
+                  : launch_tma<false, false>(p, dev, sk_mode, stream, launches);
     const bool va = (p.lda % 4 == 0) && (reinterpret_cast<uintptr_t>(p.A) % 16 == 0);
     const bool vb = (p.ldb % 4 == 0) && (reinterpret_cast<uintptr_t>(p.B) % 16 == 0);
     const int idx = (va ? 4 : 0) + (vb ? 2 : 0) + (vc ? 1 : 0);

@@ -134,13 +134,18 @@ int sgemm_device_status(void);
  *                            3 = stream-K over all tiles
  *   SGEMM_TUNE_WATCHDOG_MS   milliseconds a bounded wait polls before it gives
  *                            up (1 .. 60000; default 2000)
+ *   SGEMM_TUNE_TF32X3_KERNEL  tensor-core kernel for operands whose base
+ *                            addresses and row strides are 16-byte aligned:
+ *                            0 = per-thread loads, 1 = TMA, 2 = TMA with A's
+ *                            operands in tensor memory (default)
  * Returns SGEMM_OK or SGEMM_ERR_INVALID_ARG. sgemm_get_tuning returns the
  * value, or -1 for an unknown key.
  */
 enum sgemm_tuning_key {
     SGEMM_TUNE_FFMA_TILE = 1,
     SGEMM_TUNE_STREAM_K = 2,
-    SGEMM_TUNE_WATCHDOG_MS = 3
+    SGEMM_TUNE_WATCHDOG_MS = 3,
+    SGEMM_TUNE_TF32X3_KERNEL = 4
 };
 int sgemm_set_tuning(int key, int64_t value);
 int64_t sgemm_get_tuning(int key);

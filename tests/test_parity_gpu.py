@@ -16,12 +16,16 @@ from tests.gpu_harness import TOL, outside_box_intact, oracle_error, run_sgemm, 
 
 pytestmark = pytest.mark.gpu
 
-# (variant, ffma tile, stream-K mode) settings every small-shape test runs under.
+# (variant, ffma tile, stream-K mode, tensor-core kernel) settings every
+# small-shape test runs under. Tensor-core kernels: 0 = per-thread loads,
+# 1 = TMA, 2 = TMA with A in tensor memory (default).
 SETTINGS = [
-    ("auto", 0, 0),
-    ("ffma", 1, 1), ("ffma", 1, 3), ("ffma", 2, 2), ("ffma", 3, 0), ("ffma", 2, 3),
-    ("tf32x3", 0, 0), ("tf32x3", 0, 1), ("tf32x3", 0, 3),
+    ("auto", 0, 0, 2),
+    ("ffma", 1, 1, 2), ("ffma", 1, 3, 2), ("ffma", 2, 2, 2), ("ffma", 3, 0, 2), ("ffma", 2, 3, 2),
+    ("tf32x3", 0, 0, 2), ("tf32x3", 0, 1, 2), ("tf32x3", 0, 3, 2),
+    ("tf32x3", 0, 0, 1), ("tf32x3", 0, 3, 1), ("tf32x3", 0, 0, 0), ("tf32x3", 0, 3, 0),
 ]
+SETTING_IDS = [f"{s[0]}-t{s[1]}-sk{s[2]}-k{s[3]}" for s in SETTINGS]
 
 
 @pytest.fixture(scope="module")
@@ -35,13 +39,16 @@ def lib():
     sgemm.set_variant(0)
     sgemm.set_tuning(sgemm.SGEMM_TUNE_FFMA_TILE, 0)
     sgemm.set_tuning(sgemm.SGEMM_TUNE_STREAM_K, 0)
+    sgemm.set_tuning(sgemm.SGEMM_TUNE_TF32X3_KERNEL, 2)
 
 
 def _apply(lib, setting):
-    variant, tile, sk = setting
+    variant, tile, sk = setting[:3]
+    tc = setting[3] if len(setting) > 3 else 2
     lib.set_variant(variant)
     lib.set_tuning(lib.SGEMM_TUNE_FFMA_TILE, tile)
     lib.set_tuning(lib.SGEMM_TUNE_STREAM_K, sk)
+    lib.set_tuning(lib.SGEMM_TUNE_TF32X3_KERNEL, tc)
 
 
 def _check(A, B, C, flat, ldc, offset=0, exact=False):
@@ -58,7 +65,7 @@ def _check(A, B, C, flat, ldc, offset=0, exact=False):
 TINY = [1, 2, 3, 5, 8, 13, 16, 17]
 
 
-@pytest.mark.parametrize("setting", SETTINGS, ids=lambda s: f"{s[0]}-t{s[1]}-sk{s[2]}")
+@pytest.mark.parametrize("setting", SETTINGS, ids=SETTING_IDS)
 def test_tiny_shape_sweep(lib, setting):
     _apply(lib, setting)
     for M, N, K in itertools.product(TINY, TINY, TINY):
@@ -72,7 +79,7 @@ TILE_EDGES = [(63, 65, 15), (64, 64, 16), (65, 63, 17), (127, 255, 31), (128, 25
               (129, 257, 47), (1, 300, 100), (300, 1, 100), (200, 3, 1), (33, 257, 513)]
 
 
-@pytest.mark.parametrize("setting", SETTINGS, ids=lambda s: f"{s[0]}-t{s[1]}-sk{s[2]}")
+@pytest.mark.parametrize("setting", SETTINGS, ids=SETTING_IDS)
 @pytest.mark.parametrize("M,N,K", TILE_EDGES)
 def test_tile_boundary_crossings(lib, setting, M, N, K):
     _apply(lib, setting)
@@ -82,7 +89,7 @@ def test_tile_boundary_crossings(lib, setting, M, N, K):
     _check(A, B, C, flat, N)
 
 
-@pytest.mark.parametrize("setting", SETTINGS, ids=lambda s: f"{s[0]}-t{s[1]}-sk{s[2]}")
+@pytest.mark.parametrize("setting", SETTINGS, ids=SETTING_IDS)
 def test_integer_inputs_bit_exact(lib, setting):
     _apply(lib, setting)
     for (M, N, K) in [(257, 129, 1000), (64, 300, 4096), (1000, 40, 77)]:
@@ -92,7 +99,7 @@ def test_integer_inputs_bit_exact(lib, setting):
         _check(A, B, C, flat, N, exact=True)
 
 
-@pytest.mark.parametrize("setting", SETTINGS, ids=lambda s: f"{s[0]}-t{s[1]}-sk{s[2]}")
+@pytest.mark.parametrize("setting", SETTINGS, ids=SETTING_IDS)
 def test_padded_strides_and_unaligned_pointers(lib, setting):
     _apply(lib, setting)
     M, N, K = 150, 270, 90
@@ -162,9 +169,9 @@ def _config_error(C, A, B, w):
 
 
 @pytest.mark.parametrize("w", wl.ALL, ids=lambda w: w.name)
-@pytest.mark.parametrize("variant", ["auto", "ffma", "tf32x3"])
-def test_benchmark_configs(lib, w, variant):
-    _apply(lib, (variant, 0, 0))
+@pytest.mark.parametrize("variant,tc", [("auto", 2), ("ffma", 2), ("tf32x3", 2), ("tf32x3", 1), ("tf32x3", 0)])
+def test_benchmark_configs(lib, w, variant, tc):
+    _apply(lib, (variant, 0, 0, tc))
     A, B = wl.make_inputs(w)
     C, flat, rc = run_sgemm(A, B, lda=w.lda, ldb=w.ldb, ldc=w.ldc)
     assert rc == 0
