@@ -239,6 +239,14 @@ int sgemm_device_status(void) {
     return code ? SGEMM_ERR_TIMEOUT : SGEMM_OK;
 }
 
+int sgemm_watchdog_selftest(int64_t wait_ms, sgemm_stream_t stream) {
+    if (wait_ms < 1 || wait_ms > 60000) return SGEMM_ERR_INVALID_ARG;
+    sgemm::DeviceInfo dev;
+    const int rc = sgemm::current_device(&dev);
+    if (rc != SGEMM_OK) return rc;
+    return sgemm::watchdog_selftest_launch(wait_ms, reinterpret_cast<cudaStream_t>(stream));
+}
+
 int sgemm_set_tuning(int key, int64_t value) {
     switch (key) {
         case SGEMM_TUNE_FFMA_TILE:

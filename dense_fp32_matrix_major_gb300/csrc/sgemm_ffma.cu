@@ -279,17 +279,25 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS) ffma_kernel(const F
     }
 }
 
-// Zero the C region of tiles [first_tile, first_tile + gridDim.x) of a BM x BN grid.
+// Zero the C region of `count` tiles starting at `first_tile` of a bm x bn tile
+// grid: blockIdx.y picks the tile, blockIdx.x a band of 8 rows; a warp clears
+// one row (float4 stores when the row start is 16-byte aligned).
 __global__ void zero_tiles_kernel(float *C, int64_t M, int64_t N, int64_t ldc, int bm, int bn, int tiles_n,
                                   int first_tile) {
-    const int tile = first_tile + blockIdx.x;
+    const int tile = first_tile + blockIdx.y;
     const int64_t m0 = static_cast<int64_t>(tile / tiles_n) * bm;
     const int64_t n0 = static_cast<int64_t>(tile % tiles_n) * bn;
-    const int rows = static_cast<int>(min64(bm, M - m0));
+    const int64_t row = m0 + blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (row >= M || row >= m0 + bm) return;
     const int cols = static_cast<int>(min64(bn, N - n0));
-    for (int e = threadIdx.x; e < rows * cols; e += blockDim.x) {
-        const int r = e / cols, c = e % cols;
-        C[(m0 + r) * ldc + n0 + c] = 0.0f;
+    float *p = C + row * ldc + n0;
+    const int lane = threadIdx.x & 31;
+    if ((reinterpret_cast<uintptr_t>(p) & 15) == 0) {
+        const int v4 = cols >> 2;
+        for (int i = lane; i < v4; i += 32) reinterpret_cast<float4 *>(p)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int i = 4 * v4 + lane; i < cols; i += 32) p[i] = 0.0f;
+    } else {
+        for (int i = lane; i < cols; i += 32) p[i] = 0.0f;
     }
 }
 
@@ -419,7 +427,8 @@ int ffma_launch(const Problem &p, const DeviceInfo &dev, int tile, int sk_mode, 
 int zero_tiles_launch(float *C, int64_t M, int64_t N, int64_t ldc, int bm, int bn, int tiles_n, int first_tile,
                       int count, cudaStream_t stream, int *launches) {
     if (count <= 0) return SGEMM_OK;
-    zero_tiles_kernel<<<count, 256, 0, stream>>>(C, M, N, ldc, bm, bn, tiles_n, first_tile);
+    const dim3 grid(static_cast<unsigned>((bm + 7) / 8), static_cast<unsigned>(count));
+    zero_tiles_kernel<<<grid, 256, 0, stream>>>(C, M, N, ldc, bm, bn, tiles_n, first_tile);
     ++*launches;
     return cudaGetLastError() == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
 }

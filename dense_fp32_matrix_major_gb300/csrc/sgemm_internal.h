@@ -102,6 +102,7 @@ int watchdog_set_ms(int64_t ms);
 // Which tensor-core kernel serves TMA-compatible operands (tuning key
 // SGEMM_TUNE_TF32X3_KERNEL).
 int tf32x3_set_kernel(int64_t mode);
+int watchdog_selftest_launch(int64_t wait_ms, cudaStream_t stream);
 int64_t tf32x3_get_kernel();
 int *watchdog_flag_device_ptr();  // device address of the current device's flag, or nullptr
 

@@ -81,7 +81,7 @@ constexpr int B_TASKS = BN * (BK / 4);
 static_assert(A_TASKS % PRODUCER_THREADS == 0 && B_TASKS % PRODUCER_THREADS == 0, "even producer split");
 
 // Watchdog codes (which wait gave up).
-enum : int { WD_PRODUCER = 1, WD_MMA_FULL = 2, WD_MMA_ACC = 3, WD_EPILOGUE = 4, WD_DRAIN = 5 };
+enum : int { WD_PRODUCER = 1, WD_MMA_FULL = 2, WD_MMA_ACC = 3, WD_EPILOGUE = 4, WD_DRAIN = 5, WD_SELFTEST = 6 };
 
 struct Args {
     int64_t M, N, K;
@@ -209,6 +209,15 @@ __device__ __forceinline__ void tmem_store16(uint32_t taddr, const float (&v)[16
         "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
         "r"(__float_as_uint(v[15]))
         : "memory");
+}
+
+// 8 consecutive TMEM columns of this thread's lane.
+__device__ __forceinline__ void tmem_store8(uint32_t taddr, const float (&v)[8]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+                 "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+                 "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+                 "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7]))
+                 : "memory");
 }
 
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
@@ -877,13 +886,14 @@ __global__ void __launch_bounds__(tma::THREADS, 1)
 //   (A tile 16 KB with 128-byte swizzle | B tile 32 KB unswizzled);
 //   TMEM: the 128 x 256 accumulator (columns 0-255) and two A stages
 //   (columns 256 + 64 s: hi in the first 32, lo in the next 32).
-// Converter warps take one TMEM lane quarter (warp mod 4) and one half of the
-// 32 k-columns each: every thread splits 16 values of one row of A and stores
-// them with tcgen05.st; B is transposed into the stage as in the TMA variant.
+// Sixteen converter warps: each takes one TMEM lane quarter (warp mod 4) and
+// one quarter of the 32 k-columns, so every thread splits 8 values of one row
+// of A and stores them with tcgen05.st; each thread also transposes one 4 x 4
+// block of B into the stage (mapping as in the TMA variant).
 // One accumulator: the MMA of the next unit waits for the epilogue to drain.
 namespace tm3 {
 
-constexpr int CONV_WARPS = 8;
+constexpr int CONV_WARPS = 16;
 constexpr int CONV_THREADS = 32 * CONV_WARPS;
 constexpr int EPI_WARP0 = 2 + CONV_WARPS;
 constexpr int THREADS = 32 * (EPI_WARP0 + EPILOGUE_WARPS);
@@ -893,7 +903,8 @@ constexpr int RAW0 = STAGES * B_STAGE;
 constexpr int BAR_OFFSET = RAW0 + 2 * SLOT;
 constexpr int SMEM_BYTES = BAR_OFFSET + BAR_BYTES + 1024;
 constexpr uint32_t TMEM_A = BN;  // first A column
-static_assert((BN / 4) * (BK / 4) == 2 * CONV_THREADS, "two 4 x 4 B blocks per converter thread");
+static_assert((BN / 4) * (BK / 4) == CONV_THREADS, "one 4 x 4 B block per converter thread");
+static_assert(CONV_WARPS == 16, "four converter warps per TMEM lane quarter, 8 k-columns each");
 
 }  // namespace tm3
 
@@ -1001,9 +1012,10 @@ __global__ void __launch_bounds__(tm3::THREADS, 1)
     } else if (warp < tm3::EPI_WARP0) {
         // ------------------------------------------------------------ converters
         const int ct = threadIdx.x - 64;
-        const int l = ct & 7, quarter = ct >> 3;
-        const int q = warp & 3, half = (warp - 2) >> 2;  // TMEM lane quarter, k half
-        const int arow = 32 * q + lane;                   // A row this thread converts
+        const int l = ct & 7, tb = ct >> 3;  // 64 groups of eight lanes
+        const int g = (tb >> 3) * 8 + l, c = (l + tb) & 7;  // this thread's 4 x 4 B block
+        const int q = warp & 3, part = (warp - 2) >> 2;     // TMEM lane quarter, k-columns 8*part..+7
+        const int arow = 32 * q + lane;                     // A row this thread converts
         uint32_t it = 0;
         bool ok = true;
         for_each_unit(a, abort_flag, [&](int, int kb, int ke) {
@@ -1016,23 +1028,14 @@ __global__ void __launch_bounds__(tm3::THREADS, 1)
                     return;
                 }
                 const uint32_t sl = base + tm3::RAW0 + static_cast<uint32_t>(s * tm3::SLOT);
-                // A: 16 k-values of row arow (128-byte swizzled rows).
-                float4 av[4];
+                // A: 8 k-values of row arow (128-byte swizzled rows).
+                const float4 a0 = ld_shared_v4(sl + sw128_offset(arow, 2 * part));
+                const float4 a1 = ld_shared_v4(sl + sw128_offset(arow, 2 * part + 1));
+                // B: rows 4c..4c+3, columns 4g..4g+3 of the unswizzled staging tile.
+                float4 bq[4];
 #pragma unroll
-                for (int j = 0; j < 4; ++j) av[j] = ld_shared_v4(sl + sw128_offset(arow, 4 * half + j));
-                // B: two 4 x 4 blocks from the unswizzled staging tile.
-                float4 bv[2][4];
-                int bg[2], bc[2];
-#pragma unroll
-                for (int r = 0; r < 2; ++r) {
-                    const int tb = quarter * 2 + r;
-                    const int g = (tb >> 3) * 8 + l, c = (l + tb) & 7;
-                    bg[r] = g;
-                    bc[r] = c;
-#pragma unroll
-                    for (int qq = 0; qq < 4; ++qq)
-                        bv[r][qq] = ld_shared_v4(sl + A_TILE + static_cast<uint32_t>((4 * c + qq) * BN * 4 + g * 16));
-                }
+                for (int qq = 0; qq < 4; ++qq)
+                    bq[qq] = ld_shared_v4(sl + A_TILE + static_cast<uint32_t>((4 * c + qq) * BN * 4 + g * 16));
                 fence_proxy_async_smem();  // order these loads before the next TMA into the slot
                 mbar_arrive(bar(2 + s));
                 // The stage (B in shared memory, A in TMEM) is free once the MMA
@@ -1043,31 +1046,28 @@ __global__ void __launch_bounds__(tm3::THREADS, 1)
                 }
                 tc_fence_after();
                 const uint32_t st = base + static_cast<uint32_t>(s * tm3::B_STAGE);
-#pragma unroll
-                for (int r = 0; r < 2; ++r) {
-                    const float4 q0 = bv[r][0], q1 = bv[r][1], q2 = bv[r][2], q3 = bv[r][3];
-                    const int g = bg[r], c = bc[r];
-                    uint32_t off = sw128_offset(4 * g + 0, c);
-                    split_store(st + off, st + B_TILE + off, q0.x, q1.x, q2.x, q3.x);
-                    off = sw128_offset(4 * g + 1, c);
-                    split_store(st + off, st + B_TILE + off, q0.y, q1.y, q2.y, q3.y);
-                    off = sw128_offset(4 * g + 2, c);
-                    split_store(st + off, st + B_TILE + off, q0.z, q1.z, q2.z, q3.z);
-                    off = sw128_offset(4 * g + 3, c);
-                    split_store(st + off, st + B_TILE + off, q0.w, q1.w, q2.w, q3.w);
-                }
-                float hi[16], lo[16];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    split_tf32(av[j].x, hi[4 * j + 0], lo[4 * j + 0]);
-                    split_tf32(av[j].y, hi[4 * j + 1], lo[4 * j + 1]);
-                    split_tf32(av[j].z, hi[4 * j + 2], lo[4 * j + 2]);
-                    split_tf32(av[j].w, hi[4 * j + 3], lo[4 * j + 3]);
-                }
+                // Column j of the 4 x 4 block is chunk c of operand row 4g + j.
+                uint32_t off = sw128_offset(4 * g + 0, c);
+                split_store(st + off, st + B_TILE + off, bq[0].x, bq[1].x, bq[2].x, bq[3].x);
+                off = sw128_offset(4 * g + 1, c);
+                split_store(st + off, st + B_TILE + off, bq[0].y, bq[1].y, bq[2].y, bq[3].y);
+                off = sw128_offset(4 * g + 2, c);
+                split_store(st + off, st + B_TILE + off, bq[0].z, bq[1].z, bq[2].z, bq[3].z);
+                off = sw128_offset(4 * g + 3, c);
+                split_store(st + off, st + B_TILE + off, bq[0].w, bq[1].w, bq[2].w, bq[3].w);
+                float hi[8], lo[8];
+                split_tf32(a0.x, hi[0], lo[0]);
+                split_tf32(a0.y, hi[1], lo[1]);
+                split_tf32(a0.z, hi[2], lo[2]);
+                split_tf32(a0.w, hi[3], lo[3]);
+                split_tf32(a1.x, hi[4], lo[4]);
+                split_tf32(a1.y, hi[5], lo[5]);
+                split_tf32(a1.z, hi[6], lo[6]);
+                split_tf32(a1.w, hi[7], lo[7]);
                 const uint32_t ta = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + tm3::TMEM_A +
-                                    static_cast<uint32_t>(64 * s + 16 * half);
-                tmem_store16(ta, hi);
-                tmem_store16(ta + 32, lo);
+                                    static_cast<uint32_t>(64 * s + 8 * part);
+                tmem_store8(ta, hi);
+                tmem_store8(ta + 32, lo);
                 tmem_wait_st();
                 fence_proxy_async_smem();
                 tc_fence_before();
@@ -1122,6 +1122,26 @@ __global__ void __launch_bounds__(tm3::THREADS, 1)
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS)
                      : "memory");
     }
+}
+
+// One bounded wait on an mbarrier that nothing arrives at: it must give up
+// after timeout_ns, record WD_SELFTEST in the watchdog flag and return.
+__global__ void watchdog_selftest_kernel(uint64_t timeout_ns, int *flag) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        Args a{};
+        a.timeout_ns = timeout_ns;
+        a.watchdog = flag;
+        mbar_wait(smem_u32(&bar), 0, a, &abort_flag, WD_SELFTEST);
+    }
+    __syncthreads();
 }
 
 constexpr int kMaxDevices = 64;
@@ -1309,6 +1329,14 @@ int watchdog_read_and_clear(int *code) {
 }
 
 int64_t watchdog_ms() { return g_watchdog_ms.load(); }
+
+int watchdog_selftest_launch(int64_t wait_ms, cudaStream_t stream) {
+    if (wait_ms < 1 || wait_ms > 60000) return SGEMM_ERR_INVALID_ARG;
+    int *flag = watchdog_flag_device_ptr();
+    if (!flag) return SGEMM_ERR_LAUNCH;
+    watchdog_selftest_kernel<<<1, 32, 0, stream>>>(static_cast<uint64_t>(wait_ms) * 1000000ull, flag);
+    return cudaGetLastError() == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
+}
 
 int tf32x3_set_kernel(int64_t mode) {
     if (mode < 0 || mode > 2) return SGEMM_ERR_INVALID_ARG;

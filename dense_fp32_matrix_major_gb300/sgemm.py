@@ -42,6 +42,7 @@ SIGNATURES = {
     "sgemm_last_launch_count": (_int, []),
     "sgemm_strerror": (_cp, [_int]),
     "sgemm_device_status": (_int, []),
+    "sgemm_watchdog_selftest": (_int, [_i64, _vp]),
     "sgemm_set_tuning": (_int, [_int, _i64]),
     "sgemm_get_tuning": (_i64, [_int]),
     "sgemm_version": (_cp, []),
@@ -110,6 +111,13 @@ def get_tuning(key: int) -> int:
 
 def device_status() -> int:
     return lib.sgemm_device_status()
+
+
+def watchdog_selftest(wait_ms: int, stream=None) -> None:
+    """Enqueue a kernel whose one bounded wait must time out (see sgemm.h)."""
+    rc = lib.sgemm_watchdog_selftest(int(wait_ms), _stream_handle(stream))
+    if rc:
+        raise SgemmError(rc, "sgemm_watchdog_selftest")
 
 
 def version() -> str:

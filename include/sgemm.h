@@ -126,6 +126,18 @@ const char *sgemm_strerror(int status);
 int sgemm_device_status(void);
 
 /*
+ * Exercises the bounded-wait reporting path without faulting the device:
+ * enqueues on `stream` a one-warp kernel whose single mbarrier wait can never
+ * complete (nothing arrives). The wait gives up after wait_ms (1 .. 60000),
+ * records the event in the watchdog flag and the kernel exits normally, so a
+ * following sgemm_device_status() returns SGEMM_ERR_TIMEOUT (once) and the
+ * CUDA context stays usable. Returns SGEMM_OK once enqueued,
+ * SGEMM_ERR_INVALID_ARG for wait_ms out of range, SGEMM_ERR_DEVICE or
+ * SGEMM_ERR_LAUNCH.
+ */
+int sgemm_watchdog_selftest(int64_t wait_ms, sgemm_stream_t stream);
+
+/*
  * Tuning keys for sgemm_set_tuning / sgemm_get_tuning (process-wide).
  *   SGEMM_TUNE_FFMA_TILE     0 = choose per shape; 1 = 128x256; 2 = 128x128;
  *                            3 = 64x64 (FFMA block tile, M x N)

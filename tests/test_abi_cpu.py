@@ -63,6 +63,12 @@ def test_variant_selector_roundtrip(binding):
         binding.set_variant(old)
 
 
+def test_watchdog_selftest_rejects_bad_limits(binding):
+    # Range checks run before any device work.
+    assert binding.lib.sgemm_watchdog_selftest(0, None) == binding.SGEMM_ERR_INVALID_ARG
+    assert binding.lib.sgemm_watchdog_selftest(60001, None) == binding.SGEMM_ERR_INVALID_ARG
+
+
 def test_tuning_keys(binding):
     assert binding.get_tuning(99) == -1
     binding.set_tuning(binding.SGEMM_TUNE_FFMA_TILE, 2)

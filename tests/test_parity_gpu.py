@@ -243,3 +243,21 @@ def test_nonfinite_inputs_propagate(lib):
         assert np.all(np.isnan(C[77]))
         rest = np.delete(C, [5, 77], axis=0)
         assert np.all(rest == 40.0)
+
+
+def test_bounded_wait_reports_timeout(lib):
+    """A wait that can never complete gives up, reports SGEMM_ERR_TIMEOUT once,
+    and leaves the context usable."""
+    import time
+
+    assert lib.device_status() == 0
+    t0 = time.perf_counter()
+    lib.watchdog_selftest(200)
+    assert lib.device_status() == lib.SGEMM_ERR_TIMEOUT
+    assert time.perf_counter() - t0 >= 0.15
+    assert lib.device_status() == 0  # read-and-clear
+    _apply(lib, ("auto", 0, 0))
+    A, B = wl.make_pair(300, 500, 700, "normal", 4)
+    C, flat, rc = run_sgemm(A, B)
+    assert rc == 0 and oracle_error(C, A, B) <= TOL
+    assert lib.sgemm_f32_raw(1, 1, 1, 0, 1, 0, 1, 0, 1, 0) == lib.SGEMM_ERR_INVALID_ARG
