@@ -87,7 +87,7 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.perf_counter(), line.strip()))
 
     def stop(self):
         if self.proc is None:
@@ -100,10 +100,13 @@ class ClockSampler:
         if self._thread:
             self._thread.join(timeout=2)
 
-    def summary(self):
+    def summary(self, t0=None, t1=None):
+        """Median SM clock and throttle reasons of the samples read in [t0, t1]."""
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for t, ln in self.lines:
+            if (t0 is not None and t < t0) or (t1 is not None and t > t1):
+                continue
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 9:
                 continue
@@ -218,7 +221,9 @@ def run_ours(args, w, torch, dist):
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
-    wall = time.perf_counter() - wall0
+    wall1 = time.perf_counter()
+    wall = wall1 - wall0
+    time.sleep(0.15)  # the sample covering the end of the region is printed a little later
     sampler.stop()
     per_step = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     ms = sum(per_step) / len(per_step)
@@ -238,7 +243,7 @@ def run_ours(args, w, torch, dist):
     # End to end: host buffers through the C ABI, copies inside the timed region.
     e2e = run_e2e(args, w, torch, sgemm, A, B, device, dist, ws)
 
-    clocks = sampler.summary()
+    clocks = sampler.summary(wall0, wall1 + 0.12)
     sm_max = clocks["sm_max_mhz"] or GB300_MAX_SM_MHZ
     sm_count = torch.cuda.get_device_properties(device).multi_processor_count
     if variant_used == "tf32x3":

@@ -168,6 +168,16 @@ int sgemm_f32(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, cons
     return sgemm::enqueue(p, reinterpret_cast<cudaStream_t>(stream));
 }
 
+// rows x cols of a matrix with row stride ld: one linear copy when the rows
+// are contiguous, else a strided copy that leaves the row padding untouched.
+static cudaError_t copy_rows(float *dst, const float *src, int64_t rows, int64_t cols, int64_t ld,
+                             cudaMemcpyKind kind, cudaStream_t s) {
+    const size_t f = sizeof(float);
+    if (ld == cols || rows == 1)
+        return cudaMemcpyAsync(dst, src, static_cast<size_t>(rows * cols) * f, kind, s);
+    return cudaMemcpy2DAsync(dst, ld * f, src, ld * f, cols * f, rows, kind, s);
+}
+
 int sgemm_f32_from_host(int64_t M, int64_t N, int64_t K, const float *A_host, int64_t lda,
                         const float *B_host, int64_t ldb, float *C_host, int64_t ldc, float *dA, float *dB,
                         float *dC, sgemm_stream_t stream) {
@@ -176,18 +186,14 @@ int sgemm_f32_from_host(int64_t M, int64_t N, int64_t K, const float *A_host, in
     if ((M > 0 && K > 0 && !A_host) || (K > 0 && N > 0 && !B_host) || (M > 0 && N > 0 && !C_host))
         return SGEMM_ERR_INVALID_ARG;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const size_t f = sizeof(float);
-    if (M > 0 && K > 0 &&
-        cudaMemcpy2DAsync(dA, lda * f, A_host, lda * f, K * f, M, cudaMemcpyHostToDevice, s) != cudaSuccess)
+    if (M > 0 && K > 0 && copy_rows(dA, A_host, M, K, lda, cudaMemcpyHostToDevice, s) != cudaSuccess)
         return cudaGetLastError(), SGEMM_ERR_LAUNCH;
-    if (K > 0 && N > 0 &&
-        cudaMemcpy2DAsync(dB, ldb * f, B_host, ldb * f, N * f, K, cudaMemcpyHostToDevice, s) != cudaSuccess)
+    if (K > 0 && N > 0 && copy_rows(dB, B_host, K, N, ldb, cudaMemcpyHostToDevice, s) != cudaSuccess)
         return cudaGetLastError(), SGEMM_ERR_LAUNCH;
     Problem p{M, N, K, dA, lda, dB, ldb, dC, ldc};
     rc = sgemm::enqueue(p, s);
     if (rc != SGEMM_OK) return rc;
-    if (M > 0 && N > 0 &&
-        cudaMemcpy2DAsync(C_host, ldc * f, dC, ldc * f, N * f, M, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    if (M > 0 && N > 0 && copy_rows(C_host, dC, M, N, ldc, cudaMemcpyDeviceToHost, s) != cudaSuccess)
         return cudaGetLastError(), SGEMM_ERR_LAUNCH;
     return SGEMM_OK;
 }
