@@ -79,14 +79,14 @@ int check_args(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, con
     return SGEMM_OK;
 }
 
-// AUTO: the tensor-core path once the product is large enough to fill the
-// GPU with 128 x 256 tiles (measured crossover between 1024^3 and
-// 1023 x 2049 x 1537 on GB300), and only up to K = 8192: its accumulation
-// rounds toward zero, so its error grows with K (2.7e-6 of the 1e-5 bound at
-// K = 4096); beyond that the FFMA path keeps the bound at any K.
+// AUTO: the tensor-core path from 2^29 multiply-adds up (measured on GB300:
+// FFMA is faster at 512^3, the tensor-core path from 1024^3 on), and only up
+// to K = 8192: its accumulation rounds toward zero, so its error grows with K
+// (2.9e-6 of the 1e-5 bound at K = 4096); beyond that the FFMA path keeps the
+// bound at any K.
 int auto_variant(const Problem &p, const DeviceInfo &dev) {
     const double work = static_cast<double>(p.M) * static_cast<double>(p.N) * static_cast<double>(p.K);
-    if (work >= 2147483648.0 && p.K <= 8192 && tf32x3_supports(p, dev)) return SGEMM_TF32X3;
+    if (work >= 536870912.0 && p.K <= 8192 && tf32x3_supports(p, dev)) return SGEMM_TF32X3;
     return SGEMM_FFMA;
 }
 
