@@ -74,8 +74,13 @@ def _load():
                 _i64, _i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _vp, _i64, ctypes.c_int]
             lib.oracle_sgemm_f64_at.argtypes = [
                 _i64, _i64, _i64, _vp, _i64, _vp, _i64, _i64, _vp, _vp, _vp, _vp]
-            for fn in (lib.oracle_sgemm_f32, lib.oracle_sgemm_f64,
-                       lib.oracle_sgemm_f64_rows, lib.oracle_sgemm_f64_at):
+            _d = ctypes.c_double
+            lib.oracle_gemm_f64.argtypes = [ctypes.c_int, ctypes.c_int, _i64, _i64, _i64, _d, _vp, _i64,
+                                            _vp, _i64, _d, _vp, _i64, _vp, _vp, _i64]
+            lib.oracle_gemm_f64_at.argtypes = [ctypes.c_int, ctypes.c_int, _i64, _i64, _i64, _d, _vp,
+                                               _i64, _vp, _i64, _d, _vp, _i64, _i64, _vp, _vp, _vp, _vp]
+            for fn in (lib.oracle_sgemm_f32, lib.oracle_sgemm_f64, lib.oracle_sgemm_f64_rows,
+                       lib.oracle_sgemm_f64_at, lib.oracle_gemm_f64, lib.oracle_gemm_f64_at):
                 fn.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -165,6 +170,57 @@ def sgemm_f64_at(A: np.ndarray, B: np.ndarray, rows, cols):
     _check(_load().oracle_sgemm_f64_at(M, N, K, pa, lda, pb, ldb, r.shape[0], r.ctypes.data,
                                        c.ctypes.data, c64.ctypes.data, s.ctypes.data),
            "oracle_sgemm_f64_at")
+    return c64, s
+
+
+def _gemm_shapes(A, B, transA, transB):
+    M, K = (A.shape[1], A.shape[0]) if transA else A.shape
+    K2, N = (B.shape[1], B.shape[0]) if transB else B.shape
+    if K != K2:
+        raise ValueError("inner dimensions differ")
+    return M, N, K
+
+
+def _c_in(C_in, beta, M, N):
+    if beta == 0.0:
+        return None, max(N, 1)
+    if C_in is None or C_in.shape != (M, N):
+        raise ValueError("beta != 0 needs C_in of shape (M, N)")
+    return _rowmajor(C_in, "C_in")
+
+
+def gemm_f64(A, B, *, transA=False, transB=False, alpha=1.0, beta=0.0, C_in=None):
+    """(C64, S) of alpha * op(A) @ op(B) + beta * C_in (the BLAS GEMM form).
+
+    S = |alpha| sum_k |op(A)||op(B)| + |beta| |C_in|, the scale of the
+    acceptance measure. With beta == 0, C_in is not read.
+    """
+    M, N, K = _gemm_shapes(A, B, transA, transB)
+    pa, lda = _rowmajor(A, "A")
+    pb, ldb = _rowmajor(B, "B")
+    pc, ldc_in = _c_in(C_in, beta, M, N)
+    C64 = np.empty((M, N), dtype=np.float64)
+    S = np.empty((M, N), dtype=np.float64)
+    _check(_load().oracle_gemm_f64(int(transA), int(transB), M, N, K, float(alpha), pa, lda, pb,
+                                   ldb, float(beta), pc, ldc_in, C64.ctypes.data, S.ctypes.data,
+                                   max(N, 1)), "oracle_gemm_f64")
+    return C64, S
+
+
+def gemm_f64_at(A, B, rows, cols, *, transA=False, transB=False, alpha=1.0, beta=0.0, C_in=None):
+    """(c64, s) of the GEMM form at (rows[t], cols[t])."""
+    M, N, K = _gemm_shapes(A, B, transA, transB)
+    r = np.ascontiguousarray(rows, dtype=np.int64)
+    c = np.ascontiguousarray(cols, dtype=np.int64)
+    pa, lda = _rowmajor(A, "A")
+    pb, ldb = _rowmajor(B, "B")
+    pc, ldc_in = _c_in(C_in, beta, M, N)
+    c64 = np.empty(r.shape[0], dtype=np.float64)
+    s = np.empty(r.shape[0], dtype=np.float64)
+    _check(_load().oracle_gemm_f64_at(int(transA), int(transB), M, N, K, float(alpha), pa, lda,
+                                      pb, ldb, float(beta), pc, ldc_in, r.shape[0], r.ctypes.data,
+                                      c.ctypes.data, c64.ctypes.data, s.ctypes.data),
+           "oracle_gemm_f64_at")
     return c64, s
 
 

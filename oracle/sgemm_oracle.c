@@ -40,6 +40,12 @@
  *                        order, so it equals oracle_sgemm_f64 bit for bit.
  *   oracle_sgemm_f64_at  C64 and S at a list of (row, col) samples, for
  *                        checks at sizes where the full product is too slow.
+ *   oracle_gemm_f64      the general form C = alpha * op(A) * op(B) + beta * C
+ *   oracle_gemm_f64_at   (op = the matrix or its transpose), in double, with
+ *                        the error scale S = |alpha| sum_k |op(A)||op(B)| +
+ *                        |beta| |C_in|. The pages define only C = A * B; the
+ *                        general form is the standard BLAS GEMM, taken with
+ *                        its convention that beta = 0 means C_in is not read.
  *
  * Pins (tests/test_oracle_pins.py, CPU only): all-ones inputs give C = K
  * exactly (the all-ones check of "CUDA 性能优化实战笔记 + C++示例代码（第七章
@@ -208,6 +214,78 @@ int oracle_sgemm_f64_at(int64_t M, int64_t N, int64_t K, const float *A, int64_t
         }
         c64[t] = sum;
         if (s) s[t] = abs_sum;
+    }
+    return 0;
+}
+
+/* Element (r, c) of op(X) for a row-major X with row stride ld. */
+static double op_at(const float *X, int64_t ld, int trans, int64_t r, int64_t c)
+{
+    return trans ? (double)X[c * ld + r] : (double)X[r * ld + c];
+}
+
+static int gemm_args_ok(int transA, int transB, int64_t M, int64_t N, int64_t K, const void *A,
+                        int64_t lda, const void *B, int64_t ldb)
+{
+    if (M < 0 || N < 0 || K < 0) return 0;
+    if ((transA && lda < M) || (!transA && lda < K)) return 0;
+    if ((transB && ldb < K) || (!transB && ldb < N)) return 0;
+    if (M > 0 && K > 0 && A == NULL) return 0;
+    if (K > 0 && N > 0 && B == NULL) return 0;
+    return 1;
+}
+
+/* One element of alpha * op(A) * op(B) + beta * C_in and its error scale. */
+static void gemm_element(int transA, int transB, int64_t K, double alpha, const float *A,
+                         int64_t lda, const float *B, int64_t ldb, double beta, double c_in,
+                         int64_t i, int64_t j, double *c, double *s)
+{
+    double sum = 0.0, abs_sum = 0.0;
+    for (int64_t k = 0; k < K; ++k) {
+        double a = op_at(A, lda, transA, i, k);
+        double b = op_at(B, ldb, transB, k, j);
+        sum = sum + a * b;
+        abs_sum = abs_sum + fabs(a) * fabs(b);
+    }
+    double out = alpha * sum, scale = fabs(alpha) * abs_sum;
+    if (beta != 0.0) {
+        out = out + beta * c_in;
+        scale = scale + fabs(beta) * fabs(c_in);
+    }
+    *c = out;
+    if (s) *s = scale;
+}
+
+int oracle_gemm_f64(int transA, int transB, int64_t M, int64_t N, int64_t K, double alpha,
+                    const float *A, int64_t lda, const float *B, int64_t ldb, double beta,
+                    const float *C_in, int64_t ldc_in, double *C64, double *S, int64_t ldc)
+{
+    if (!gemm_args_ok(transA, transB, M, N, K, A, lda, B, ldb)) return 1;
+    if (ldc < N || (M > 0 && N > 0 && C64 == NULL)) return 1;
+    if (beta != 0.0 && M > 0 && N > 0 && (C_in == NULL || ldc_in < N)) return 1;
+    for (int64_t i = 0; i < M; ++i)
+        for (int64_t j = 0; j < N; ++j) {
+            double c_in = beta != 0.0 ? (double)C_in[i * ldc_in + j] : 0.0;
+            gemm_element(transA, transB, K, alpha, A, lda, B, ldb, beta, c_in, i, j,
+                         &C64[i * ldc + j], S ? &S[i * ldc + j] : NULL);
+        }
+    return 0;
+}
+
+int oracle_gemm_f64_at(int transA, int transB, int64_t M, int64_t N, int64_t K, double alpha,
+                       const float *A, int64_t lda, const float *B, int64_t ldb, double beta,
+                       const float *C_in, int64_t ldc_in, int64_t n_samples, const int64_t *rows,
+                       const int64_t *cols, double *c64, double *s)
+{
+    if (!gemm_args_ok(transA, transB, M, N, K, A, lda, B, ldb) || n_samples < 0) return 1;
+    if (n_samples > 0 && (!rows || !cols || !c64)) return 1;
+    if (beta != 0.0 && n_samples > 0 && (C_in == NULL || ldc_in < N)) return 1;
+    for (int64_t t = 0; t < n_samples; ++t) {
+        int64_t i = rows[t], j = cols[t];
+        if (i < 0 || i >= M || j < 0 || j >= N) return 1;
+        double c_in = beta != 0.0 ? (double)C_in[i * ldc_in + j] : 0.0;
+        gemm_element(transA, transB, K, alpha, A, lda, B, ldb, beta, c_in, i, j, &c64[t],
+                     s ? &s[t] : NULL);
     }
     return 0;
 }

@@ -32,6 +32,20 @@ int oracle_sgemm_f64_at(int64_t M, int64_t N, int64_t K, const float *A, int64_t
                         const float *B, int64_t ldb, int64_t n_samples, const int64_t *rows,
                         const int64_t *cols, double *c64, double *s);
 
+/* C64 = alpha * op(A) * op(B) + beta * C_in in double (op = matrix or its
+ * transpose; trans = 0 or 1; A is M x K, or K x M when transA; B is K x N, or
+ * N x K when transB; all row-major). S = |alpha| sum_k |op(A)||op(B)| +
+ * |beta| |C_in|. beta == 0: C_in is not read. */
+int oracle_gemm_f64(int transA, int transB, int64_t M, int64_t N, int64_t K, double alpha,
+                    const float *A, int64_t lda, const float *B, int64_t ldb, double beta,
+                    const float *C_in, int64_t ldc_in, double *C64, double *S, int64_t ldc);
+
+/* The same at n_samples (rows[t], cols[t]) positions. */
+int oracle_gemm_f64_at(int transA, int transB, int64_t M, int64_t N, int64_t K, double alpha,
+                       const float *A, int64_t lda, const float *B, int64_t ldb, double beta,
+                       const float *C_in, int64_t ldc_in, int64_t n_samples, const int64_t *rows,
+                       const int64_t *cols, double *c64, double *s);
+
 #ifdef __cplusplus
 }
 #endif
