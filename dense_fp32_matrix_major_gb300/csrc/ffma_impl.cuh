@@ -1,0 +1,416 @@
+// Register-blocked fp32 FFMA kernel family: the template shared by the
+// translation units that instantiate it (sgemm_ffma.cu: op(A) = A,
+// op(B) = B; sgemm_ffma_t.cu: the transposed forms). The design notes are at
+// the top of sgemm_ffma.cu.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "sgemm.h"
+#include "sgemm_internal.h"
+
+namespace sgemm {
+namespace ffma {
+
+struct FfmaArgs {
+    int64_t M, N, K;
+    const float *A;
+    int64_t lda;
+    const float *B;
+    int64_t ldb;
+    float *C;
+    int64_t ldc;
+    float alpha, beta;  // C = alpha * op(A) op(B) + beta * C; beta == 0: C not read
+    int vec_a;          // op(A) = A^T and its rows allow 16-byte copies
+    int vec_c;          // C rows allow 16-byte stores (used when VEC_C is not set)
+    int tiles_n;        // tiles along N (tiles are numbered row-major over the tile grid)
+    int k_tiles;        // ceil(K / BK)
+    int dp_tiles;       // tiles [0, dp_tiles) go round-robin to CTAs, whole
+    int total_tiles;    // tiles [dp_tiles, total_tiles) are split along K
+    int64_t sk_iters;   // (total_tiles - dp_tiles) * k_tiles
+    int sk_ctas;        // CTAs [0, sk_ctas) share the split iterations evenly
+};
+
+template <int WARPS_M_, int WARPS_N_, int CN_, int STAGES_, int MIN_BLOCKS_, int KU_>
+struct Cfg {
+    static constexpr int WARPS_M = WARPS_M_, WARPS_N = WARPS_N_, CN = CN_, STAGES = STAGES_;
+    static constexpr int KU = KU_;  // k-steps unrolled per pass of the inner loop (8 or 16)
+    static constexpr int MIN_BLOCKS = MIN_BLOCKS_;  // resident CTAs per SM the registers must allow
+    static constexpr int BK = 16;
+    static constexpr int THREADS = 32 * WARPS_M * WARPS_N;
+    static constexpr int WM = 64;       // warp tile rows: 8 lanes x 2 groups x 4 rows
+    static constexpr int WN = 16 * CN;  // warp tile cols: 4 lanes x CN chunks x 4 cols
+    static constexpr int BM = WM * WARPS_M;
+    static constexpr int BN = WN * WARPS_N;
+    static constexpr int TN = 4 * CN;
+    static constexpr int A_STAGE = BK * BM;  // floats
+    static constexpr int B_STAGE = BK * BN;
+    static constexpr int SMEM_BYTES = STAGES * (A_STAGE + B_STAGE) * 4;
+    static constexpr int A_PER_THREAD = BM * BK / THREADS;
+    static constexpr int A4_PER_THREAD = BM * BK / 4 / THREADS;
+    static constexpr int B_PER_THREAD = BK * BN / THREADS;
+    static constexpr int B4_PER_THREAD = BK * BN / 4 / THREADS;
+    static_assert(BM * BK / 4 % THREADS == 0, "A tile must split evenly over threads");
+    static_assert(BK * BN / 4 % THREADS == 0, "B tile must split evenly over threads");
+};
+
+using CfgBig = Cfg<2, 4, 4, 4, 1, 8>;     // 128 x 256, 256 threads, 8 x 16 per thread
+using CfgMid = Cfg<2, 4, 2, 4, 2, 16>;    // 128 x 128, 256 threads, 8 x 8 per thread
+using CfgSmall = Cfg<1, 2, 2, 3, 6, 16>;  // 64 x 64, 64 threads, 8 x 8 per thread
+
+__host__ __device__ __forceinline__ int64_t min64(int64_t x, int64_t y) { return x < y ? x : y; }
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// 4-byte asynchronous copy; src_bytes 0 writes a zero.
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const float *src, int src_bytes) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(dst), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+
+// 16-byte asynchronous copy of src_bytes (0..16) bytes; the rest is zero-filled.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const float *src, int src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
+// Position of op(A) element (m, k) in one stage of As: k-major rows of BM,
+// 16-byte groups XOR-swizzled by (k & 7) so the transposing 4-byte copies
+// spread over the banks and 4 consecutive m stay one aligned float4.
+template <class C>
+__device__ __forceinline__ int as_index(int k, int m) {
+    return k * C::BM + (m ^ ((k & 7) << 2));
+}
+
+// Position of op(B) element (k, n) in one stage of Bs: k-major rows of BN,
+// swizzled the same way when op(B) = B^T (the copies transpose).
+template <class C, bool TB>
+__device__ __forceinline__ int bs_index(int k, int n) {
+    return k * C::BN + (TB ? (n ^ ((k & 7) << 2)) : n);
+}
+
+template <class C, bool TA, bool TB, bool VEC_B>
+__device__ __forceinline__ void load_stage(const FfmaArgs &a, float *As, float *Bs, int64_t m0,
+                                           int64_t n0, int64_t k0, int tid) {
+    constexpr int BK = C::BK;
+    if constexpr (!TA) {
+        // A is M x K: 4 consecutive threads read one row along k; copies transpose.
+#pragma unroll
+        for (int r = 0; r < C::A_PER_THREAD; ++r) {
+            const int e = r * C::THREADS + tid;
+            const int m = e / BK, k = e % BK;
+            const int64_t gm = m0 + m, gk = k0 + k;
+            const bool ok = gm < a.M && gk < a.K;
+            const float *src = ok ? a.A + gm * a.lda + gk : a.A;
+            cp_async_4(smem_addr(As + as_index<C>(k, m)), src, ok ? 4 : 0);
+        }
+    } else if (a.vec_a) {
+        // A is stored K x M: rows of As come straight from rows of A, 16 bytes at a time.
+#pragma unroll
+        for (int r = 0; r < C::A4_PER_THREAD; ++r) {
+            const int e = r * C::THREADS + tid;
+            const int k = e / (C::BM / 4), m = (e % (C::BM / 4)) * 4;
+            const int64_t gk = k0 + k, gm = m0 + m;
+            int bytes = 0;
+            if (gk < a.K && gm < a.M) bytes = static_cast<int>(min64(4, a.M - gm)) * 4;
+            const float *src = bytes ? a.A + gk * a.lda + gm : a.A;
+            cp_async_16(smem_addr(As + as_index<C>(k, m)), src, bytes);
+        }
+    } else {
+#pragma unroll
+        for (int r = 0; r < C::A_PER_THREAD; ++r) {
+            const int e = r * C::THREADS + tid;
+            const int k = e / C::BM, m = e % C::BM;
+            const int64_t gk = k0 + k, gm = m0 + m;
+            const bool ok = gk < a.K && gm < a.M;
+            const float *src = ok ? a.A + gk * a.lda + gm : a.A;
+            cp_async_4(smem_addr(As + as_index<C>(k, m)), src, ok ? 4 : 0);
+        }
+    }
+    if constexpr (TB) {
+        // B is stored N x K: consecutive threads read along k; copies transpose.
+#pragma unroll
+        for (int r = 0; r < C::B_PER_THREAD; ++r) {
+            const int e = r * C::THREADS + tid;
+            const int n = e / BK, k = e % BK;
+            const int64_t gn = n0 + n, gk = k0 + k;
+            const bool ok = gk < a.K && gn < a.N;
+            const float *src = ok ? a.B + gn * a.ldb + gk : a.B;
+            cp_async_4(smem_addr(Bs + bs_index<C, TB>(k, n)), src, ok ? 4 : 0);
+        }
+    } else if constexpr (VEC_B) {
+#pragma unroll
+        for (int r = 0; r < C::B4_PER_THREAD; ++r) {
+            const int e = r * C::THREADS + tid;
+            const int k = e / (C::BN / 4), n = (e % (C::BN / 4)) * 4;
+            const int64_t gk = k0 + k, gn = n0 + n;
+            int bytes = 0;
+            if (gk < a.K && gn < a.N) bytes = static_cast<int>(min64(4, a.N - gn)) * 4;
+            const float *src = bytes ? a.B + gk * a.ldb + gn : a.B;
+            cp_async_16(smem_addr(Bs + bs_index<C, TB>(k, n)), src, bytes);
+        }
+    } else {
+#pragma unroll
+        for (int r = 0; r < C::B_PER_THREAD; ++r) {
+            const int e = r * C::THREADS + tid;
+            const int k = e / C::BN, n = e % C::BN;
+            const int64_t gk = k0 + k, gn = n0 + n;
+            const bool ok = gk < a.K && gn < a.N;
+            const float *src = ok ? a.B + gk * a.ldb + gn : a.B;
+            cp_async_4(smem_addr(Bs + bs_index<C, TB>(k, n)), src, ok ? 4 : 0);
+        }
+    }
+}
+
+// One tile over k-tiles [kb, ke). atomic: add alpha * the partial sum into C
+// (C was scaled by beta beforehand) instead of storing.
+template <class C, bool TA, bool TB, bool VEC_B, bool VEC_C>
+__device__ __forceinline__ void process_tile(const FfmaArgs &a, float *As, float *Bs, int tile, int kb,
+                                             int ke, bool atomic) {
+    constexpr int BK = C::BK, S = C::STAGES, TN = C::TN;
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int wm0 = (warp / C::WARPS_N) * C::WM;
+    const int wn0 = (warp % C::WARPS_N) * C::WN;
+    const int tm = lane >> 2, tn = lane & 3;
+    const int64_t m0 = static_cast<int64_t>(tile / a.tiles_n) * C::BM;
+    const int64_t n0 = static_cast<int64_t>(tile % a.tiles_n) * C::BN;
+    const int nk = ke - kb;
+
+    float acc[8][TN];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < TN; ++j) acc[i][j] = 0.0f;
+
+    __syncthreads();  // the previous tile of this CTA is done with the ring
+#pragma unroll
+    for (int s = 0; s < S - 1; ++s) {
+        if (s < nk)
+            load_stage<C, TA, TB, VEC_B>(a, As + s * C::A_STAGE, Bs + s * C::B_STAGE, m0, n0,
+                                         static_cast<int64_t>(kb + s) * BK, tid);
+        cp_async_commit();
+    }
+
+    for (int t = 0; t < nk; ++t) {
+        cp_async_wait<S - 2>();
+        __syncthreads();
+        {
+            const int tl = t + S - 1;
+            if (tl < nk) {
+                const int sl = tl % S;
+                load_stage<C, TA, TB, VEC_B>(a, As + sl * C::A_STAGE, Bs + sl * C::B_STAGE, m0, n0,
+                                             static_cast<int64_t>(kb + tl) * BK, tid);
+            }
+            cp_async_commit();
+        }
+        const float *as = As + (t % S) * C::A_STAGE;
+        const float *bs = Bs + (t % S) * C::B_STAGE;
+        // Rolled passes of KU unrolled k-steps. With the 8 x 16 register tile a
+        // full unroll of BK = 16 overflows the instruction cache, so that
+        // configuration runs two passes of 8; the swizzle term
+        // ((k8 + kk) & 7 = kk & 7) stays a compile-time constant.
+#pragma unroll 1
+        for (int k8 = 0; k8 < BK; k8 += C::KU)
+#pragma unroll
+        for (int kk = 0; kk < C::KU; ++kk) {
+            float av[8], bv[TN];
+#pragma unroll
+            for (int g = 0; g < 2; ++g) {
+                const float4 v = *reinterpret_cast<const float4 *>(
+                    as + (k8 + kk) * C::BM + ((wm0 + g * 32 + tm * 4) ^ ((kk & 7) << 2)));
+                av[g * 4 + 0] = v.x;
+                av[g * 4 + 1] = v.y;
+                av[g * 4 + 2] = v.z;
+                av[g * 4 + 3] = v.w;
+            }
+#pragma unroll
+            for (int c = 0; c < C::CN; ++c) {
+                const int n = wn0 + c * 16 + tn * 4;
+                const float4 v = *reinterpret_cast<const float4 *>(
+                    bs + (k8 + kk) * C::BN + (TB ? (n ^ ((kk & 7) << 2)) : n));
+                bv[c * 4 + 0] = v.x;
+                bv[c * 4 + 1] = v.y;
+                bv[c * 4 + 2] = v.z;
+                bv[c * 4 + 3] = v.w;
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+#pragma unroll
+                for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+        }
+    }
+    cp_async_wait<0>();
+
+    // Epilogue: rows wm0 + g*32 + tm*4 + r, columns wn0 + c*16 + tn*4 + q.
+    const float alpha = a.alpha, beta = a.beta;
+    const bool vec_c = VEC_C || a.vec_c;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int64_t row = m0 + wm0 + (i >> 2) * 32 + tm * 4 + (i & 3);
+        if (row >= a.M) continue;
+        float *crow = a.C + row * a.ldc;
+#pragma unroll
+        for (int c = 0; c < C::CN; ++c) {
+            const int64_t col = n0 + wn0 + c * 16 + tn * 4;
+            if (col >= a.N) continue;
+            float v[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) v[q] = alpha * acc[i][c * 4 + q];
+            if (atomic) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    if (col + q < a.N) atomicAdd(crow + col + q, v[q]);
+            } else if (vec_c && col + 3 < a.N) {
+                float4 *p = reinterpret_cast<float4 *>(crow + col);
+                if (beta != 0.0f) {
+                    const float4 o = *p;
+                    v[0] = fmaf(beta, o.x, v[0]);
+                    v[1] = fmaf(beta, o.y, v[1]);
+                    v[2] = fmaf(beta, o.z, v[2]);
+                    v[3] = fmaf(beta, o.w, v[3]);
+                }
+                *p = make_float4(v[0], v[1], v[2], v[3]);
+            } else {
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    if (col + q < a.N) crow[col + q] = beta != 0.0f ? fmaf(beta, crow[col + q], v[q]) : v[q];
+            }
+        }
+    }
+}
+
+template <class C, bool TA, bool TB, bool VEC_B, bool VEC_C>
+__global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS) ffma_kernel(const FfmaArgs a) {
+    extern __shared__ float4 smem_f4[];
+    float *As = reinterpret_cast<float *>(smem_f4);
+    float *Bs = As + C::STAGES * C::A_STAGE;
+
+    for (int t = blockIdx.x; t < a.dp_tiles; t += gridDim.x)
+        process_tile<C, TA, TB, VEC_B, VEC_C>(a, As, Bs, t, 0, a.k_tiles, false);
+
+    if (static_cast<int>(blockIdx.x) < a.sk_ctas) {
+        int64_t it = a.sk_iters * blockIdx.x / a.sk_ctas;
+        const int64_t end = a.sk_iters * (blockIdx.x + 1) / a.sk_ctas;
+        while (it < end) {
+            const int tile = a.dp_tiles + static_cast<int>(it / a.k_tiles);
+            const int kb = static_cast<int>(it % a.k_tiles);
+            const int ke = static_cast<int>(min64(a.k_tiles, kb + (end - it)));
+            // Stream-K tiles were scaled by beta beforehand: every unit adds,
+            // also one that happens to cover the whole K range.
+            process_tile<C, TA, TB, VEC_B, VEC_C>(a, As, Bs, tile, kb, ke, true);
+            it += ke - kb;
+        }
+    }
+}
+
+// ------------------------------------------------------------------ host side
+
+constexpr int kMaxDevices = 64;
+
+struct KernelSlot {
+    std::once_flag once[kMaxDevices];
+    int ctas_per_sm[kMaxDevices];
+    cudaError_t err[kMaxDevices];
+};
+
+template <class C, bool TA, bool TB, bool VEC_B, bool VEC_C>
+KernelSlot &slot() {
+    static KernelSlot s;
+    return s;
+}
+
+template <class C, bool TA, bool TB, bool VEC_B, bool VEC_C>
+int occupancy(const DeviceInfo &dev, int *ctas_per_sm) {
+    if (dev.device < 0 || dev.device >= kMaxDevices) return SGEMM_ERR_DEVICE;
+    KernelSlot &s = slot<C, TA, TB, VEC_B, VEC_C>();
+    std::call_once(s.once[dev.device], [&] {
+        auto fn = ffma_kernel<C, TA, TB, VEC_B, VEC_C>;
+        cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+        int n = 0;
+        if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, C::THREADS, C::SMEM_BYTES);
+        s.err[dev.device] = e;
+        s.ctas_per_sm[dev.device] = n;
+    });
+    if (s.err[dev.device] != cudaSuccess || s.ctas_per_sm[dev.device] < 1) {
+        cudaGetLastError();
+        return SGEMM_ERR_LAUNCH;
+    }
+    *ctas_per_sm = s.ctas_per_sm[dev.device];
+    return SGEMM_OK;
+}
+
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+template <class C, bool TA, bool TB, bool VEC_B, bool VEC_C>
+int launch_cfg(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStream_t stream, int *launches) {
+    int per_sm = 0;
+    int rc = occupancy<C, TA, TB, VEC_B, VEC_C>(dev, &per_sm);
+    if (rc != SGEMM_OK) return rc;
+
+    const int64_t tiles_m = ceil_div(p.M, C::BM), tiles_n = ceil_div(p.N, C::BN);
+    const int64_t tiles64 = tiles_m * tiles_n;
+    const int64_t k_tiles = ceil_div(p.K, C::BK);
+    if (tiles64 > INT32_MAX / 2 || k_tiles > INT32_MAX / 2) return SGEMM_ERR_UNSUPPORTED;
+    const int tiles = static_cast<int>(tiles64);
+    const int slots = dev.sm_count * per_sm;
+    // A stream-K share below this many k-steps costs more in fix-up than it saves.
+    const Schedule sch = make_schedule(tiles, k_tiles, slots, sk_mode, 8);
+
+    FfmaArgs a;
+    a.M = p.M;
+    a.N = p.N;
+    a.K = p.K;
+    a.A = p.A;
+    a.lda = p.lda;
+    a.B = p.B;
+    a.ldb = p.ldb;
+    a.C = p.C;
+    a.ldc = p.ldc;
+    a.alpha = p.alpha;
+    a.beta = p.beta;
+    a.vec_a = (p.lda % 4 == 0) && (reinterpret_cast<uintptr_t>(p.A) % 16 == 0);
+    a.vec_c = (p.ldc % 4 == 0) && (reinterpret_cast<uintptr_t>(p.C) % 16 == 0);
+    a.tiles_n = static_cast<int>(tiles_n);
+    a.k_tiles = static_cast<int>(k_tiles);
+    a.total_tiles = tiles;
+    a.dp_tiles = sch.dp_tiles;
+    a.sk_iters = sch.sk_iters;
+    a.sk_ctas = sch.sk_ctas;
+    if (tiles > sch.dp_tiles) {
+        rc = scale_tiles_launch(p.C, p.M, p.N, p.ldc, p.beta, C::BM, C::BN, a.tiles_n, sch.dp_tiles,
+                                tiles - sch.dp_tiles, stream, launches);
+        if (rc != SGEMM_OK) return rc;
+    }
+    ffma_kernel<C, TA, TB, VEC_B, VEC_C><<<sch.grid, C::THREADS, C::SMEM_BYTES, stream>>>(a);
+    ++*launches;
+    return cudaGetLastError() == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
+}
+
+// Block tile for AUTO: large outputs take the widest register tile (fewest
+// shared-memory loads per FFMA); small outputs smaller tiles so the grid
+// covers the SMs.
+inline int pick_tile(const Problem &p, const DeviceInfo &dev, int tile) {
+    if (tile != FFMA_TILE_AUTO) return tile;
+    const int64_t big_tiles = ceil_div(p.M, CfgBig::BM) * ceil_div(p.N, CfgBig::BN);
+    const int64_t mid_tiles = ceil_div(p.M, CfgMid::BM) * ceil_div(p.N, CfgMid::BN);
+    if (big_tiles >= dev.sm_count) return FFMA_TILE_128x256;
+    if (mid_tiles >= dev.sm_count / 2) return FFMA_TILE_128x128;
+    return FFMA_TILE_64x64;
+}
+
+}  // namespace ffma
+}  // namespace sgemm

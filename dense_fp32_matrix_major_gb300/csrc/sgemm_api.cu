@@ -60,20 +60,25 @@ bool overlaps(const void *x, int64_t xr, int64_t xc, int64_t xld, const void *y,
     return a0 < b1 && b0 < a1;
 }
 
-int check_args(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, const float *B, int64_t ldb,
-               const float *C, int64_t ldc) {
+int check_args(int transA, int transB, int64_t M, int64_t N, int64_t K, const float *A, int64_t lda,
+               const float *B, int64_t ldb, const float *C, int64_t ldc) {
+    if (transA != SGEMM_OP_N && transA != SGEMM_OP_T) return SGEMM_ERR_INVALID_ARG;
+    if (transB != SGEMM_OP_N && transB != SGEMM_OP_T) return SGEMM_ERR_INVALID_ARG;
     if (M < 0 || N < 0 || K < 0) return SGEMM_ERR_INVALID_ARG;
-    if (lda < K || ldb < N || ldc < N) return SGEMM_ERR_INVALID_ARG;
+    // Stored shapes: A is M x K (K x M when transposed), B is K x N (N x K).
+    const int64_t a_rows = transA ? K : M, a_cols = transA ? M : K;
+    const int64_t b_rows = transB ? N : K, b_cols = transB ? K : N;
+    if (lda < a_cols || ldb < b_cols || ldc < N) return SGEMM_ERR_INVALID_ARG;
     if (lda < 1 || ldb < 1 || ldc < 1) return SGEMM_ERR_INVALID_ARG;
     // Element offsets must fit in int64 with room to spare.
     const int64_t lim = INT64_C(1) << 60;
-    if ((M > 0 && lda > lim / M) || (K > 0 && ldb > lim / K) || (M > 0 && ldc > lim / M))
+    if ((a_rows > 0 && lda > lim / a_rows) || (b_rows > 0 && ldb > lim / b_rows) || (M > 0 && ldc > lim / M))
         return SGEMM_ERR_INVALID_ARG;
     if (M > 0 && K > 0 && !A) return SGEMM_ERR_INVALID_ARG;
     if (K > 0 && N > 0 && !B) return SGEMM_ERR_INVALID_ARG;
     if (M > 0 && N > 0 && !C) return SGEMM_ERR_INVALID_ARG;
     if (M > 0 && N > 0) {
-        if (overlaps(C, M, N, ldc, A, M, K, lda) || overlaps(C, M, N, ldc, B, K, N, ldb))
+        if (overlaps(C, M, N, ldc, A, a_rows, a_cols, lda) || overlaps(C, M, N, ldc, B, b_rows, b_cols, ldb))
             return SGEMM_ERR_INVALID_ARG;
     }
     return SGEMM_OK;
@@ -100,8 +105,9 @@ int enqueue(const Problem &p, cudaStream_t stream) {
         g_last_launches.store(0);
         return SGEMM_OK;
     }
-    if (p.K == 0) {
-        rc = zero_launch(p.C, p.M, p.N, p.ldc, dev, stream, &launches);
+    if (p.K == 0 || p.alpha == 0.0f) {
+        // The empty sum (or alpha = 0): C = beta * C.
+        rc = scale_launch(p.C, p.M, p.N, p.ldc, p.beta, dev, stream, &launches);
         if (rc == SGEMM_OK) {
             g_last_variant.store(SGEMM_FFMA);
             g_last_launches.store(launches);
@@ -162,9 +168,22 @@ extern "C" {
 
 int sgemm_f32(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, const float *B, int64_t ldb,
               float *C, int64_t ldc, sgemm_stream_t stream) {
-    int rc = sgemm::check_args(M, N, K, A, lda, B, ldb, C, ldc);
+    int rc = sgemm::check_args(SGEMM_OP_N, SGEMM_OP_N, M, N, K, A, lda, B, ldb, C, ldc);
     if (rc != SGEMM_OK) return rc;
     Problem p{M, N, K, A, lda, B, ldb, C, ldc};
+    return sgemm::enqueue(p, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int sgemm_f32_ex(int transA, int transB, int64_t M, int64_t N, int64_t K, float alpha, const float *A,
+                 int64_t lda, const float *B, int64_t ldb, float beta, float *C, int64_t ldc,
+                 sgemm_stream_t stream) {
+    int rc = sgemm::check_args(transA, transB, M, N, K, A, lda, B, ldb, C, ldc);
+    if (rc != SGEMM_OK) return rc;
+    Problem p{M, N, K, A, lda, B, ldb, C, ldc};
+    p.transA = transA;
+    p.transB = transB;
+    p.alpha = alpha;
+    p.beta = beta;
     return sgemm::enqueue(p, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -181,7 +200,7 @@ static cudaError_t copy_rows(float *dst, const float *src, int64_t rows, int64_t
 int sgemm_f32_from_host(int64_t M, int64_t N, int64_t K, const float *A_host, int64_t lda,
                         const float *B_host, int64_t ldb, float *C_host, int64_t ldc, float *dA, float *dB,
                         float *dC, sgemm_stream_t stream) {
-    int rc = sgemm::check_args(M, N, K, dA, lda, dB, ldb, dC, ldc);
+    int rc = sgemm::check_args(SGEMM_OP_N, SGEMM_OP_N, M, N, K, dA, lda, dB, ldb, dC, ldc);
     if (rc != SGEMM_OK) return rc;
     if ((M > 0 && K > 0 && !A_host) || (K > 0 && N > 0 && !B_host) || (M > 0 && N > 0 && !C_host))
         return SGEMM_ERR_INVALID_ARG;

@@ -7,8 +7,10 @@
 
 namespace sgemm {
 
-// One product request after argument checks: all pointers are device
-// pointers, strides are in elements, M, N, K > 0.
+// One product request after argument checks: C = alpha * op(A) * op(B) +
+// beta * C with op(X) = X or X^T (transA / transB); all pointers are device
+// pointers, strides are in elements, M, N, K > 0 and alpha != 0. A is stored
+// M x K (K x M when transA), B is stored K x N (N x K when transB).
 struct Problem {
     int64_t M, N, K;
     const float *A;
@@ -17,6 +19,8 @@ struct Problem {
     int64_t ldb;
     float *C;
     int64_t ldc;
+    int transA = 0, transB = 0;
+    float alpha = 1.0f, beta = 0.0f;
 };
 
 // Properties of the current device that the launchers need.
@@ -76,18 +80,23 @@ inline Schedule make_schedule(int tiles, int64_t k_steps, int slots, int mode, i
     return s;
 }
 
-// Enqueue a kernel that zeroes the C region of `count` tiles starting at
-// tile `first_tile` of a bm x bn tile grid with tiles_n tiles per row.
-int zero_tiles_launch(float *C, int64_t M, int64_t N, int64_t ldc, int bm, int bn, int tiles_n, int first_tile,
-                      int count, cudaStream_t stream, int *launches);
+// Enqueue a kernel that sets C = beta * C (C = 0 when beta = 0, without
+// reading C) over `count` tiles starting at tile `first_tile` of a bm x bn
+// tile grid with tiles_n tiles per row.
+int scale_tiles_launch(float *C, int64_t M, int64_t N, int64_t ldc, float beta, int bm, int bn, int tiles_n,
+                       int first_tile, int count, cudaStream_t stream, int *launches);
 
 // Enqueue the FFMA product. `launches` receives the number of kernels enqueued.
 int ffma_launch(const Problem &p, const DeviceInfo &dev, int tile, int sk_mode, cudaStream_t stream,
                 int *launches);
+// The transposed forms (op(A) = A^T and/or op(B) = B^T).
+int ffma_launch_t(const Problem &p, const DeviceInfo &dev, int tile, int sk_mode, cudaStream_t stream,
+                  int *launches);
 
-// Enqueue C[0:M, 0:N] = 0 (the empty sum).
-int zero_launch(float *C, int64_t M, int64_t N, int64_t ldc, const DeviceInfo &dev,
-                cudaStream_t stream, int *launches);
+// Enqueue C[0:M, 0:N] = beta * C (0 when beta = 0): the result when K = 0
+// (the empty sum) or alpha = 0.
+int scale_launch(float *C, int64_t M, int64_t N, int64_t ldc, float beta, const DeviceInfo &dev,
+                 cudaStream_t stream, int *launches);
 
 // Tensor-core three-term TF32 variant. Returns SGEMM_ERR_UNSUPPORTED when it
 // cannot run the request.

@@ -96,6 +96,7 @@ struct Args {
     int64_t sk_iters;
     uint64_t timeout_ns;
     int *watchdog;
+    float alpha = 1.0f, beta = 0.0f;  // C = alpha * op(A) op(B) + beta * C; beta == 0: C not read
 };
 
 // Instruction descriptor of tcgen05.mma kind::tf32: D fp32 (bits 4-5 = 1),
@@ -236,6 +237,12 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
+__device__ __forceinline__ float ld_shared_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+
 __device__ __forceinline__ float4 ld_shared_v4(uint32_t addr) {
     float4 v;
     asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
@@ -320,6 +327,40 @@ __device__ __forceinline__ void split_store(uint32_t hi_addr, uint32_t lo_addr, 
 // Byte offset of 16-byte chunk `chunk` of row `row` in a 128-byte-swizzled tile.
 __device__ __forceinline__ uint32_t sw128_offset(int row, int chunk) {
     return static_cast<uint32_t>(row * 128 + ((chunk ^ (row & 7)) << 4));
+}
+
+// Writes 32 accumulator values (columns col0 .. col0 + 31 of one row of C):
+// C = alpha * v + beta * C (C read only when beta != 0), or, for a tile split
+// along K (C already scaled by beta), C += alpha * v with atomics.
+template <bool VEC_C>
+__device__ __forceinline__ void store_chunk(const Args &a, float *crow, int64_t row, int64_t col0, const float (&v)[32],
+                                            bool atomic) {
+    if (row >= a.M || col0 >= a.N) return;
+    const float alpha = a.alpha, beta = a.beta;
+    if (atomic) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            if (col0 + j < a.N) atomicAdd(crow + col0 + j, alpha * v[j]);
+    } else if (VEC_C && col0 + 31 < a.N) {
+#pragma unroll
+        for (int j = 0; j < 32; j += 4) {
+            float4 *p = reinterpret_cast<float4 *>(crow + col0 + j);
+            float4 o = make_float4(alpha * v[j], alpha * v[j + 1], alpha * v[j + 2], alpha * v[j + 3]);
+            if (beta != 0.0f) {
+                const float4 c = *p;
+                o.x = fmaf(beta, c.x, o.x);
+                o.y = fmaf(beta, c.y, o.y);
+                o.z = fmaf(beta, c.z, o.z);
+                o.w = fmaf(beta, c.w, o.w);
+            }
+            *p = o;
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            if (col0 + j < a.N)
+                crow[col0 + j] = beta != 0.0f ? fmaf(beta, crow[col0 + j], alpha * v[j]) : alpha * v[j];
+    }
 }
 
 // Calls f(tile, kb, ke) for this CTA's units of work, in order.
@@ -573,29 +614,15 @@ __global__ void __launch_bounds__(THREADS, 1) tf32x3_kernel(const Args a) {
             const int64_t m0 = static_cast<int64_t>(tile / a.tiles_n) * BM;
             const int64_t n0 = static_cast<int64_t>(tile % a.tiles_n) * BN;
             const int64_t row = m0 + q * 32 + lane;
-            const bool atomic = !(kb == 0 && ke == a.k_blocks);
+            // Stream-K tiles were scaled by beta beforehand: every unit adds.
+            const bool atomic = tile >= a.dp_tiles;
             float *crow = a.C + row * a.ldc;
 #pragma unroll 1
             for (int ch = 0; ch < BN / 32; ++ch) {
                 float v[32];
                 tmem_load32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * BN + ch * 32),
                             v);
-                const int64_t col0 = n0 + ch * 32;
-                if (row < a.M && col0 < a.N) {
-                    if (atomic) {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            if (col0 + j < a.N) atomicAdd(crow + col0 + j, v[j]);
-                    } else if (VEC_C && col0 + 31 < a.N) {
-#pragma unroll
-                        for (int j = 0; j < 32; j += 4)
-                            *reinterpret_cast<float4 *>(crow + col0 + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            if (col0 + j < a.N) crow[col0 + j] = v[j];
-                    }
-                }
+                store_chunk<VEC_C>(a, crow, row, n0 + ch * 32, v, atomic);
             }
             tc_fence_before();
             mbar_arrive(bar(6 + buf));
@@ -838,29 +865,15 @@ __global__ void __launch_bounds__(tma::THREADS, 1)
             const int64_t m0 = static_cast<int64_t>(tile / a.tiles_n) * BM;
             const int64_t n0 = static_cast<int64_t>(tile % a.tiles_n) * BN;
             const int64_t row = m0 + q * 32 + lane;
-            const bool atomic = !(kb == 0 && ke == a.k_blocks);
+            // Stream-K tiles were scaled by beta beforehand: every unit adds.
+            const bool atomic = tile >= a.dp_tiles;
             float *crow = a.C + row * a.ldc;
 #pragma unroll 1
             for (int ch = 0; ch < BN / 32; ++ch) {
                 float v[32];
                 tmem_load32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * BN + ch * 32),
                             v);
-                const int64_t col0 = n0 + ch * 32;
-                if (row < a.M && col0 < a.N) {
-                    if (atomic) {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            if (col0 + j < a.N) atomicAdd(crow + col0 + j, v[j]);
-                    } else if (VEC_C && col0 + 31 < a.N) {
-#pragma unroll
-                        for (int j = 0; j < 32; j += 4)
-                            *reinterpret_cast<float4 *>(crow + col0 + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            if (col0 + j < a.N) crow[col0 + j] = v[j];
-                    }
-                }
+                store_chunk<VEC_C>(a, crow, row, n0 + ch * 32, v, atomic);
             }
             tc_fence_before();
             mbar_arrive(bar(6 + buf));
@@ -908,7 +921,7 @@ static_assert(CONV_WARPS == 16, "four converter warps per TMEM lane quarter, 8 k
 
 }  // namespace tm3
 
-template <bool VEC_C>
+template <bool VEC_C, bool TA, bool TB>
 __global__ void __launch_bounds__(tm3::THREADS, 1)
     tf32x3_tmem_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const Args a) {
     extern __shared__ uint8_t smem_raw[];
@@ -1004,8 +1017,17 @@ __global__ void __launch_bounds__(tm3::THREADS, 1)
                     }
                     const uint32_t sl = base + tm3::RAW0 + static_cast<uint32_t>(slot * tm3::SLOT);
                     mbar_arrive_expect_tx(bar(slot), tm3::SLOT);
-                    tma_load_2d(sl, &tmA, kblk * BK, m0, bar(slot));
-                    tma_load_2d(sl + A_TILE, &tmB, n0, kblk * BK, bar(slot));
+                    if (TA) {  // A stored K x M: four boxes of 32 m x 32 k
+#pragma unroll
+                        for (int b = 0; b < BM / 32; ++b)
+                            tma_load_2d(sl + b * 4096, &tmA, m0 + 32 * b, kblk * BK, bar(slot));
+                    } else {
+                        tma_load_2d(sl, &tmA, kblk * BK, m0, bar(slot));
+                    }
+                    if (TB)  // B stored N x K: already K-major, 256 rows of 32 k
+                        tma_load_2d(sl + A_TILE, &tmB, kblk * BK, n0, bar(slot));
+                    else
+                        tma_load_2d(sl + A_TILE, &tmB, n0, kblk * BK, bar(slot));
                 }
             });
         }
@@ -1028,14 +1050,36 @@ __global__ void __launch_bounds__(tm3::THREADS, 1)
                     return;
                 }
                 const uint32_t sl = base + tm3::RAW0 + static_cast<uint32_t>(s * tm3::SLOT);
-                // A: 8 k-values of row arow (128-byte swizzled rows).
-                const float4 a0 = ld_shared_v4(sl + sw128_offset(arow, 2 * part));
-                const float4 a1 = ld_shared_v4(sl + sw128_offset(arow, 2 * part + 1));
-                // B: rows 4c..4c+3, columns 4g..4g+3 of the unswizzled staging tile.
+                // A: 8 k-values of row arow.
+                float av[8];
+                if (TA) {
+                    // Box q holds rows k = 0..31 of columns m = 32q..32q+31 (128-byte
+                    // swizzled): column arow is lane `lane` of each row.
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const int k = 8 * part + j;
+                        av[j] = ld_shared_f32(sl + static_cast<uint32_t>(q * 4096) + sw128_offset(k, lane >> 2) +
+                                              static_cast<uint32_t>((lane & 3) * 4));
+                    }
+                } else {
+                    const float4 a0 = ld_shared_v4(sl + sw128_offset(arow, 2 * part));
+                    const float4 a1 = ld_shared_v4(sl + sw128_offset(arow, 2 * part + 1));
+                    av[0] = a0.x;
+                    av[1] = a0.y;
+                    av[2] = a0.z;
+                    av[3] = a0.w;
+                    av[4] = a1.x;
+                    av[5] = a1.y;
+                    av[6] = a1.z;
+                    av[7] = a1.w;
+                }
+                // B: rows 4c..4c+3, columns 4g..4g+3 of the unswizzled staging tile
+                // (op(B) = B), or four 16-byte chunks of the K-major tile (B^T).
                 float4 bq[4];
 #pragma unroll
                 for (int qq = 0; qq < 4; ++qq)
-                    bq[qq] = ld_shared_v4(sl + A_TILE + static_cast<uint32_t>((4 * c + qq) * BN * 4 + g * 16));
+                    bq[qq] = TB ? ld_shared_v4(sl + A_TILE + static_cast<uint32_t>((qq * tm3::CONV_THREADS + ct) * 16))
+                                : ld_shared_v4(sl + A_TILE + static_cast<uint32_t>((4 * c + qq) * BN * 4 + g * 16));
                 fence_proxy_async_smem();  // order these loads before the next TMA into the slot
                 mbar_arrive(bar(2 + s));
                 // The stage (B in shared memory, A in TMEM) is free once the MMA
@@ -1046,24 +1090,27 @@ __global__ void __launch_bounds__(tm3::THREADS, 1)
                 }
                 tc_fence_after();
                 const uint32_t st = base + static_cast<uint32_t>(s * tm3::B_STAGE);
-                // Column j of the 4 x 4 block is chunk c of operand row 4g + j.
-                uint32_t off = sw128_offset(4 * g + 0, c);
-                split_store(st + off, st + B_TILE + off, bq[0].x, bq[1].x, bq[2].x, bq[3].x);
-                off = sw128_offset(4 * g + 1, c);
-                split_store(st + off, st + B_TILE + off, bq[0].y, bq[1].y, bq[2].y, bq[3].y);
-                off = sw128_offset(4 * g + 2, c);
-                split_store(st + off, st + B_TILE + off, bq[0].z, bq[1].z, bq[2].z, bq[3].z);
-                off = sw128_offset(4 * g + 3, c);
-                split_store(st + off, st + B_TILE + off, bq[0].w, bq[1].w, bq[2].w, bq[3].w);
+                if (TB) {
+                    // Same swizzled K-major layout: chunk for chunk.
+#pragma unroll
+                    for (int qq = 0; qq < 4; ++qq) {
+                        const uint32_t off = static_cast<uint32_t>((qq * tm3::CONV_THREADS + ct) * 16);
+                        split_store(st + off, st + B_TILE + off, bq[qq].x, bq[qq].y, bq[qq].z, bq[qq].w);
+                    }
+                } else {
+                    // Column j of the 4 x 4 block is chunk c of operand row 4g + j.
+                    uint32_t off = sw128_offset(4 * g + 0, c);
+                    split_store(st + off, st + B_TILE + off, bq[0].x, bq[1].x, bq[2].x, bq[3].x);
+                    off = sw128_offset(4 * g + 1, c);
+                    split_store(st + off, st + B_TILE + off, bq[0].y, bq[1].y, bq[2].y, bq[3].y);
+                    off = sw128_offset(4 * g + 2, c);
+                    split_store(st + off, st + B_TILE + off, bq[0].z, bq[1].z, bq[2].z, bq[3].z);
+                    off = sw128_offset(4 * g + 3, c);
+                    split_store(st + off, st + B_TILE + off, bq[0].w, bq[1].w, bq[2].w, bq[3].w);
+                }
                 float hi[8], lo[8];
-                split_tf32(a0.x, hi[0], lo[0]);
-                split_tf32(a0.y, hi[1], lo[1]);
-                split_tf32(a0.z, hi[2], lo[2]);
-                split_tf32(a0.w, hi[3], lo[3]);
-                split_tf32(a1.x, hi[4], lo[4]);
-                split_tf32(a1.y, hi[5], lo[5]);
-                split_tf32(a1.z, hi[6], lo[6]);
-                split_tf32(a1.w, hi[7], lo[7]);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) split_tf32(av[j], hi[j], lo[j]);
                 const uint32_t ta = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + tm3::TMEM_A +
                                     static_cast<uint32_t>(64 * s + 8 * part);
                 tmem_store8(ta, hi);
@@ -1084,7 +1131,8 @@ __global__ void __launch_bounds__(tm3::THREADS, 1)
             const int64_t m0 = static_cast<int64_t>(tile / a.tiles_n) * BM;
             const int64_t n0 = static_cast<int64_t>(tile % a.tiles_n) * BN;
             const int64_t row = m0 + q * 32 + lane;
-            const bool atomic = !(kb == 0 && ke == a.k_blocks);
+            // Stream-K tiles were scaled by beta beforehand: every unit adds.
+            const bool atomic = tile >= a.dp_tiles;
             float *crow = a.C + row * a.ldc;
 #pragma unroll 1
             for (int ch = 0; ch < BN / 32; ++ch) {
@@ -1094,22 +1142,7 @@ __global__ void __launch_bounds__(tm3::THREADS, 1)
                     tc_fence_before();
                     mbar_arrive(bar(9));  // accumulator read out: the next unit may start
                 }
-                const int64_t col0 = n0 + ch * 32;
-                if (row < a.M && col0 < a.N) {
-                    if (atomic) {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            if (col0 + j < a.N) atomicAdd(crow + col0 + j, v[j]);
-                    } else if (VEC_C && col0 + 31 < a.N) {
-#pragma unroll
-                        for (int j = 0; j < 32; j += 4)
-                            *reinterpret_cast<float4 *>(crow + col0 + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            if (col0 + j < a.N) crow[col0 + j] = v[j];
-                    }
-                }
+                store_chunk<VEC_C>(a, crow, row, n0 + ch * 32, v, atomic);
             }
             ++unit;
         });
@@ -1171,8 +1204,8 @@ int launch(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStream_t st
     // share below 4 k-blocks costs more in fix-up than it saves.
     const Schedule sch = make_schedule(tiles, k_blocks, dev.sm_count, sk_mode, 4);
     if (tiles > sch.dp_tiles) {
-        int rc = zero_tiles_launch(p.C, p.M, p.N, p.ldc, BM, BN, static_cast<int>(tiles_n), sch.dp_tiles,
-                                   tiles - sch.dp_tiles, stream, launches);
+        int rc = scale_tiles_launch(p.C, p.M, p.N, p.ldc, p.beta, BM, BN, static_cast<int>(tiles_n),
+                                    sch.dp_tiles, tiles - sch.dp_tiles, stream, launches);
         if (rc != SGEMM_OK) return rc;
     }
     Args a;
@@ -1192,6 +1225,8 @@ int launch(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStream_t st
     a.sk_iters = sch.sk_iters;
     a.timeout_ns = static_cast<uint64_t>(g_watchdog_ms.load()) * 1000000ull;
     a.watchdog = flag;
+    a.alpha = p.alpha;
+    a.beta = p.beta;
     kernel<<<sch.grid, THREADS, SMEM_BYTES, stream>>>(a);
     ++*launches;
     return cudaGetLastError() == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
@@ -1237,16 +1272,18 @@ bool tma_ok(const Problem &p) {
            p.K < INT32_MAX / 2 && tensor_map_encoder() != nullptr;
 }
 
-std::once_flag g_tma_attr_once[kMaxDevices][4];
-cudaError_t g_tma_attr_err[kMaxDevices][4];
+std::once_flag g_tma_attr_once[kMaxDevices][16];
+cudaError_t g_tma_attr_err[kMaxDevices][16];
 
-// V3 = A in TMEM (tf32x3_tmem_kernel), else the TMA variant (tf32x3_tma_kernel).
-template <bool V3, bool VEC_C>
+// V3 = A in TMEM (tf32x3_tmem_kernel, every operand form), else the TMA
+// variant (tf32x3_tma_kernel, op(A) = A and op(B) = B only).
+template <bool V3, bool VEC_C, bool TA = false, bool TB = false>
 int launch_tma(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStream_t stream, int *launches) {
-    auto kernel = V3 ? tf32x3_tmem_kernel<VEC_C> : tf32x3_tma_kernel<VEC_C>;
+    static_assert(V3 || (!TA && !TB), "the TMA variant serves op(A) = A, op(B) = B only");
+    auto kernel = V3 ? tf32x3_tmem_kernel<VEC_C, TA, TB> : tf32x3_tma_kernel<VEC_C>;
     constexpr int smem = V3 ? tm3::SMEM_BYTES : tma::SMEM_BYTES;
     constexpr int threads = V3 ? tm3::THREADS : tma::THREADS;
-    constexpr int idx = (V3 ? 2 : 0) + (VEC_C ? 1 : 0);
+    constexpr int idx = (V3 ? 2 : 0) + (VEC_C ? 1 : 0) + (TA ? 4 : 0) + (TB ? 8 : 0);
     std::call_once(g_tma_attr_once[dev.device][idx], [&] {
         g_tma_attr_err[dev.device][idx] = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     });
@@ -1257,8 +1294,11 @@ int launch_tma(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStream_
     int *flag = watchdog_flag_device_ptr();
     if (!flag) return SGEMM_ERR_LAUNCH;
     alignas(64) CUtensorMap mapA, mapB;
-    if (!encode_map(&mapA, p.A, p.M, p.K, p.lda, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B)) return SGEMM_ERR_LAUNCH;
-    if (!encode_map(&mapB, p.B, p.K, p.N, p.ldb, BN, BK, CU_TENSOR_MAP_SWIZZLE_NONE)) return SGEMM_ERR_LAUNCH;
+    const bool ok_a = TA ? encode_map(&mapA, p.A, p.K, p.M, p.lda, 32, 32, CU_TENSOR_MAP_SWIZZLE_128B)
+                         : encode_map(&mapA, p.A, p.M, p.K, p.lda, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B);
+    const bool ok_b = TB ? encode_map(&mapB, p.B, p.N, p.K, p.ldb, BK, BN, CU_TENSOR_MAP_SWIZZLE_128B)
+                         : encode_map(&mapB, p.B, p.K, p.N, p.ldb, BN, BK, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (!ok_a || !ok_b) return SGEMM_ERR_LAUNCH;
 
     const int64_t tiles_m = (p.M + BM - 1) / BM, tiles_n = (p.N + BN - 1) / BN;
     const int64_t k_blocks = (p.K + BK - 1) / BK;
@@ -1266,8 +1306,8 @@ int launch_tma(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStream_
     const int tiles = static_cast<int>(tiles_m * tiles_n);
     const Schedule sch = make_schedule(tiles, k_blocks, dev.sm_count, sk_mode, 4);
     if (tiles > sch.dp_tiles) {
-        int rc = zero_tiles_launch(p.C, p.M, p.N, p.ldc, BM, BN, static_cast<int>(tiles_n), sch.dp_tiles,
-                                   tiles - sch.dp_tiles, stream, launches);
+        int rc = scale_tiles_launch(p.C, p.M, p.N, p.ldc, p.beta, BM, BN, static_cast<int>(tiles_n),
+                                    sch.dp_tiles, tiles - sch.dp_tiles, stream, launches);
         if (rc != SGEMM_OK) return rc;
     }
     Args a{};
@@ -1283,6 +1323,8 @@ int launch_tma(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStream_
     a.sk_iters = sch.sk_iters;
     a.timeout_ns = static_cast<uint64_t>(g_watchdog_ms.load()) * 1000000ull;
     a.watchdog = flag;
+    a.alpha = p.alpha;
+    a.beta = p.beta;
     kernel<<<sch.grid, threads, smem, stream>>>(mapA, mapB, a);
     ++*launches;
     return cudaGetLastError() == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
@@ -1353,6 +1395,8 @@ int watchdog_set_ms(int64_t ms) {
 }
 
 bool tf32x3_supports(const Problem &p, const DeviceInfo &dev) {
+    // Transposed forms need the TMA path (16-byte aligned bases and strides).
+    if ((p.transA || p.transB) && !tma_ok(p)) return false;
     return p.M > 0 && p.N > 0 && p.K > 0 && dev.cc_major == 10 && dev.cc_minor == 3 &&
            dev.smem_optin >= static_cast<size_t>(tma::SMEM_BYTES);
 }
@@ -1361,6 +1405,18 @@ int tf32x3_launch(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStre
     if (!tf32x3_supports(p, dev) || dev.device < 0 || dev.device >= kMaxDevices) return SGEMM_ERR_UNSUPPORTED;
     const bool vc = (p.ldc % 4 == 0) && (reinterpret_cast<uintptr_t>(p.C) % 16 == 0);
     const int mode = g_use_tma.load();
+    if (p.transA || p.transB) {
+        // Transposed forms: the tensor-memory kernel (TMA loads needed).
+        if (!tma_ok(p)) return SGEMM_ERR_UNSUPPORTED;
+        if (p.transA && p.transB)
+            return vc ? launch_tma<true, true, true, true>(p, dev, sk_mode, stream, launches)
+                      : launch_tma<true, false, true, true>(p, dev, sk_mode, stream, launches);
+        if (p.transA)
+            return vc ? launch_tma<true, true, true, false>(p, dev, sk_mode, stream, launches)
+                      : launch_tma<true, false, true, false>(p, dev, sk_mode, stream, launches);
+        return vc ? launch_tma<true, true, false, true>(p, dev, sk_mode, stream, launches)
+                  : launch_tma<true, false, false, true>(p, dev, sk_mode, stream, launches);
+    }
     if (mode == 2 && tma_ok(p))
         return vc ? launch_tma<true, true>(p, dev, sk_mode, stream, launches)
                   : launch_tma<true, false>(p, dev, sk_mode, stream, launches);

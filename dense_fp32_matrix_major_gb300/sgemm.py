@@ -21,6 +21,9 @@ SGEMM_ERR_LAUNCH = 3
 SGEMM_ERR_DEVICE = 4
 SGEMM_ERR_TIMEOUT = 5
 
+SGEMM_OP_N = 0
+SGEMM_OP_T = 1
+
 SGEMM_AUTO = 0
 SGEMM_FFMA = 1
 SGEMM_TF32X3 = 2
@@ -34,6 +37,8 @@ SGEMM_TUNE_TF32X3_KERNEL = 4
 _i64, _int, _vp, _cp = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_char_p
 SIGNATURES = {
     "sgemm_f32": (_int, [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _vp]),
+    "sgemm_f32_ex": (_int, [_int, _int, _i64, _i64, _i64, ctypes.c_float, _vp, _i64, _vp, _i64,
+                            ctypes.c_float, _vp, _i64, _vp]),
     "sgemm_f32_from_host": (_int, [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _vp, _vp, _vp, _vp]),
     "sgemm_set_variant": (_int, [_int]),
     "sgemm_get_variant": (_int, []),
@@ -175,6 +180,35 @@ def sgemm_f32(A, B, C=None, stream=None):
                        _stream_handle(stream))
     if rc:
         raise SgemmError(rc, "sgemm_f32")
+    return C
+
+
+def gemm(A, B, C=None, *, transA=False, transB=False, alpha=1.0, beta=0.0, stream=None):
+    """C = alpha * op(A) @ op(B) + beta * C for row-major float32 CUDA tensors.
+
+    A is given as stored: M x K, or K x M when transA (op(A) = A^T); B is
+    K x N, or N x K when transB. C (M x N) is read only when beta != 0; if
+    C is None a new tensor is allocated by PyTorch (then beta must be 0).
+    """
+    import torch
+
+    lda = _rowmajor_2d(A, "A")
+    ldb = _rowmajor_2d(B, "B")
+    M, K = (A.shape[1], A.shape[0]) if transA else tuple(A.shape)
+    K2, N = (B.shape[1], B.shape[0]) if transB else tuple(B.shape)
+    if K != K2:
+        raise ValueError(f"inner dimensions differ: {K} vs {K2}")
+    if C is None:
+        if beta != 0.0:
+            raise ValueError("beta != 0 needs C")
+        C = torch.empty((M, N), dtype=torch.float32, device=A.device)
+    ldc = _rowmajor_2d(C, "C")
+    if tuple(C.shape) != (M, N):
+        raise ValueError("C has the wrong shape")
+    rc = lib.sgemm_f32_ex(int(transA), int(transB), M, N, K, float(alpha), A.data_ptr(), lda,
+                          B.data_ptr(), ldb, float(beta), C.data_ptr(), ldc, _stream_handle(stream))
+    if rc:
+        raise SgemmError(rc, "sgemm_f32_ex")
     return C
 
 

@@ -83,6 +83,34 @@ enum sgemm_variant {
 int sgemm_f32(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, const float *B,
               int64_t ldb, float *C, int64_t ldc, sgemm_stream_t stream);
 
+/* Operand forms for sgemm_f32_ex. */
+enum sgemm_op {
+    SGEMM_OP_N = 0, /* op(X) = X */
+    SGEMM_OP_T = 1  /* op(X) = X^T */
+};
+
+/*
+ * C = alpha * op(A) * op(B) + beta * C, the general (BLAS GEMM) form; the
+ * source pages define only C = A * B, which is sgemm_f32 (alpha = 1,
+ * beta = 0, no transposes).
+ *   transA    SGEMM_OP_N: A is stored M x K, row stride lda >= K.
+ *             SGEMM_OP_T: A is stored K x M, row stride lda >= M (op(A) = A^T).
+ *   transB    SGEMM_OP_N: B is stored K x N, row stride ldb >= N.
+ *             SGEMM_OP_T: B is stored N x K, row stride ldb >= K.
+ *   C, ldc    M x N, row stride ldc >= N. beta == 0: C is only written (it may
+ *             hold NaN); otherwise C is read and updated in place.
+ *   alpha     alpha == 0 or K == 0: C = beta * C (C = 0 when beta == 0) and A,
+ *             B are not read.
+ * Same conventions, errors and accuracy bound as sgemm_f32, with the error
+ * scale |alpha| sum_k |op(A)[i][k]| |op(B)[k][j]| + |beta| |C[i][j]|.
+ * SGEMM_TF32X3 serves op(A) = A, op(B) = B at any alignment and the
+ * transposed forms when A and B have 16-byte aligned bases and row strides;
+ * SGEMM_AUTO picks a variant that serves the request.
+ */
+int sgemm_f32_ex(int transA, int transB, int64_t M, int64_t N, int64_t K, float alpha, const float *A,
+                 int64_t lda, const float *B, int64_t ldb, float beta, float *C, int64_t ldc,
+                 sgemm_stream_t stream);
+
 /*
  * C = A * B for matrices that live in HOST memory, through caller-owned
  * device buffers. Enqueues, on `stream`: the copy of A_host into dA and of

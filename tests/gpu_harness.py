@@ -78,3 +78,29 @@ def oracle_error(C: np.ndarray, A: np.ndarray, B: np.ndarray, nthreads=None) -> 
 def sampled_error(C: np.ndarray, A: np.ndarray, B: np.ndarray, rows, cols) -> float:
     c64, s = oracle.sgemm_f64_at(A, B, rows, cols)
     return oracle.normalized_error(C[rows, cols], c64, s)
+
+
+def run_gemm_ex(A: np.ndarray, B: np.ndarray, *, transA=False, transB=False, alpha=1.0, beta=0.0,
+                C_init=None, lda=None, ldb=None, ldc=None, offsets=(0, 0, 0)):
+    """sgemm_f32_ex on numpy inputs given in STORED form (A is K x M when
+    transA, B is N x K when transB); returns (C, flat C buffer, status)."""
+    import torch
+    from dense_fp32_matrix_major_gb300 import sgemm
+
+    M = A.shape[1] if transA else A.shape[0]
+    K = A.shape[0] if transA else A.shape[1]
+    N = B.shape[0] if transB else B.shape[1]
+    lda = max(A.shape[1], 1) if lda is None else lda
+    ldb = max(B.shape[1], 1) if ldb is None else ldb
+    ldc = max(N, 1) if ldc is None else ldc
+    fa, vA = device_matrix(A, lda, offsets[0])
+    fb, vB = device_matrix(B, ldb, offsets[1])
+    cvals = np.full((M, N), np.nan, dtype=np.float32) if C_init is None else C_init
+    fc, vC = device_matrix(cvals, ldc, offsets[2])
+    stream = torch.cuda.current_stream()
+    rc = sgemm.lib.sgemm_f32_ex(int(transA), int(transB), M, N, K, float(alpha), vA.data_ptr(), lda,
+                                vB.data_ptr(), ldb, float(beta), vC.data_ptr(), ldc, stream.cuda_stream)
+    torch.cuda.synchronize()
+    flat = fc.cpu().numpy()
+    box = vC.cpu().numpy() if M and N else np.zeros((M, N), np.float32)
+    return box, flat, rc

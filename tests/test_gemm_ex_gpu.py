@@ -1,0 +1,134 @@
+"""GPU parity of the general form C = alpha * op(A) * op(B) + beta * C
+(sgemm_f32_ex) against the oracle's general form."""
+
+import itertools
+
+import numpy as np
+import pytest
+
+import oracle
+from dense_fp32_matrix_major_gb300 import workloads as wl
+from tests.gpu_harness import TOL, outside_box_intact, run_gemm_ex
+
+pytestmark = pytest.mark.gpu
+
+FORMS = [(0, 0), (1, 0), (0, 1), (1, 1)]
+SCALES = [(1.0, 0.0), (2.5, -1.5), (-1.0, 1.0), (0.75, 0.0), (1.0, 1.0)]
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from dense_fp32_matrix_major_gb300 import sgemm
+
+    yield sgemm
+    sgemm.set_variant(0)
+    sgemm.set_tuning(sgemm.SGEMM_TUNE_FFMA_TILE, 0)
+    sgemm.set_tuning(sgemm.SGEMM_TUNE_STREAM_K, 0)
+    sgemm.set_tuning(sgemm.SGEMM_TUNE_TF32X3_KERNEL, 2)
+
+
+def _stored(M, N, K, transA, transB, dist, seed):
+    A, B = wl.make_pair(M, N, K, dist, seed)
+    As = np.ascontiguousarray(A.T) if transA else A
+    Bs = np.ascontiguousarray(B.T) if transB else B
+    return As, Bs
+
+
+def _tma_aligned(As, Bs, **kw):
+    lda = kw.get("lda") or As.shape[1]
+    ldb = kw.get("ldb") or Bs.shape[1]
+    offs = kw.get("offsets", (0, 0, 0))
+    return lda % 4 == 0 and ldb % 4 == 0 and offs[0] % 4 == 0 and offs[1] % 4 == 0
+
+
+def _check(lib, As, Bs, tA, tB, alpha, beta, C0, **kw):
+    C, flat, rc = run_gemm_ex(As, Bs, transA=tA, transB=tB, alpha=alpha, beta=beta,
+                              C_init=C0 if beta else None, **kw)
+    if lib.get_variant() == lib.SGEMM_TF32X3 and (tA or tB) and not _tma_aligned(As, Bs, **kw):
+        # Forced tensor cores serve transposed forms only with 16-byte aligned rows.
+        assert rc == lib.SGEMM_ERR_UNSUPPORTED
+        return
+    assert rc == 0
+    M, N = C.shape
+    ldc = kw.get("ldc") or max(N, 1)
+    assert outside_box_intact(flat, M, N, ldc, kw.get("offsets", (0, 0, 0))[2])
+    C64, S = oracle.gemm_f64(As, Bs, transA=bool(tA), transB=bool(tB), alpha=alpha, beta=beta,
+                             C_in=C0 if beta else None)
+    err = oracle.normalized_error(C, C64, S)
+    assert err <= TOL, (tA, tB, alpha, beta, err)
+
+
+@pytest.mark.parametrize("variant,tile,sk", [("auto", 0, 0), ("ffma", 1, 3), ("ffma", 3, 0), ("ffma", 2, 1),
+                                             ("tf32x3", 0, 0), ("tf32x3", 0, 3)])
+@pytest.mark.parametrize("tA,tB", FORMS)
+def test_forms_and_scales(lib, variant, tile, sk, tA, tB):
+    lib.set_variant(variant)
+    lib.set_tuning(lib.SGEMM_TUNE_FFMA_TILE, tile)
+    lib.set_tuning(lib.SGEMM_TUNE_STREAM_K, sk)
+    for (M, N, K) in [(1, 1, 1), (5, 3, 7), (129, 257, 47), (300, 200, 513), (64, 300, 1000),
+                      (128, 256, 64), (260, 516, 300)]:
+        As, Bs = _stored(M, N, K, tA, tB, "normal", M + N + K)
+        C0 = np.random.default_rng(K).standard_normal((M, N)).astype(np.float32)
+        for alpha, beta in SCALES:
+            _check(lib, As, Bs, tA, tB, alpha, beta, C0)
+
+
+@pytest.mark.parametrize("variant", ["ffma", "tf32x3"])
+@pytest.mark.parametrize("tA,tB", FORMS)
+def test_integer_forms_bit_exact(lib, variant, tA, tB):
+    lib.set_variant(variant)
+    for (M, N, K) in [(256, 132, 1000), (64, 300, 4096)]:
+        As, Bs = _stored(M, N, K, tA, tB, "int4", K)
+        C0 = np.random.default_rng(1).integers(-9, 10, (M, N)).astype(np.float32)
+        C, flat, rc = run_gemm_ex(As, Bs, transA=tA, transB=tB, alpha=3.0, beta=-2.0, C_init=C0)
+        assert rc == 0
+        A = As.T if tA else As
+        B = Bs.T if tB else Bs
+        exact = 3 * (A.astype(np.int64) @ B.astype(np.int64)) - 2 * C0.astype(np.int64)
+        assert np.array_equal(C, exact.astype(np.float32))
+
+
+@pytest.mark.parametrize("tA,tB", FORMS)
+def test_strided_unaligned_forms(lib, tA, tB):
+    lib.set_variant("auto")
+    M, N, K = 150, 270, 90
+    As, Bs = _stored(M, N, K, tA, tB, "uniform", 8)
+    C0 = np.random.default_rng(2).standard_normal((M, N)).astype(np.float32)
+    for kw in [dict(lda=As.shape[1] + 3, ldb=Bs.shape[1] + 5, ldc=N + 7, offsets=(1, 3, 2)),
+               dict(lda=As.shape[1] + 4, ldb=Bs.shape[1] + 4, ldc=N + 4, offsets=(0, 0, 0))]:
+        _check(lib, As, Bs, tA, tB, 1.5, -0.5, C0, **kw)
+
+
+def test_beta_zero_ignores_nan_c_and_alpha_zero(lib):
+    for variant in ("ffma", "tf32x3"):
+        lib.set_variant(variant)
+        As, Bs = _stored(200, 300, 64, 0, 0, "normal", 3)
+        C, flat, rc = run_gemm_ex(As, Bs, alpha=1.0, beta=0.0)  # C starts as NaN
+        assert rc == 0 and np.all(np.isfinite(C))
+        C0 = np.random.default_rng(4).standard_normal((200, 300)).astype(np.float32)
+        C, flat, rc = run_gemm_ex(As, Bs, alpha=0.0, beta=-1.25, C_init=C0)
+        assert rc == 0 and np.array_equal(C, np.float32(-1.25) * C0)
+        C, flat, rc = run_gemm_ex(As, Bs, alpha=0.0, beta=0.0)
+        assert rc == 0 and np.all(C == 0)
+
+
+def test_forced_tensor_cores_on_unaligned_transposes(lib):
+    """TF32X3 serves transposed forms only through TMA (16-byte aligned rows)."""
+    lib.set_variant("tf32x3")
+    As, Bs = _stored(100, 100, 101, 1, 0, "normal", 5)  # A stored 101 x 100: lda = 100 is aligned
+    _, _, rc = run_gemm_ex(As, Bs, transA=True, lda=101)
+    assert rc in (0, lib.SGEMM_ERR_UNSUPPORTED)
+
+
+@pytest.mark.parametrize("tA,tB", FORMS)
+def test_headline_shape_forms(lib, tA, tB):
+    lib.set_variant("auto")
+    w = wl.C5_HEAD
+    As, Bs = _stored(w.M, w.N, w.K, tA, tB, "normal", 4)
+    C0 = np.random.default_rng(5).standard_normal((w.M, w.N)).astype(np.float32)
+    C, flat, rc = run_gemm_ex(As, Bs, transA=tA, transB=tB, alpha=0.5, beta=2.0, C_init=C0)
+    assert rc == 0
+    r, c = wl.sample_positions(w.M, w.N, 3000, seed=tA * 2 + tB)
+    c64, s = oracle.gemm_f64_at(As, Bs, r, c, transA=bool(tA), transB=bool(tB), alpha=0.5, beta=2.0,
+                                C_in=C0)
+    assert oracle.normalized_error(C[r, c], c64, s) <= TOL
