@@ -272,6 +272,45 @@ def run_ours(args, w, torch, dist):
     }
 
 
+def run_batched_bench(args, bw, torch):
+    """GFLOP/s of one strided-batched call over packed items (inputs resident,
+    L2 flushed between steps), with a sampled parity check of a few items."""
+    from dense_fp32_matrix_major_gb300 import sgemm
+    import oracle  # test infrastructure: spot check only
+
+    _, _, local = _dist_env()
+    device = torch.device("cuda", local)
+    sgemm.set_variant(args.variant)
+    A, B = wl.make_batched(bw)
+    dA = torch.from_numpy(A).to(device)
+    dB = torch.from_numpy(B).to(device)
+    dC = torch.empty((bw.batch, bw.M, bw.N), dtype=torch.float32, device=device)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        flush.zero_()
+        sgemm.gemm_batched(dA, dB, dC)
+    torch.cuda.synchronize()
+    steps = max(3, min(args.steps, 500))
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for e0, e1 in ev:
+        flush.zero_()
+        e0.record(stream)
+        sgemm.gemm_batched(dA, dB, dC)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    ms = sum(e0.elapsed_time(e1) for e0, e1 in ev) / steps
+    C = dC.cpu().numpy()
+    err = 0.0
+    for b in (0, bw.batch // 2, bw.batch - 1):
+        r, c = wl.sample_positions(bw.M, bw.N, 32, seed=b)
+        c64, s = oracle.sgemm_f64_at(A[b], B[b], r, c)
+        err = max(err, oracle.normalized_error(C[b][r, c], c64, s))
+    return {"workload": bw.name, "batch": bw.batch, "value": round(bw.flops / (ms * 1e-3) / 1e9, 2),
+            "unit": UNIT, "ms_per_step": round(ms, 5), "variant": sgemm.variant_name(sgemm.last_variant_used()),
+            "launches_per_step": sgemm.last_launch_count(), "parity_sampled_err": err}
+
+
 def run_e2e(args, w, torch, sgemm, A, B, device, dist, ws):
     Ah = torch.from_numpy(np.ascontiguousarray(A)).pin_memory()
     Bh = torch.from_numpy(np.ascontiguousarray(B)).pin_memory()
@@ -389,6 +428,8 @@ def main():
     ap.add_argument("--ref-step-seconds", type=float, default=4.0)
     ap.add_argument("--all-configs", action="store_true",
                     help="also print one extra line per workload (not the headline line)")
+    ap.add_argument("--batched", action="store_true",
+                    help="also print one extra line per strided-batched workload")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -438,6 +479,9 @@ def main():
                                   "ms_per_step": round(r["ms_per_step"], 5), "variant": r["variant"],
                                   "roofline_frac": r["roofline"]["frac"],
                                   "parity_sampled_err": r["parity_sampled_err"]}), flush=True)
+        if args.batched:
+            for bw in wl.BATCHED:
+                print(json.dumps(run_batched_bench(args, bw, torch)), flush=True)
     if dist is not None:
         dist.barrier()
         dist.destroy_process_group()

@@ -25,6 +25,8 @@ struct FfmaArgs {
     float *C;
     int64_t ldc;
     float alpha, beta;  // C = alpha * op(A) op(B) + beta * C; beta == 0: C not read
+    int64_t strideA, strideB, strideC;  // elements between the items of a batch
+    int tiles_per_item;                 // tiles of one product (tiles run item-major)
     int vec_a;          // op(A) = A^T and its rows allow 16-byte copies
     int vec_c;          // C rows allow 16-byte stores (used when VEC_C is not set)
     int tiles_n;        // tiles along N (tiles are numbered row-major over the tile grid)
@@ -103,7 +105,8 @@ __device__ __forceinline__ int bs_index(int k, int n) {
 }
 
 template <class C, bool TA, bool TB, bool VEC_B>
-__device__ __forceinline__ void load_stage(const FfmaArgs &a, float *As, float *Bs, int64_t m0,
+__device__ __forceinline__ void load_stage(const FfmaArgs &a, const float *__restrict__ Ab,
+                                           const float *__restrict__ Bb, float *As, float *Bs, int64_t m0,
                                            int64_t n0, int64_t k0, int tid) {
     constexpr int BK = C::BK;
     if constexpr (!TA) {
@@ -114,7 +117,7 @@ __device__ __forceinline__ void load_stage(const FfmaArgs &a, float *As, float *
             const int m = e / BK, k = e % BK;
             const int64_t gm = m0 + m, gk = k0 + k;
             const bool ok = gm < a.M && gk < a.K;
-            const float *src = ok ? a.A + gm * a.lda + gk : a.A;
+            const float *src = ok ? Ab + gm * a.lda + gk : Ab;
             cp_async_4(smem_addr(As + as_index<C>(k, m)), src, ok ? 4 : 0);
         }
     } else if (a.vec_a) {
@@ -126,7 +129,7 @@ __device__ __forceinline__ void load_stage(const FfmaArgs &a, float *As, float *
             const int64_t gk = k0 + k, gm = m0 + m;
             int bytes = 0;
             if (gk < a.K && gm < a.M) bytes = static_cast<int>(min64(4, a.M - gm)) * 4;
-            const float *src = bytes ? a.A + gk * a.lda + gm : a.A;
+            const float *src = bytes ? Ab + gk * a.lda + gm : Ab;
             cp_async_16(smem_addr(As + as_index<C>(k, m)), src, bytes);
         }
     } else {
@@ -136,7 +139,7 @@ __device__ __forceinline__ void load_stage(const FfmaArgs &a, float *As, float *
             const int k = e / C::BM, m = e % C::BM;
             const int64_t gk = k0 + k, gm = m0 + m;
             const bool ok = gk < a.K && gm < a.M;
-            const float *src = ok ? a.A + gk * a.lda + gm : a.A;
+            const float *src = ok ? Ab + gk * a.lda + gm : Ab;
             cp_async_4(smem_addr(As + as_index<C>(k, m)), src, ok ? 4 : 0);
         }
     }
@@ -148,7 +151,7 @@ __device__ __forceinline__ void load_stage(const FfmaArgs &a, float *As, float *
             const int n = e / BK, k = e % BK;
             const int64_t gn = n0 + n, gk = k0 + k;
             const bool ok = gk < a.K && gn < a.N;
-            const float *src = ok ? a.B + gn * a.ldb + gk : a.B;
+            const float *src = ok ? Bb + gn * a.ldb + gk : Bb;
             cp_async_4(smem_addr(Bs + bs_index<C, TB>(k, n)), src, ok ? 4 : 0);
         }
     } else if constexpr (VEC_B) {
@@ -159,7 +162,7 @@ __device__ __forceinline__ void load_stage(const FfmaArgs &a, float *As, float *
             const int64_t gk = k0 + k, gn = n0 + n;
             int bytes = 0;
             if (gk < a.K && gn < a.N) bytes = static_cast<int>(min64(4, a.N - gn)) * 4;
-            const float *src = bytes ? a.B + gk * a.ldb + gn : a.B;
+            const float *src = bytes ? Bb + gk * a.ldb + gn : Bb;
             cp_async_16(smem_addr(Bs + bs_index<C, TB>(k, n)), src, bytes);
         }
     } else {
@@ -169,7 +172,7 @@ __device__ __forceinline__ void load_stage(const FfmaArgs &a, float *As, float *
             const int k = e / C::BN, n = e % C::BN;
             const int64_t gk = k0 + k, gn = n0 + n;
             const bool ok = gk < a.K && gn < a.N;
-            const float *src = ok ? a.B + gk * a.ldb + gn : a.B;
+            const float *src = ok ? Bb + gk * a.ldb + gn : Bb;
             cp_async_4(smem_addr(Bs + bs_index<C, TB>(k, n)), src, ok ? 4 : 0);
         }
     }
@@ -186,8 +189,12 @@ __device__ __forceinline__ void process_tile(const FfmaArgs &a, float *As, float
     const int wm0 = (warp / C::WARPS_N) * C::WM;
     const int wn0 = (warp % C::WARPS_N) * C::WN;
     const int tm = lane >> 2, tn = lane & 3;
-    const int64_t m0 = static_cast<int64_t>(tile / a.tiles_n) * C::BM;
-    const int64_t n0 = static_cast<int64_t>(tile % a.tiles_n) * C::BN;
+    const int item = tile / a.tiles_per_item, rest = tile % a.tiles_per_item;
+    const int64_t m0 = static_cast<int64_t>(rest / a.tiles_n) * C::BM;
+    const int64_t n0 = static_cast<int64_t>(rest % a.tiles_n) * C::BN;
+    const float *Ab = a.A + item * a.strideA;
+    const float *Bb = a.B + item * a.strideB;
+    float *Cb = a.C + item * a.strideC;
     const int nk = ke - kb;
 
     float acc[8][TN];
@@ -200,7 +207,7 @@ __device__ __forceinline__ void process_tile(const FfmaArgs &a, float *As, float
 #pragma unroll
     for (int s = 0; s < S - 1; ++s) {
         if (s < nk)
-            load_stage<C, TA, TB, VEC_B>(a, As + s * C::A_STAGE, Bs + s * C::B_STAGE, m0, n0,
+            load_stage<C, TA, TB, VEC_B>(a, Ab, Bb, As + s * C::A_STAGE, Bs + s * C::B_STAGE, m0, n0,
                                          static_cast<int64_t>(kb + s) * BK, tid);
         cp_async_commit();
     }
@@ -212,7 +219,7 @@ __device__ __forceinline__ void process_tile(const FfmaArgs &a, float *As, float
             const int tl = t + S - 1;
             if (tl < nk) {
                 const int sl = tl % S;
-                load_stage<C, TA, TB, VEC_B>(a, As + sl * C::A_STAGE, Bs + sl * C::B_STAGE, m0, n0,
+                load_stage<C, TA, TB, VEC_B>(a, Ab, Bb, As + sl * C::A_STAGE, Bs + sl * C::B_STAGE, m0, n0,
                                              static_cast<int64_t>(kb + tl) * BK, tid);
             }
             cp_async_commit();
@@ -262,7 +269,7 @@ __device__ __forceinline__ void process_tile(const FfmaArgs &a, float *As, float
     for (int i = 0; i < 8; ++i) {
         const int64_t row = m0 + wm0 + (i >> 2) * 32 + tm * 4 + (i & 3);
         if (row >= a.M) continue;
-        float *crow = a.C + row * a.ldc;
+        float *crow = Cb + row * a.ldc;
 #pragma unroll
         for (int c = 0; c < C::CN; ++c) {
             const int64_t col = n0 + wn0 + c * 16 + tn * 4;
@@ -362,7 +369,7 @@ int launch_cfg(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStream_
     if (rc != SGEMM_OK) return rc;
 
     const int64_t tiles_m = ceil_div(p.M, C::BM), tiles_n = ceil_div(p.N, C::BN);
-    const int64_t tiles64 = tiles_m * tiles_n;
+    const int64_t tiles64 = tiles_m * tiles_n * p.batch;
     const int64_t k_tiles = ceil_div(p.K, C::BK);
     if (tiles64 > INT32_MAX / 2 || k_tiles > INT32_MAX / 2) return SGEMM_ERR_UNSUPPORTED;
     const int tiles = static_cast<int>(tiles64);
@@ -382,8 +389,12 @@ int launch_cfg(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStream_
     a.ldc = p.ldc;
     a.alpha = p.alpha;
     a.beta = p.beta;
-    a.vec_a = (p.lda % 4 == 0) && (reinterpret_cast<uintptr_t>(p.A) % 16 == 0);
-    a.vec_c = (p.ldc % 4 == 0) && (reinterpret_cast<uintptr_t>(p.C) % 16 == 0);
+    a.strideA = p.strideA;
+    a.strideB = p.strideB;
+    a.strideC = p.strideC;
+    a.tiles_per_item = static_cast<int>(tiles_m * tiles_n);
+    a.vec_a = (p.lda % 4 == 0) && (p.strideA % 4 == 0) && (reinterpret_cast<uintptr_t>(p.A) % 16 == 0);
+    a.vec_c = (p.ldc % 4 == 0) && (p.strideC % 4 == 0) && (reinterpret_cast<uintptr_t>(p.C) % 16 == 0);
     a.tiles_n = static_cast<int>(tiles_n);
     a.k_tiles = static_cast<int>(k_tiles);
     a.total_tiles = tiles;
@@ -391,8 +402,8 @@ int launch_cfg(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStream_
     a.sk_iters = sch.sk_iters;
     a.sk_ctas = sch.sk_ctas;
     if (tiles > sch.dp_tiles) {
-        rc = scale_tiles_launch(p.C, p.M, p.N, p.ldc, p.beta, C::BM, C::BN, a.tiles_n, sch.dp_tiles,
-                                tiles - sch.dp_tiles, stream, launches);
+        rc = scale_tiles_launch(p.C, p.M, p.N, p.ldc, p.strideC, p.beta, C::BM, C::BN, a.tiles_n,
+                                a.tiles_per_item, sch.dp_tiles, tiles - sch.dp_tiles, stream, launches);
         if (rc != SGEMM_OK) return rc;
     }
     ffma_kernel<C, TA, TB, VEC_B, VEC_C><<<sch.grid, C::THREADS, C::SMEM_BYTES, stream>>>(a);
@@ -405,8 +416,8 @@ int launch_cfg(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStream_
 // covers the SMs.
 inline int pick_tile(const Problem &p, const DeviceInfo &dev, int tile) {
     if (tile != FFMA_TILE_AUTO) return tile;
-    const int64_t big_tiles = ceil_div(p.M, CfgBig::BM) * ceil_div(p.N, CfgBig::BN);
-    const int64_t mid_tiles = ceil_div(p.M, CfgMid::BM) * ceil_div(p.N, CfgMid::BN);
+    const int64_t big_tiles = ceil_div(p.M, CfgBig::BM) * ceil_div(p.N, CfgBig::BN) * p.batch;
+    const int64_t mid_tiles = ceil_div(p.M, CfgMid::BM) * ceil_div(p.N, CfgMid::BN) * p.batch;
     if (big_tiles >= dev.sm_count) return FFMA_TILE_128x256;
     if (mid_tiles >= dev.sm_count / 2) return FFMA_TILE_128x128;
     return FFMA_TILE_64x64;

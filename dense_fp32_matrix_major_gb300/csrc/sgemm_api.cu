@@ -84,15 +84,44 @@ int check_args(int transA, int transB, int64_t M, int64_t N, int64_t K, const fl
     return SGEMM_OK;
 }
 
-// AUTO: the tensor-core path from 2^29 multiply-adds up (measured on GB300:
-// FFMA is faster at 512^3, the tensor-core path from 1024^3 on), and only up
-// to K = 8192: its accumulation rounds toward zero, so its error grows with K
-// (2.9e-6 of the 1e-5 bound at K = 4096); beyond that the FFMA path keeps the
-// bound at any K.
+// AUTO: the tensor-core path from 2^29 useful multiply-adds up (measured on
+// GB300: FFMA is faster at 512^3, the tensor-core path from 1024^3 on), and
+// only up to K = 8192: its accumulation rounds toward zero, so its error
+// grows with K (2.9e-6 of the 1e-5 bound at K = 4096); beyond that the FFMA
+// path keeps the bound at any K. "Useful" discounts the padding of the
+// tensor-core path's 128 x 256 tiles, which matters for batches of small
+// products (the FFMA path has 64 x 64 tiles for those).
 int auto_variant(const Problem &p, const DeviceInfo &dev) {
-    const double work = static_cast<double>(p.M) * static_cast<double>(p.N) * static_cast<double>(p.K);
+    const double m_pad = static_cast<double>((p.M + 127) / 128 * 128);
+    const double n_pad = static_cast<double>((p.N + 255) / 256 * 256);
+    const double fill = static_cast<double>(p.M) * static_cast<double>(p.N) / (m_pad * n_pad);
+    const double work = static_cast<double>(p.M) * static_cast<double>(p.N) * static_cast<double>(p.K) *
+                        static_cast<double>(p.batch) * fill;
     if (work >= 536870912.0 && p.K <= 8192 && tf32x3_supports(p, dev)) return SGEMM_TF32X3;
     return SGEMM_FFMA;
+}
+
+// Extra checks for a strided batch: non-negative strides, C items that do
+// not overlap one another, and no C item overlapping any A or B item (checked
+// on the ranges the whole batch spans).
+int check_batch(const Problem &p) {
+    if (p.batch < 0 || p.strideA < 0 || p.strideB < 0 || p.strideC < 0) return SGEMM_ERR_INVALID_ARG;
+    if (p.batch <= 1 || p.M == 0 || p.N == 0) return SGEMM_OK;
+    const int64_t lim = INT64_C(1) << 60;
+    if (p.strideA > lim / p.batch || p.strideB > lim / p.batch || p.strideC > lim / p.batch)
+        return SGEMM_ERR_INVALID_ARG;
+    if (p.strideC < (p.M - 1) * p.ldc + p.N) return SGEMM_ERR_INVALID_ARG;  // C items would overlap
+    const int64_t a_rows = p.transA ? p.K : p.M, a_cols = p.transA ? p.M : p.K;
+    const int64_t b_rows = p.transB ? p.N : p.K, b_cols = p.transB ? p.K : p.N;
+    const int64_t c_span = (p.batch - 1) * p.strideC + (p.M - 1) * p.ldc + p.N;
+    if (p.K > 0) {
+        const int64_t a_span = (p.batch - 1) * p.strideA + (a_rows - 1) * p.lda + a_cols;
+        const int64_t b_span = (p.batch - 1) * p.strideB + (b_rows - 1) * p.ldb + b_cols;
+        if (overlaps(p.C, 1, c_span, c_span, p.A, 1, a_span, a_span) ||
+            overlaps(p.C, 1, c_span, c_span, p.B, 1, b_span, b_span))
+            return SGEMM_ERR_INVALID_ARG;
+    }
+    return SGEMM_OK;
 }
 
 int enqueue(const Problem &p, cudaStream_t stream) {
@@ -101,13 +130,13 @@ int enqueue(const Problem &p, cudaStream_t stream) {
     int rc = current_device(&dev);
     if (rc != SGEMM_OK) return rc;
     int launches = 0;
-    if (p.M == 0 || p.N == 0) {
+    if (p.M == 0 || p.N == 0 || p.batch == 0) {
         g_last_launches.store(0);
         return SGEMM_OK;
     }
     if (p.K == 0 || p.alpha == 0.0f) {
         // The empty sum (or alpha = 0): C = beta * C.
-        rc = scale_launch(p.C, p.M, p.N, p.ldc, p.beta, dev, stream, &launches);
+        rc = scale_launch(p.C, p.M, p.N, p.ldc, p.strideC, p.batch, p.beta, dev, stream, &launches);
         if (rc == SGEMM_OK) {
             g_last_variant.store(SGEMM_FFMA);
             g_last_launches.store(launches);
@@ -195,6 +224,25 @@ static cudaError_t copy_rows(float *dst, const float *src, int64_t rows, int64_t
     if (ld == cols || rows == 1)
         return cudaMemcpyAsync(dst, src, static_cast<size_t>(rows * cols) * f, kind, s);
     return cudaMemcpy2DAsync(dst, ld * f, src, ld * f, cols * f, rows, kind, s);
+}
+
+int sgemm_f32_batched(int transA, int transB, int64_t M, int64_t N, int64_t K, float alpha, const float *A,
+                      int64_t lda, int64_t strideA, const float *B, int64_t ldb, int64_t strideB, float beta,
+                      float *C, int64_t ldc, int64_t strideC, int64_t batch, sgemm_stream_t stream) {
+    int rc = sgemm::check_args(transA, transB, M, N, K, A, lda, B, ldb, C, ldc);
+    if (rc != SGEMM_OK) return rc;
+    Problem p{M, N, K, A, lda, B, ldb, C, ldc};
+    p.transA = transA;
+    p.transB = transB;
+    p.alpha = alpha;
+    p.beta = beta;
+    p.batch = batch;
+    p.strideA = strideA;
+    p.strideB = strideB;
+    p.strideC = strideC;
+    rc = sgemm::check_batch(p);
+    if (rc != SGEMM_OK) return rc;
+    return sgemm::enqueue(p, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int sgemm_f32_from_host(int64_t M, int64_t N, int64_t K, const float *A_host, int64_t lda,

@@ -50,13 +50,16 @@ namespace {
 using namespace ffma;
 
 // C = beta * C over `count` tiles starting at `first_tile` of a bm x bn tile
-// grid (C = 0 when beta = 0: C is not read). blockIdx.y picks the tile,
+// grid (C = 0 when beta = 0: C is not read); tiles run item-major over a
+// batch whose items are strideC elements apart. blockIdx.y picks the tile,
 // blockIdx.x a band of 8 rows; a warp handles one row (float4 when aligned).
-__global__ void scale_tiles_kernel(float *C, int64_t M, int64_t N, int64_t ldc, float beta, int bm, int bn,
-                                   int tiles_n, int first_tile) {
+__global__ void scale_tiles_kernel(float *C, int64_t M, int64_t N, int64_t ldc, int64_t strideC, float beta, int bm,
+                                   int bn, int tiles_n, int tiles_per_item, int first_tile) {
     const int tile = first_tile + blockIdx.y;
-    const int64_t m0 = static_cast<int64_t>(tile / tiles_n) * bm;
-    const int64_t n0 = static_cast<int64_t>(tile % tiles_n) * bn;
+    const int item = tile / tiles_per_item, rest = tile % tiles_per_item;
+    C += item * strideC;
+    const int64_t m0 = static_cast<int64_t>(rest / tiles_n) * bm;
+    const int64_t n0 = static_cast<int64_t>(rest % tiles_n) * bn;
     const int64_t row = m0 + blockIdx.x * 8 + (threadIdx.x >> 5);
     if (row >= M || row >= m0 + bm) return;
     const int cols = static_cast<int>(min64(bn, N - n0));
@@ -82,20 +85,23 @@ __global__ void scale_tiles_kernel(float *C, int64_t M, int64_t N, int64_t ldc, 
     }
 }
 
-// C[0:M, 0:N] = beta * C (0 when beta = 0) with a grid-stride loop.
-__global__ void scale_rect_kernel(float *C, int64_t M, int64_t N, int64_t ldc, float beta) {
-    const int64_t total = M * N;
+// C[0:M, 0:N] = beta * C (0 when beta = 0) for every item of a batch, with a
+// grid-stride loop.
+__global__ void scale_rect_kernel(float *C, int64_t M, int64_t N, int64_t ldc, int64_t strideC, int64_t batch,
+                                  float beta) {
+    const int64_t per_item = M * N, total = per_item * batch;
     for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < total;
          e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        float *p = C + (e / N) * ldc + e % N;
+        const int64_t item = e / per_item, r = e % per_item;
+        float *p = C + item * strideC + (r / N) * ldc + r % N;
         *p = beta != 0.0f ? beta * *p : 0.0f;
     }
 }
 
 template <class C>
 int launch_nn(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStream_t stream, int *launches) {
-    const bool vb = (p.ldb % 4 == 0) && (reinterpret_cast<uintptr_t>(p.B) % 16 == 0);
-    const bool vc = (p.ldc % 4 == 0) && (reinterpret_cast<uintptr_t>(p.C) % 16 == 0);
+    const bool vb = (p.ldb % 4 == 0) && (p.strideB % 4 == 0) && (reinterpret_cast<uintptr_t>(p.B) % 16 == 0);
+    const bool vc = (p.ldc % 4 == 0) && (p.strideC % 4 == 0) && (reinterpret_cast<uintptr_t>(p.C) % 16 == 0);
     if (vb && vc) return launch_cfg<C, false, false, true, true>(p, dev, sk_mode, stream, launches);
     if (vb) return launch_cfg<C, false, false, true, false>(p, dev, sk_mode, stream, launches);
     if (vc) return launch_cfg<C, false, false, false, true>(p, dev, sk_mode, stream, launches);
@@ -115,20 +121,23 @@ int ffma_launch(const Problem &p, const DeviceInfo &dev, int tile, int sk_mode, 
     }
 }
 
-int scale_tiles_launch(float *C, int64_t M, int64_t N, int64_t ldc, float beta, int bm, int bn, int tiles_n,
-                       int first_tile, int count, cudaStream_t stream, int *launches) {
+int scale_tiles_launch(float *C, int64_t M, int64_t N, int64_t ldc, int64_t strideC, float beta, int bm, int bn,
+                       int tiles_n, int tiles_per_item, int first_tile, int count, cudaStream_t stream,
+                       int *launches) {
     if (count <= 0) return SGEMM_OK;
     const dim3 grid(static_cast<unsigned>((bm + 7) / 8), static_cast<unsigned>(count));
-    scale_tiles_kernel<<<grid, 256, 0, stream>>>(C, M, N, ldc, beta, bm, bn, tiles_n, first_tile);
+    scale_tiles_kernel<<<grid, 256, 0, stream>>>(C, M, N, ldc, strideC, beta, bm, bn, tiles_n, tiles_per_item,
+                                                  first_tile);
     ++*launches;
     return cudaGetLastError() == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
 }
 
-int scale_launch(float *C, int64_t M, int64_t N, int64_t ldc, float beta, const DeviceInfo &dev,
-                 cudaStream_t stream, int *launches) {
-    const int64_t total = M * N;
+int scale_launch(float *C, int64_t M, int64_t N, int64_t ldc, int64_t strideC, int64_t batch, float beta,
+                 const DeviceInfo &dev, cudaStream_t stream, int *launches) {
+    const int64_t total = M * N * batch;
     const int64_t blocks = min64(ceil_div(total, 256), static_cast<int64_t>(dev.sm_count) * 8);
-    scale_rect_kernel<<<static_cast<int>(blocks > 1 ? blocks : 1), 256, 0, stream>>>(C, M, N, ldc, beta);
+    scale_rect_kernel<<<static_cast<int>(blocks > 1 ? blocks : 1), 256, 0, stream>>>(C, M, N, ldc, strideC, batch,
+                                                                                     beta);
     ++*launches;
     return cudaGetLastError() == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
 }

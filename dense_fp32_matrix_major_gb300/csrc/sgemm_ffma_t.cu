@@ -15,7 +15,7 @@ using namespace ffma;
 
 template <class C>
 int launch_t(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStream_t stream, int *launches) {
-    const bool vb = (p.ldb % 4 == 0) && (reinterpret_cast<uintptr_t>(p.B) % 16 == 0);
+    const bool vb = (p.ldb % 4 == 0) && (p.strideB % 4 == 0) && (reinterpret_cast<uintptr_t>(p.B) % 16 == 0);
     if (p.transA && p.transB) return launch_cfg<C, true, true, false, false>(p, dev, sk_mode, stream, launches);
     if (p.transB) return launch_cfg<C, false, true, false, false>(p, dev, sk_mode, stream, launches);
     if (vb) return launch_cfg<C, true, false, true, false>(p, dev, sk_mode, stream, launches);

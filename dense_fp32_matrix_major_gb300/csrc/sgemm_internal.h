@@ -21,6 +21,8 @@ struct Problem {
     int64_t ldc;
     int transA = 0, transB = 0;
     float alpha = 1.0f, beta = 0.0f;
+    // Strided batch: item b uses A + b*strideA, B + b*strideB, C + b*strideC.
+    int64_t batch = 1, strideA = 0, strideB = 0, strideC = 0;
 };
 
 // Properties of the current device that the launchers need.
@@ -82,9 +84,11 @@ inline Schedule make_schedule(int tiles, int64_t k_steps, int slots, int mode, i
 
 // Enqueue a kernel that sets C = beta * C (C = 0 when beta = 0, without
 // reading C) over `count` tiles starting at tile `first_tile` of a bm x bn
-// tile grid with tiles_n tiles per row.
-int scale_tiles_launch(float *C, int64_t M, int64_t N, int64_t ldc, float beta, int bm, int bn, int tiles_n,
-                       int first_tile, int count, cudaStream_t stream, int *launches);
+// tile grid with tiles_n tiles per row and tiles_per_item tiles per batch
+// item (items strideC elements apart).
+int scale_tiles_launch(float *C, int64_t M, int64_t N, int64_t ldc, int64_t strideC, float beta, int bm, int bn,
+                       int tiles_n, int tiles_per_item, int first_tile, int count, cudaStream_t stream,
+                       int *launches);
 
 // Enqueue the FFMA product. `launches` receives the number of kernels enqueued.
 int ffma_launch(const Problem &p, const DeviceInfo &dev, int tile, int sk_mode, cudaStream_t stream,
@@ -95,8 +99,8 @@ int ffma_launch_t(const Problem &p, const DeviceInfo &dev, int tile, int sk_mode
 
 // Enqueue C[0:M, 0:N] = beta * C (0 when beta = 0): the result when K = 0
 // (the empty sum) or alpha = 0.
-int scale_launch(float *C, int64_t M, int64_t N, int64_t ldc, float beta, const DeviceInfo &dev,
-                 cudaStream_t stream, int *launches);
+int scale_launch(float *C, int64_t M, int64_t N, int64_t ldc, int64_t strideC, int64_t batch, float beta,
+                 const DeviceInfo &dev, cudaStream_t stream, int *launches);
 
 // Tensor-core three-term TF32 variant. Returns SGEMM_ERR_UNSUPPORTED when it
 // cannot run the request.

@@ -97,7 +97,26 @@ struct Args {
     uint64_t timeout_ns;
     int *watchdog;
     float alpha = 1.0f, beta = 0.0f;  // C = alpha * op(A) op(B) + beta * C; beta == 0: C not read
+    // Strided batch: tiles run item-major, tiles_per_item per product; item b
+    // uses A + b*strideA, B + b*strideB, C + b*strideC. In the TMA kernels the
+    // item is the third tensor-map coordinate (0 for an operand shared by all
+    // items, stride 0).
+    int64_t strideA = 0, strideB = 0, strideC = 0;
+    int tiles_per_item = 1;
+    int a_shared = 0, b_shared = 0;
 };
+
+// Item and top-left corner of tile `tile` of the item-major tile order.
+struct TileAt {
+    int item;
+    int64_t m0, n0;
+};
+
+__device__ __forceinline__ TileAt tile_at(const Args &a, int tile) {
+    const int rest = tile % a.tiles_per_item;
+    return TileAt{tile / a.tiles_per_item, static_cast<int64_t>(rest / a.tiles_n) * BM,
+                  static_cast<int64_t>(rest % a.tiles_n) * BN};
+}
 
 // Instruction descriptor of tcgen05.mma kind::tf32: D fp32 (bits 4-5 = 1),
 // A and B tf32 (bits 7-9 and 10-12 = 2), both K-major (bits 15, 16 = 0),
@@ -227,13 +246,15 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
 
-// 2-D tiled TMA load of the box at (x, y) (x innermost, in elements) into
-// shared memory, completing `bytes` of transactions on the mbarrier.
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar) {
+// 3-D tiled TMA load of the box at (x, y, z) (x innermost, in elements; z is
+// the batch item) into shared memory, completing its bytes of transactions
+// on the mbarrier.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int x, int y, int z,
+                                            uint32_t bar) {
     asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
-            "r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+        "[%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
         : "memory");
 }
 
@@ -478,12 +499,14 @@ __global__ void __launch_bounds__(THREADS, 1) tf32x3_kernel(const Args a) {
         bool ok = true;
         for_each_unit(a, abort_flag, [&](int tile, int kb, int ke) {
             if (!ok) return;
-            const int64_t m0 = static_cast<int64_t>(tile / a.tiles_n) * BM;
-            const int64_t n0 = static_cast<int64_t>(tile % a.tiles_n) * BN;
+            const TileAt at = tile_at(a, tile);
+            const int64_t m0 = at.m0, n0 = at.n0;
+            const float *Ai = a.A + at.item * a.strideA;
+            const float *Bi = a.B + at.item * a.strideB;
             const bool full_mn = (m0 + BM <= a.M) && (n0 + BN <= a.N);
-            const float *a_base = a.A + (m0 + a_row0) * a.lda + a_ch * 4;
-            const float *b_base = VEC_B ? a.B + static_cast<int64_t>(4 * b_c) * a.ldb + n0 + 4 * b_g0
-                                        : a.B + n0 + pt;
+            const float *a_base = Ai + (m0 + a_row0) * a.lda + a_ch * 4;
+            const float *b_base = VEC_B ? Bi + static_cast<int64_t>(4 * b_c) * a.ldb + n0 + 4 * b_g0
+                                        : Bi + n0 + pt;
             for (int kblk = kb; kblk < ke; ++kblk, ++it) {
                 const int s = it & 1;
                 const int64_t k0 = static_cast<int64_t>(kblk) * BK;
@@ -521,7 +544,7 @@ __global__ void __launch_bounds__(THREADS, 1) tf32x3_kernel(const Args a) {
                         const int64_t gm = m0 + a_row0 + r * 32, gk = k0 + a_ch * 4;
                         float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
                         if (gm < a.M) {
-                            const float *src = a.A + gm * a.lda + gk;
+                            const float *src = Ai + gm * a.lda + gk;
                             if (gk + 0 < a.K) v.x = __ldg(src + 0);
                             if (gk + 1 < a.K) v.y = __ldg(src + 1);
                             if (gk + 2 < a.K) v.z = __ldg(src + 2);
@@ -537,7 +560,7 @@ __global__ void __launch_bounds__(THREADS, 1) tf32x3_kernel(const Args a) {
                                 const int64_t gk = k0 + 4 * b_c + q, gn = n0 + 4 * (b_g0 + 32 * r);
                                 float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
                                 if (gk < a.K) {
-                                    const float *src = a.B + gk * a.ldb + gn;
+                                    const float *src = Bi + gk * a.ldb + gn;
                                     if (gn + 3 < a.N) {
                                         v = __ldg(reinterpret_cast<const float4 *>(src));
                                     } else {
@@ -554,7 +577,7 @@ __global__ void __launch_bounds__(THREADS, 1) tf32x3_kernel(const Args a) {
                             const int64_t gn = n0 + pt, gk = k0 + 4 * r;
                             float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
                             if (gn < a.N) {
-                                const float *src = a.B + gk * a.ldb + gn;
+                                const float *src = Bi + gk * a.ldb + gn;
                                 if (gk + 0 < a.K) v.x = __ldg(src);
                                 if (gk + 1 < a.K) v.y = __ldg(src + a.ldb);
                                 if (gk + 2 < a.K) v.z = __ldg(src + 2 * a.ldb);
@@ -611,12 +634,12 @@ __global__ void __launch_bounds__(THREADS, 1) tf32x3_kernel(const Args a) {
             const int buf = unit & 1;
             if (!mbar_wait(bar(4 + buf), (unit >> 1) & 1, a, abort_flag, WD_EPILOGUE)) return;
             tc_fence_after();
-            const int64_t m0 = static_cast<int64_t>(tile / a.tiles_n) * BM;
-            const int64_t n0 = static_cast<int64_t>(tile % a.tiles_n) * BN;
+            const TileAt at = tile_at(a, tile);
+            const int64_t m0 = at.m0, n0 = at.n0;
             const int64_t row = m0 + q * 32 + lane;
             // Stream-K tiles were scaled by beta beforehand: every unit adds.
             const bool atomic = tile >= a.dp_tiles;
-            float *crow = a.C + row * a.ldc;
+            float *crow = a.C + at.item * a.strideC + row * a.ldc;
 #pragma unroll 1
             for (int ch = 0; ch < BN / 32; ++ch) {
                 float v[32];
@@ -769,8 +792,9 @@ __global__ void __launch_bounds__(tma::THREADS, 1)
             bool ok = true;
             for_each_unit(a, abort_flag, [&](int tile, int kb, int ke) {
                 if (!ok) return;
-                const int m0 = (tile / a.tiles_n) * BM;
-                const int n0 = (tile % a.tiles_n) * BN;
+                const TileAt at = tile_at(a, tile);
+                const int m0 = static_cast<int>(at.m0), n0 = static_cast<int>(at.n0);
+                const int za = a.a_shared ? 0 : at.item, zb = a.b_shared ? 0 : at.item;
                 for (int kblk = kb; kblk < ke; ++kblk, ++it) {
                     const int s = it & 1;
                     const int k0 = kblk * BK;
@@ -780,14 +804,14 @@ __global__ void __launch_bounds__(tma::THREADS, 1)
                         return;
                     }
                     mbar_arrive_expect_tx(bar(11), tma::STAGING_BYTES);
-                    tma_load_2d(staging, &tmB, n0, k0, bar(11));
+                    tma_load_3d(staging, &tmB, n0, k0, zb, bar(11));
                     // A straight into the stage once the MMA is done with it.
                     if (!mbar_wait(bar(2 + s), ((it >> 1) & 1) ^ 1, a, abort_flag, WD_PRODUCER)) {
                         ok = false;
                         return;
                     }
                     mbar_arrive_expect_tx(bar(s), A_TILE);
-                    tma_load_2d(base + static_cast<uint32_t>(s * STAGE_BYTES) + tma::A_RAW, &tmA, k0, m0, bar(s));
+                    tma_load_3d(base + static_cast<uint32_t>(s * STAGE_BYTES) + tma::A_RAW, &tmA, k0, m0, za, bar(s));
                 }
             });
         }
@@ -862,12 +886,12 @@ __global__ void __launch_bounds__(tma::THREADS, 1)
             const int buf = unit & 1;
             if (!mbar_wait(bar(4 + buf), (unit >> 1) & 1, a, abort_flag, WD_EPILOGUE)) return;
             tc_fence_after();
-            const int64_t m0 = static_cast<int64_t>(tile / a.tiles_n) * BM;
-            const int64_t n0 = static_cast<int64_t>(tile % a.tiles_n) * BN;
+            const TileAt at = tile_at(a, tile);
+            const int64_t m0 = at.m0, n0 = at.n0;
             const int64_t row = m0 + q * 32 + lane;
             // Stream-K tiles were scaled by beta beforehand: every unit adds.
             const bool atomic = tile >= a.dp_tiles;
-            float *crow = a.C + row * a.ldc;
+            float *crow = a.C + at.item * a.strideC + row * a.ldc;
 #pragma unroll 1
             for (int ch = 0; ch < BN / 32; ++ch) {
                 float v[32];
@@ -1007,8 +1031,9 @@ __global__ void __launch_bounds__(tm3::THREADS, 1)
             bool ok = true;
             for_each_unit(a, abort_flag, [&](int tile, int kb, int ke) {
                 if (!ok) return;
-                const int m0 = (tile / a.tiles_n) * BM;
-                const int n0 = (tile % a.tiles_n) * BN;
+                const TileAt at = tile_at(a, tile);
+                const int m0 = static_cast<int>(at.m0), n0 = static_cast<int>(at.n0);
+                const int za = a.a_shared ? 0 : at.item, zb = a.b_shared ? 0 : at.item;
                 for (int kblk = kb; kblk < ke; ++kblk, ++it) {
                     const int slot = it & 1;
                     if (!mbar_wait(bar(2 + slot), ((it >> 1) & 1) ^ 1, a, abort_flag, WD_PRODUCER)) {
@@ -1020,14 +1045,14 @@ __global__ void __launch_bounds__(tm3::THREADS, 1)
                     if (TA) {  // A stored K x M: four boxes of 32 m x 32 k
 #pragma unroll
                         for (int b = 0; b < BM / 32; ++b)
-                            tma_load_2d(sl + b * 4096, &tmA, m0 + 32 * b, kblk * BK, bar(slot));
+                            tma_load_3d(sl + b * 4096, &tmA, m0 + 32 * b, kblk * BK, za, bar(slot));
                     } else {
-                        tma_load_2d(sl, &tmA, kblk * BK, m0, bar(slot));
+                        tma_load_3d(sl, &tmA, kblk * BK, m0, za, bar(slot));
                     }
                     if (TB)  // B stored N x K: already K-major, 256 rows of 32 k
-                        tma_load_2d(sl + A_TILE, &tmB, kblk * BK, n0, bar(slot));
+                        tma_load_3d(sl + A_TILE, &tmB, kblk * BK, n0, zb, bar(slot));
                     else
-                        tma_load_2d(sl + A_TILE, &tmB, n0, kblk * BK, bar(slot));
+                        tma_load_3d(sl + A_TILE, &tmB, n0, kblk * BK, zb, bar(slot));
                 }
             });
         }
@@ -1128,12 +1153,12 @@ __global__ void __launch_bounds__(tm3::THREADS, 1)
         for_each_unit(a, abort_flag, [&](int tile, int kb, int ke) {
             if (!mbar_wait(bar(8), unit & 1, a, abort_flag, WD_EPILOGUE)) return;
             tc_fence_after();
-            const int64_t m0 = static_cast<int64_t>(tile / a.tiles_n) * BM;
-            const int64_t n0 = static_cast<int64_t>(tile % a.tiles_n) * BN;
+            const TileAt at = tile_at(a, tile);
+            const int64_t m0 = at.m0, n0 = at.n0;
             const int64_t row = m0 + q * 32 + lane;
             // Stream-K tiles were scaled by beta beforehand: every unit adds.
             const bool atomic = tile >= a.dp_tiles;
-            float *crow = a.C + row * a.ldc;
+            float *crow = a.C + at.item * a.strideC + row * a.ldc;
 #pragma unroll 1
             for (int ch = 0; ch < BN / 32; ++ch) {
                 float v[32];
@@ -1198,14 +1223,15 @@ int launch(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStream_t st
 
     const int64_t tiles_m = (p.M + BM - 1) / BM, tiles_n = (p.N + BN - 1) / BN;
     const int64_t k_blocks = (p.K + BK - 1) / BK;
-    if (tiles_m * tiles_n > INT32_MAX / 2 || k_blocks > INT32_MAX / 2) return SGEMM_ERR_UNSUPPORTED;
-    const int tiles = static_cast<int>(tiles_m * tiles_n);
+    if (tiles_m * tiles_n * p.batch > INT32_MAX / 2 || k_blocks > INT32_MAX / 2) return SGEMM_ERR_UNSUPPORTED;
+    const int tiles = static_cast<int>(tiles_m * tiles_n * p.batch);
     // One CTA per SM (the stage ring takes most of shared memory). A stream-K
     // share below 4 k-blocks costs more in fix-up than it saves.
     const Schedule sch = make_schedule(tiles, k_blocks, dev.sm_count, sk_mode, 4);
     if (tiles > sch.dp_tiles) {
-        int rc = scale_tiles_launch(p.C, p.M, p.N, p.ldc, p.beta, BM, BN, static_cast<int>(tiles_n),
-                                    sch.dp_tiles, tiles - sch.dp_tiles, stream, launches);
+        int rc = scale_tiles_launch(p.C, p.M, p.N, p.ldc, p.strideC, p.beta, BM, BN, static_cast<int>(tiles_n),
+                                    static_cast<int>(tiles_m * tiles_n), sch.dp_tiles, tiles - sch.dp_tiles,
+                                    stream, launches);
         if (rc != SGEMM_OK) return rc;
     }
     Args a;
@@ -1227,6 +1253,12 @@ int launch(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStream_t st
     a.watchdog = flag;
     a.alpha = p.alpha;
     a.beta = p.beta;
+    a.strideA = p.strideA;
+    a.strideB = p.strideB;
+    a.strideC = p.strideC;
+    a.tiles_per_item = static_cast<int>(tiles_m * tiles_n);
+    a.a_shared = p.strideA == 0;
+    a.b_shared = p.strideB == 0;
     kernel<<<sch.grid, THREADS, SMEM_BYTES, stream>>>(a);
     ++*launches;
     return cudaGetLastError() == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
@@ -1249,17 +1281,21 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
-// Row-major rows x cols fp32 matrix with row stride ld (elements), boxes of
-// box_cols x box_rows, out-of-range elements read as zero.
-bool encode_map(CUtensorMap *map, const float *ptr, int64_t rows, int64_t cols, int64_t ld, uint32_t box_cols,
-                uint32_t box_rows, CUtensorMapSwizzle swizzle) {
+// A batch of row-major rows x cols fp32 matrices with row stride ld and item
+// stride `stride` (elements; 0 = one matrix shared by all items), boxes of
+// box_cols x box_rows x 1, out-of-range elements read as zero.
+bool encode_map(CUtensorMap *map, const float *ptr, int64_t rows, int64_t cols, int64_t ld, int64_t batch,
+                int64_t stride, uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle swizzle) {
     auto enc = tensor_map_encoder();
     if (!enc) return false;
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * sizeof(float)};
-    const cuuint32_t box[2] = {box_cols, box_rows};
-    const cuuint32_t estr[2] = {1, 1};
-    return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(ptr), dims, strides, box, estr,
+    const int64_t items = stride == 0 ? 1 : batch;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
+                                static_cast<cuuint64_t>(items)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld) * sizeof(float),
+                                   static_cast<cuuint64_t>(stride == 0 ? ld * rows : stride) * sizeof(float)};
+    const cuuint32_t box[3] = {box_cols, box_rows, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(ptr), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -1268,8 +1304,12 @@ bool encode_map(CUtensorMap *map, const float *ptr, int64_t rows, int64_t cols, 
 // fit int32.
 bool tma_ok(const Problem &p) {
     return (reinterpret_cast<uintptr_t>(p.A) % 16 == 0) && (reinterpret_cast<uintptr_t>(p.B) % 16 == 0) &&
-           (p.lda % 4 == 0) && (p.ldb % 4 == 0) && p.M < INT32_MAX / 2 && p.N < INT32_MAX / 2 &&
-           p.K < INT32_MAX / 2 && tensor_map_encoder() != nullptr;
+           (p.lda % 4 == 0) && (p.ldb % 4 == 0) && (p.strideA % 4 == 0) && (p.strideB % 4 == 0) &&
+           p.M < INT32_MAX / 2 && p.N < INT32_MAX / 2 && p.K < INT32_MAX / 2 && p.batch < INT32_MAX / 2 &&
+           // batch items of A and B that overlap cannot be described as a tensor
+           (p.batch == 1 || p.strideA == 0 || p.strideA >= (p.transA ? p.K : p.M) * p.lda) &&
+           (p.batch == 1 || p.strideB == 0 || p.strideB >= (p.transB ? p.N : p.K) * p.ldb) &&
+           tensor_map_encoder() != nullptr;
 }
 
 std::once_flag g_tma_attr_once[kMaxDevices][16];
@@ -1294,20 +1334,23 @@ int launch_tma(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStream_
     int *flag = watchdog_flag_device_ptr();
     if (!flag) return SGEMM_ERR_LAUNCH;
     alignas(64) CUtensorMap mapA, mapB;
-    const bool ok_a = TA ? encode_map(&mapA, p.A, p.K, p.M, p.lda, 32, 32, CU_TENSOR_MAP_SWIZZLE_128B)
-                         : encode_map(&mapA, p.A, p.M, p.K, p.lda, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B);
-    const bool ok_b = TB ? encode_map(&mapB, p.B, p.N, p.K, p.ldb, BK, BN, CU_TENSOR_MAP_SWIZZLE_128B)
-                         : encode_map(&mapB, p.B, p.K, p.N, p.ldb, BN, BK, CU_TENSOR_MAP_SWIZZLE_NONE);
+    const bool ok_a =
+        TA ? encode_map(&mapA, p.A, p.K, p.M, p.lda, p.batch, p.strideA, 32, 32, CU_TENSOR_MAP_SWIZZLE_128B)
+           : encode_map(&mapA, p.A, p.M, p.K, p.lda, p.batch, p.strideA, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B);
+    const bool ok_b =
+        TB ? encode_map(&mapB, p.B, p.N, p.K, p.ldb, p.batch, p.strideB, BK, BN, CU_TENSOR_MAP_SWIZZLE_128B)
+           : encode_map(&mapB, p.B, p.K, p.N, p.ldb, p.batch, p.strideB, BN, BK, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (!ok_a || !ok_b) return SGEMM_ERR_LAUNCH;
 
     const int64_t tiles_m = (p.M + BM - 1) / BM, tiles_n = (p.N + BN - 1) / BN;
     const int64_t k_blocks = (p.K + BK - 1) / BK;
-    if (tiles_m * tiles_n > INT32_MAX / 2) return SGEMM_ERR_UNSUPPORTED;
-    const int tiles = static_cast<int>(tiles_m * tiles_n);
+    if (tiles_m * tiles_n * p.batch > INT32_MAX / 2) return SGEMM_ERR_UNSUPPORTED;
+    const int tiles = static_cast<int>(tiles_m * tiles_n * p.batch);
     const Schedule sch = make_schedule(tiles, k_blocks, dev.sm_count, sk_mode, 4);
     if (tiles > sch.dp_tiles) {
-        int rc = scale_tiles_launch(p.C, p.M, p.N, p.ldc, p.beta, BM, BN, static_cast<int>(tiles_n),
-                                    sch.dp_tiles, tiles - sch.dp_tiles, stream, launches);
+        int rc = scale_tiles_launch(p.C, p.M, p.N, p.ldc, p.strideC, p.beta, BM, BN, static_cast<int>(tiles_n),
+                                    static_cast<int>(tiles_m * tiles_n), sch.dp_tiles, tiles - sch.dp_tiles,
+                                    stream, launches);
         if (rc != SGEMM_OK) return rc;
     }
     Args a{};
@@ -1325,6 +1368,12 @@ int launch_tma(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStream_
     a.watchdog = flag;
     a.alpha = p.alpha;
     a.beta = p.beta;
+    a.strideA = p.strideA;
+    a.strideB = p.strideB;
+    a.strideC = p.strideC;
+    a.tiles_per_item = static_cast<int>(tiles_m * tiles_n);
+    a.a_shared = p.strideA == 0;
+    a.b_shared = p.strideB == 0;
     kernel<<<sch.grid, threads, smem, stream>>>(mapA, mapB, a);
     ++*launches;
     return cudaGetLastError() == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
@@ -1403,7 +1452,7 @@ bool tf32x3_supports(const Problem &p, const DeviceInfo &dev) {
 
 int tf32x3_launch(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStream_t stream, int *launches) {
     if (!tf32x3_supports(p, dev) || dev.device < 0 || dev.device >= kMaxDevices) return SGEMM_ERR_UNSUPPORTED;
-    const bool vc = (p.ldc % 4 == 0) && (reinterpret_cast<uintptr_t>(p.C) % 16 == 0);
+    const bool vc = (p.ldc % 4 == 0) && (p.strideC % 4 == 0) && (reinterpret_cast<uintptr_t>(p.C) % 16 == 0);
     const int mode = g_use_tma.load();
     if (p.transA || p.transB) {
         // Transposed forms: the tensor-memory kernel (TMA loads needed).
@@ -1423,8 +1472,8 @@ int tf32x3_launch(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStre
     if (mode >= 1 && tma_ok(p))
         return vc ? launch_tma<false, true>(p, dev, sk_mode, stream, launches)
                   : launch_tma<false, false>(p, dev, sk_mode, stream, launches);
-    const bool va = (p.lda % 4 == 0) && (reinterpret_cast<uintptr_t>(p.A) % 16 == 0);
-    const bool vb = (p.ldb % 4 == 0) && (reinterpret_cast<uintptr_t>(p.B) % 16 == 0);
+    const bool va = (p.lda % 4 == 0) && (p.strideA % 4 == 0) && (reinterpret_cast<uintptr_t>(p.A) % 16 == 0);
+    const bool vb = (p.ldb % 4 == 0) && (p.strideB % 4 == 0) && (reinterpret_cast<uintptr_t>(p.B) % 16 == 0);
     const int idx = (va ? 4 : 0) + (vb ? 2 : 0) + (vc ? 1 : 0);
     switch (idx) {
         case 0: return launch<false, false, false>(p, dev, sk_mode, stream, launches);

@@ -39,6 +39,8 @@ SIGNATURES = {
     "sgemm_f32": (_int, [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _vp]),
     "sgemm_f32_ex": (_int, [_int, _int, _i64, _i64, _i64, ctypes.c_float, _vp, _i64, _vp, _i64,
                             ctypes.c_float, _vp, _i64, _vp]),
+    "sgemm_f32_batched": (_int, [_int, _int, _i64, _i64, _i64, ctypes.c_float, _vp, _i64, _i64, _vp, _i64,
+                                 _i64, ctypes.c_float, _vp, _i64, _i64, _i64, _vp]),
     "sgemm_f32_from_host": (_int, [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _vp, _vp, _vp, _vp]),
     "sgemm_set_variant": (_int, [_int]),
     "sgemm_get_variant": (_int, []),
@@ -209,6 +211,44 @@ def gemm(A, B, C=None, *, transA=False, transB=False, alpha=1.0, beta=0.0, strea
                           B.data_ptr(), ldb, float(beta), C.data_ptr(), ldc, _stream_handle(stream))
     if rc:
         raise SgemmError(rc, "sgemm_f32_ex")
+    return C
+
+
+def gemm_batched(A, B, C=None, *, transA=False, transB=False, alpha=1.0, beta=0.0, stream=None):
+    """C[b] = alpha * op(A[b]) @ op(B[b]) + beta * C[b] for 3-D float32 CUDA tensors.
+
+    A is batch x M x K (batch x K x M when transA), B batch x K x N (batch x N
+    x K when transB), C batch x M x N; each item row-major with unit column
+    stride; a batch dimension of size 1 with stride 0 (expand) shares one
+    matrix across the batch.
+    """
+    import torch
+
+    def dims(t, name):
+        if not isinstance(t, torch.Tensor) or t.dtype != torch.float32 or t.dim() != 3 or not t.is_cuda:
+            raise TypeError(f"{name} must be a 3-D float32 CUDA tensor")
+        if t.shape[2] > 1 and t.stride(2) != 1:
+            raise ValueError(f"{name} must have unit column stride")
+        ld = t.stride(1) if t.shape[1] > 1 else max(t.shape[2], 1)
+        return ld, t.stride(0)
+
+    batch = A.shape[0]
+    lda, sa = dims(A, "A")
+    ldb, sb = dims(B, "B")
+    M, K = (A.shape[2], A.shape[1]) if transA else (A.shape[1], A.shape[2])
+    K2, N = (B.shape[2], B.shape[1]) if transB else (B.shape[1], B.shape[2])
+    if K != K2 or B.shape[0] != batch:
+        raise ValueError("shape mismatch")
+    if C is None:
+        if beta != 0.0:
+            raise ValueError("beta != 0 needs C")
+        C = torch.empty((batch, M, N), dtype=torch.float32, device=A.device)
+    ldc, sc = dims(C, "C")
+    rc = lib.sgemm_f32_batched(int(transA), int(transB), M, N, K, float(alpha), A.data_ptr(), lda, sa,
+                               B.data_ptr(), ldb, sb, float(beta), C.data_ptr(), ldc, sc, batch,
+                               _stream_handle(stream))
+    if rc:
+        raise SgemmError(rc, "sgemm_f32_batched")
     return C
 
 

@@ -107,3 +107,34 @@ def sample_positions(M: int, N: int, count: int, seed: int = 0):
     r = np.concatenate([np.array(fixed_r), rng.integers(0, M, count)])
     c = np.concatenate([np.array(fixed_c), rng.integers(0, N, count)])
     return r.astype(np.int64), c.astype(np.int64)
+
+
+@dataclass(frozen=True)
+class BatchedWorkload:
+    """A strided batch of independent products of one shape (items packed)."""
+    name: str
+    batch: int
+    M: int
+    N: int
+    K: int
+    dist: str
+    seed: int = 0
+
+    @property
+    def flops(self) -> int:
+        return 2 * self.batch * self.M * self.N * self.K
+
+
+# Many small products: the tiled-decomposition workload of "【infra之路】Tiled
+# Matrix Multiplication详解" taken per item (each item tiled independently).
+B512_128 = BatchedWorkload("batch512_m128_n128_k128_normal_s5", 512, 128, 128, 128, "normal", 5)
+B32_512 = BatchedWorkload("batch32_m512_n512_k512_normal_s6", 32, 512, 512, 512, "normal", 6)
+BATCHED = (B512_128, B32_512)
+
+
+def make_batched(w: BatchedWorkload):
+    """(A, B) float32 arrays of shape (batch, M, K) and (batch, K, N)."""
+    rng = np.random.default_rng(w.seed)
+    A = _draw(rng, (w.batch, w.M, w.K), w.dist)
+    B = _draw(rng, (w.batch, w.K, w.N), w.dist)
+    return A, B

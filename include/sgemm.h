@@ -112,6 +112,21 @@ int sgemm_f32_ex(int transA, int transB, int64_t M, int64_t N, int64_t K, float 
                  sgemm_stream_t stream);
 
 /*
+ * Strided batch of independent products: for b = 0 .. batch-1,
+ *     C_b = alpha * op(A_b) * op(B_b) + beta * C_b
+ * with A_b = A + b*strideA, B_b = B + b*strideB, C_b = C + b*strideC
+ * (strides in elements). Each item follows sgemm_f32_ex (same transA, transB,
+ * M, N, K, alpha, beta, lda, ldb, ldc for all items). strideA or strideB may
+ * be 0 (one matrix shared by every item); C items must not overlap one
+ * another (strideC >= (M-1)*ldc + N) nor any A or B item. batch == 0:
+ * nothing is enqueued. The whole batch runs as one persistent launch (plus a
+ * small scaling launch when some tiles are split along K).
+ */
+int sgemm_f32_batched(int transA, int transB, int64_t M, int64_t N, int64_t K, float alpha, const float *A,
+                      int64_t lda, int64_t strideA, const float *B, int64_t ldb, int64_t strideB, float beta,
+                      float *C, int64_t ldc, int64_t strideC, int64_t batch, sgemm_stream_t stream);
+
+/*
  * C = A * B for matrices that live in HOST memory, through caller-owned
  * device buffers. Enqueues, on `stream`: the copy of A_host into dA and of
  * B_host into dB (row strides kept), the product into dC, and the copy of

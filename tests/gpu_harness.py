@@ -104,3 +104,50 @@ def run_gemm_ex(A: np.ndarray, B: np.ndarray, *, transA=False, transB=False, alp
     flat = fc.cpu().numpy()
     box = vC.cpu().numpy() if M and N else np.zeros((M, N), np.float32)
     return box, flat, rc
+
+
+def run_batched(As, Bs, *, transA=False, transB=False, alpha=1.0, beta=0.0, C0=None,
+                strideA=None, strideB=None, strideC=None, share_a=False, share_b=False):
+    """sgemm_f32_batched on lists of stored-form items (dense rows). Items sit
+    stride elements apart in one buffer (default: packed); share_a / share_b
+    pass stride 0 with a single matrix. Returns (list of C items, flat C
+    buffer, status, strideC)."""
+    import torch
+    from dense_fp32_matrix_major_gb300 import sgemm
+
+    batch = len(As)
+    A0, B0 = As[0], Bs[0]
+    M = A0.shape[1] if transA else A0.shape[0]
+    K = A0.shape[0] if transA else A0.shape[1]
+    N = B0.shape[0] if transB else B0.shape[1]
+    lda, ldb, ldc = max(A0.shape[1], 1), max(B0.shape[1], 1), max(N, 1)
+
+    def pack(items, stride, share, fill):
+        rows, cols = items[0].shape
+        stride = 0 if share else (rows * cols if stride is None else stride)
+        n = 1 if share else len(items)
+        size = (n - 1) * stride + rows * cols + GUARD
+        flat = np.full(size, fill, dtype=np.float32)
+        for b in range(n):
+            flat[b * stride: b * stride + rows * cols] = np.ascontiguousarray(items[b]).ravel()
+        return torch.from_numpy(flat).cuda(), stride
+
+    dA, sA = pack(As, strideA, share_a, 0.0)
+    dB, sB = pack(Bs, strideB, share_b, 0.0)
+    Cs = C0 if C0 is not None else [np.full((M, N), np.nan, np.float32) for _ in range(batch)]
+    dC, sC = pack(Cs, strideC, False, CANARY)
+    stream = torch.cuda.current_stream()
+    rc = sgemm.lib.sgemm_f32_batched(int(transA), int(transB), M, N, K, float(alpha), dA.data_ptr(), lda,
+                                     sA, dB.data_ptr(), ldb, sB, float(beta), dC.data_ptr(), ldc, sC,
+                                     batch, stream.cuda_stream)
+    torch.cuda.synchronize()
+    flat = dC.cpu().numpy()
+    out = [flat[b * sC: b * sC + M * N].reshape(M, N).copy() for b in range(batch)]
+    return out, flat, rc, sC
+
+
+def batched_outside_intact(flat, batch, M, N, strideC):
+    mask = np.ones(flat.shape[0], dtype=bool)
+    for b in range(batch):
+        mask[b * strideC: b * strideC + M * N] = False
+    return bool(np.all(flat[mask].view(np.uint32) == np.float32(CANARY).view(np.uint32)))
