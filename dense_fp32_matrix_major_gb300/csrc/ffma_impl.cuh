@@ -278,9 +278,15 @@ __device__ __forceinline__ void process_tile(const FfmaArgs &a, float *As, float
 #pragma unroll
             for (int q = 0; q < 4; ++q) v[q] = alpha * acc[i][c * 4 + q];
             if (atomic) {
+                if (vec_c && col + 3 < a.N) {
+                    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(crow + col), "f"(v[0]),
+                                 "f"(v[1]), "f"(v[2]), "f"(v[3])
+                                 : "memory");
+                } else {
 #pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    if (col + q < a.N) atomicAdd(crow + col + q, v[q]);
+                    for (int q = 0; q < 4; ++q)
+                        if (col + q < a.N) atomicAdd(crow + col + q, v[q]);
+                }
             } else if (vec_c && col + 3 < a.N) {
                 float4 *p = reinterpret_cast<float4 *>(crow + col);
                 if (beta != 0.0f) {
@@ -375,7 +381,7 @@ int launch_cfg(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStream_
     const int tiles = static_cast<int>(tiles64);
     const int slots = dev.sm_count * per_sm;
     // A stream-K share below this many k-steps costs more in fix-up than it saves.
-    const Schedule sch = make_schedule(tiles, k_tiles, slots, sk_mode, 8);
+    const Schedule sch = make_schedule(tiles, k_tiles, slots, sk_mode, 8, 0.10);
 
     FfmaArgs a;
     a.M = p.M;
@@ -412,14 +418,15 @@ int launch_cfg(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStream_
 }
 
 // Block tile for AUTO: large outputs take the widest register tile (fewest
-// shared-memory loads per FFMA); small outputs smaller tiles so the grid
-// covers the SMs.
+// shared-memory loads per FFMA); below a full wave of those, 128 x 128 tiles
+// with stream-K (measured faster than 64 x 64 at 512^3 and 1024^3 on GB300);
+// 64 x 64 only for outputs of a handful of tiles.
 inline int pick_tile(const Problem &p, const DeviceInfo &dev, int tile) {
     if (tile != FFMA_TILE_AUTO) return tile;
     const int64_t big_tiles = ceil_div(p.M, CfgBig::BM) * ceil_div(p.N, CfgBig::BN) * p.batch;
     const int64_t mid_tiles = ceil_div(p.M, CfgMid::BM) * ceil_div(p.N, CfgMid::BN) * p.batch;
     if (big_tiles >= dev.sm_count) return FFMA_TILE_128x256;
-    if (mid_tiles >= dev.sm_count / 2) return FFMA_TILE_128x128;
+    if (mid_tiles >= 8) return FFMA_TILE_128x128;
     return FFMA_TILE_64x64;
 }
 

@@ -84,8 +84,8 @@ int check_args(int transA, int transB, int64_t M, int64_t N, int64_t K, const fl
     return SGEMM_OK;
 }
 
-// AUTO: the tensor-core path from 2^29 useful multiply-adds up (measured on
-// GB300: FFMA is faster at 512^3, the tensor-core path from 1024^3 on), and
+// AUTO: the tensor-core path from 2^26 useful multiply-adds up (measured on
+// GB300: it is faster than FFMA from 512^3 on), and
 // only up to K = 8192: its accumulation rounds toward zero, so its error
 // grows with K (2.9e-6 of the 1e-5 bound at K = 4096); beyond that the FFMA
 // path keeps the bound at any K. "Useful" discounts the padding of the
@@ -97,7 +97,7 @@ int auto_variant(const Problem &p, const DeviceInfo &dev) {
     const double fill = static_cast<double>(p.M) * static_cast<double>(p.N) / (m_pad * n_pad);
     const double work = static_cast<double>(p.M) * static_cast<double>(p.N) * static_cast<double>(p.K) *
                         static_cast<double>(p.batch) * fill;
-    if (work >= 536870912.0 && p.K <= 8192 && tf32x3_supports(p, dev)) return SGEMM_TF32X3;
+    if (work >= 67108864.0 && p.K <= 8192 && tf32x3_supports(p, dev)) return SGEMM_TF32X3;
     return SGEMM_FFMA;
 }
 

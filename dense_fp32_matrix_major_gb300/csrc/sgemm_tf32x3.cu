@@ -350,6 +350,12 @@ __device__ __forceinline__ uint32_t sw128_offset(int row, int chunk) {
     return static_cast<uint32_t>(row * 128 + ((chunk ^ (row & 7)) << 4));
 }
 
+// Atomic add of four consecutive floats at a 16-byte aligned address.
+__device__ __forceinline__ void red_add_v4(float *p, float a, float b, float c, float d) {
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d)
+                 : "memory");
+}
+
 // Writes 32 accumulator values (columns col0 .. col0 + 31 of one row of C):
 // C = alpha * v + beta * C (C read only when beta != 0), or, for a tile split
 // along K (C already scaled by beta), C += alpha * v with atomics.
@@ -359,9 +365,15 @@ __device__ __forceinline__ void store_chunk(const Args &a, float *crow, int64_t 
     if (row >= a.M || col0 >= a.N) return;
     const float alpha = a.alpha, beta = a.beta;
     if (atomic) {
+        if (VEC_C && col0 + 31 < a.N) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-            if (col0 + j < a.N) atomicAdd(crow + col0 + j, alpha * v[j]);
+            for (int j = 0; j < 32; j += 4)
+                red_add_v4(crow + col0 + j, alpha * v[j], alpha * v[j + 1], alpha * v[j + 2], alpha * v[j + 3]);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                if (col0 + j < a.N) atomicAdd(crow + col0 + j, alpha * v[j]);
+        }
     } else if (VEC_C && col0 + 31 < a.N) {
 #pragma unroll
         for (int j = 0; j < 32; j += 4) {
@@ -1227,7 +1239,7 @@ int launch(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStream_t st
     const int tiles = static_cast<int>(tiles_m * tiles_n * p.batch);
     // One CTA per SM (the stage ring takes most of shared memory). A stream-K
     // share below 4 k-blocks costs more in fix-up than it saves.
-    const Schedule sch = make_schedule(tiles, k_blocks, dev.sm_count, sk_mode, 4);
+    const Schedule sch = make_schedule(tiles, k_blocks, dev.sm_count, sk_mode, 4, 0.25);
     if (tiles > sch.dp_tiles) {
         int rc = scale_tiles_launch(p.C, p.M, p.N, p.ldc, p.strideC, p.beta, BM, BN, static_cast<int>(tiles_n),
                                     static_cast<int>(tiles_m * tiles_n), sch.dp_tiles, tiles - sch.dp_tiles,
@@ -1346,7 +1358,7 @@ int launch_tma(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStream_
     const int64_t k_blocks = (p.K + BK - 1) / BK;
     if (tiles_m * tiles_n * p.batch > INT32_MAX / 2) return SGEMM_ERR_UNSUPPORTED;
     const int tiles = static_cast<int>(tiles_m * tiles_n * p.batch);
-    const Schedule sch = make_schedule(tiles, k_blocks, dev.sm_count, sk_mode, 4);
+    const Schedule sch = make_schedule(tiles, k_blocks, dev.sm_count, sk_mode, 4, 0.25);
     if (tiles > sch.dp_tiles) {
         int rc = scale_tiles_launch(p.C, p.M, p.N, p.ldc, p.strideC, p.beta, BM, BN, static_cast<int>(tiles_n),
                                     static_cast<int>(tiles_m * tiles_n), sch.dp_tiles, tiles - sch.dp_tiles,
