@@ -79,8 +79,11 @@ def _load():
                                             _vp, _i64, _d, _vp, _i64, _vp, _vp, _i64]
             lib.oracle_gemm_f64_at.argtypes = [ctypes.c_int, ctypes.c_int, _i64, _i64, _i64, _d, _vp,
                                                _i64, _vp, _i64, _d, _vp, _i64, _i64, _vp, _vp, _vp, _vp]
+            lib.oracle_epilogue_f64.argtypes = [_i64, _vp, _vp, _i64, _i64, _vp, ctypes.c_int, ctypes.c_int,
+                                                _vp, _vp]
             for fn in (lib.oracle_sgemm_f32, lib.oracle_sgemm_f64, lib.oracle_sgemm_f64_rows,
-                       lib.oracle_sgemm_f64_at, lib.oracle_gemm_f64, lib.oracle_gemm_f64_at):
+                       lib.oracle_sgemm_f64_at, lib.oracle_gemm_f64, lib.oracle_gemm_f64_at,
+                       lib.oracle_epilogue_f64):
                 fn.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -222,6 +225,46 @@ def gemm_f64_at(A, B, rows, cols, *, transA=False, transB=False, alpha=1.0, beta
                                       c.ctypes.data, c64.ctypes.data, s.ctypes.data),
            "oracle_gemm_f64_at")
     return c64, s
+
+
+_BIAS_KINDS = {None: 0, "none": 0, "col": 1, "row": 2}
+_ACTS = {None: 0, "none": 0, "relu": 1, "gelu": 2, "silu": 3}
+
+
+def epilogue_f64(c64, s, *, bias=None, bias_kind=None, act=None, rows=None, cols=None, shape=None):
+    """(act(c64 + bias), s + |bias|) for values of a double product, as new arrays.
+
+    ``c64`` and ``s`` are the full M x N result, or 1-D samples at
+    ``(rows[t], cols[t])`` of a result of the given ``shape`` (M, N).
+    ``bias_kind`` is None / "col" (bias[j], N values) / "row" (bias[i], M
+    values); ``act`` is None / "relu" / "gelu" / "silu".
+    """
+    kind = _BIAS_KINDS[bias_kind]
+    code = _ACTS[act]
+    flat = np.array(c64, dtype=np.float64).reshape(-1)
+    sflat = np.array(s, dtype=np.float64).reshape(-1)
+    if rows is None:
+        M, N = np.shape(c64)
+        rr, cc = np.indices((M, N))
+        r, c = rr.reshape(-1), cc.reshape(-1)
+    else:
+        if shape is None:
+            raise ValueError("samples need the shape (M, N) of the result")
+        M, N = shape
+        r, c = rows, cols
+    r = np.ascontiguousarray(r, dtype=np.int64)
+    c = np.ascontiguousarray(c, dtype=np.int64)
+    if r.shape != flat.shape or c.shape != flat.shape or sflat.shape != flat.shape:
+        raise ValueError("samples, values and scales must have the same length")
+    pb = None
+    if kind:
+        b = np.ascontiguousarray(bias, dtype=np.float32).reshape(-1)
+        if b.shape[0] != (N if kind == 1 else M):
+            raise ValueError("bias length must be N (per column) or M (per row)")
+        pb = b.ctypes.data
+    _check(_load().oracle_epilogue_f64(flat.shape[0], r.ctypes.data, c.ctypes.data, M, N, pb, kind, code,
+                                       flat.ctypes.data, sflat.ctypes.data), "oracle_epilogue_f64")
+    return flat.reshape(np.shape(c64)), sflat.reshape(np.shape(s))
 
 
 def normalized_error(C_test, C64, S) -> float:

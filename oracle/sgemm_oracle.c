@@ -46,6 +46,17 @@
  *                        |beta| |C_in|. The pages define only C = A * B; the
  *                        general form is the standard BLAS GEMM, taken with
  *                        its convention that beta = 0 means C_in is not read.
+ *   oracle_epilogue_f64  the fused epilogue act(x + bias) applied to values
+ *                        of the double product, in double, with |bias| added
+ *                        to S. The pages compute the product alone and call
+ *                        it the core operation of neural-network layers
+ *                        ("CUDA内存优化入门：从Naive到Tiled矩阵乘法",
+ *                        section 一); a layer adds a bias and applies an
+ *                        activation to it. Each activation is its textbook
+ *                        definition on top of libm: ReLU(x) = max(x, 0) with
+ *                        NaN kept, GELU(x) = x Phi(x) with the standard
+ *                        normal CDF Phi(x) = (1 + erf(x / sqrt 2)) / 2,
+ *                        SiLU(x) = x sigma(x) = x / (1 + exp(-x)).
  *
  * Pins (tests/test_oracle_pins.py, CPU only): all-ones inputs give C = K
  * exactly (the all-ones check of "CUDA 性能优化实战笔记 + C++示例代码（第七章
@@ -286,6 +297,48 @@ int oracle_gemm_f64_at(int transA, int transB, int64_t M, int64_t N, int64_t K, 
         double c_in = beta != 0.0 ? (double)C_in[i * ldc_in + j] : 0.0;
         gemm_element(transA, transB, K, alpha, A, lda, B, ldb, beta, c_in, i, j, &c64[t],
                      s ? &s[t] : NULL);
+    }
+    return 0;
+}
+
+/* Activation codes of oracle_epilogue_f64 (this oracle's own numbering). */
+enum { ORACLE_ACT_NONE = 0, ORACLE_ACT_RELU = 1, ORACLE_ACT_GELU = 2, ORACLE_ACT_SILU = 3 };
+enum { ORACLE_BIAS_NONE = 0, ORACLE_BIAS_COL = 1, ORACLE_BIAS_ROW = 2 };
+
+static double oracle_activate(int act, double x)
+{
+    switch (act) {
+    case ORACLE_ACT_RELU:
+        return x < 0.0 ? 0.0 : x;
+    case ORACLE_ACT_GELU: {
+        double phi = 0.5 * (1.0 + erf(x / sqrt(2.0))); /* standard normal CDF */
+        return x * phi;
+    }
+    case ORACLE_ACT_SILU: {
+        double sigma = 1.0 / (1.0 + exp(-x)); /* logistic function */
+        return x * sigma;
+    }
+    default:
+        return x;
+    }
+}
+
+int oracle_epilogue_f64(int64_t n, const int64_t *rows, const int64_t *cols, int64_t M, int64_t N,
+                        const float *bias, int bias_kind, int act, double *c64, double *s)
+{
+    if (n < 0 || M < 0 || N < 0) return 1;
+    if (bias_kind < ORACLE_BIAS_NONE || bias_kind > ORACLE_BIAS_ROW) return 1;
+    if (act < ORACLE_ACT_NONE || act > ORACLE_ACT_SILU) return 1;
+    if (n > 0 && (!rows || !cols || !c64)) return 1;
+    if (n > 0 && bias_kind != ORACLE_BIAS_NONE && !bias) return 1;
+    for (int64_t t = 0; t < n; ++t) {
+        int64_t i = rows[t], j = cols[t];
+        if (i < 0 || i >= M || j < 0 || j >= N) return 1;
+        double b = 0.0;
+        if (bias_kind == ORACLE_BIAS_COL) b = (double)bias[j];
+        if (bias_kind == ORACLE_BIAS_ROW) b = (double)bias[i];
+        c64[t] = oracle_activate(act, c64[t] + b);
+        if (s) s[t] += fabs(b);
     }
     return 0;
 }

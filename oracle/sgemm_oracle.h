@@ -46,6 +46,14 @@ int oracle_gemm_f64_at(int transA, int transB, int64_t M, int64_t N, int64_t K, 
                        const float *C_in, int64_t ldc_in, int64_t n_samples, const int64_t *rows,
                        const int64_t *cols, double *c64, double *s);
 
+/* Fused epilogue on n values of a double product at (rows[t], cols[t]) of
+ * an M x N result, in place: x = c64[t] + b with b = bias[cols[t]]
+ * (bias_kind 1), bias[rows[t]] (2) or 0 (0); c64[t] = act(x) with act
+ * 0 none, 1 ReLU, 2 GELU (x Phi(x)), 3 SiLU (x / (1 + exp(-x))); s[t] += |b|
+ * (s may be NULL). */
+int oracle_epilogue_f64(int64_t n, const int64_t *rows, const int64_t *cols, int64_t M, int64_t N,
+                        const float *bias, int bias_kind, int act, double *c64, double *s);
+
 #ifdef __cplusplus
 }
 #endif
