@@ -311,6 +311,49 @@ def run_batched_bench(args, bw, torch):
             "launches_per_step": sgemm.last_launch_count(), "parity_sampled_err": err}
 
 
+def run_fused_bench(args, w, torch, plain_ms):
+    """GFLOP/s of the fused product act(A B + bias) at workload w, one line per
+    (bias kind, activation), against the plain product's time; sampled parity
+    against the oracle's product followed by its epilogue."""
+    from dense_fp32_matrix_major_gb300 import sgemm
+    import oracle  # test infrastructure: spot check only
+
+    _, _, local = _dist_env()
+    device = torch.device("cuda", local)
+    sgemm.set_variant(args.variant)
+    A, B, dA, dB, dC = _device_inputs(w, torch, device)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream()
+    out = []
+    for kind, act in (("col", "gelu"), ("col", "relu"), ("row", "silu")):
+        bias = (np.random.default_rng(17).standard_normal(w.N if kind == "col" else w.M)).astype(np.float32)
+        dbias = torch.from_numpy(bias).to(device)
+        for _ in range(args.warmup):
+            flush.zero_()
+            sgemm.gemm_fused(dA, dB, dC, bias=dbias, bias_kind=kind, act=act)
+        torch.cuda.synchronize()
+        steps = max(3, min(args.steps, 500))
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for e0, e1 in ev:
+            flush.zero_()
+            e0.record(stream)
+            sgemm.gemm_fused(dA, dB, dC, bias=dbias, bias_kind=kind, act=act)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        ms = sum(e0.elapsed_time(e1) for e0, e1 in ev) / steps
+        r, c = wl.sample_positions(w.M, w.N, 64, seed=7)
+        c64, sc = oracle.sgemm_f64_at(A, B, r, c)
+        e64, es = oracle.epilogue_f64(c64, sc, bias=bias, bias_kind=kind, act=act, rows=r, cols=c,
+                                      shape=(w.M, w.N))
+        err = oracle.normalized_error(dC.cpu().numpy()[r, c], e64, es)
+        out.append({"workload": w.name, "epilogue": f"bias per {kind} + {act}",
+                    "value": round(w.flops / (ms * 1e-3) / 1e9, 2), "unit": UNIT, "ms_per_step": round(ms, 5),
+                    "plain_ms_per_step": round(plain_ms, 5), "overhead": round(ms / plain_ms - 1.0, 4),
+                    "variant": sgemm.variant_name(sgemm.last_variant_used()),
+                    "launches_per_step": sgemm.last_launch_count(), "parity_sampled_err": err})
+    return out
+
+
 def run_e2e(args, w, torch, sgemm, A, B, device, dist, ws):
     Ah = torch.from_numpy(np.ascontiguousarray(A)).pin_memory()
     Bh = torch.from_numpy(np.ascontiguousarray(B)).pin_memory()
@@ -430,6 +473,8 @@ def main():
                     help="also print one extra line per workload (not the headline line)")
     ap.add_argument("--batched", action="store_true",
                     help="also print one extra line per strided-batched workload")
+    ap.add_argument("--fused", action="store_true",
+                    help="also print one extra line per fused epilogue (bias + activation) at the workload")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -482,6 +527,9 @@ def main():
         if args.batched:
             for bw in wl.BATCHED:
                 print(json.dumps(run_batched_bench(args, bw, torch)), flush=True)
+        if args.fused:
+            for line in run_fused_bench(args, w, torch, res["ms_per_step"]):
+                print(json.dumps(line), flush=True)
     if dist is not None:
         dist.barrier()
         dist.destroy_process_group()

@@ -10,6 +10,7 @@
 #include <algorithm>
 #include <mutex>
 
+#include "epilogue.cuh"
 #include "sgemm.h"
 #include "sgemm_internal.h"
 
@@ -35,6 +36,9 @@ struct FfmaArgs {
     int total_tiles;    // tiles [dp_tiles, total_tiles) are split along K
     int64_t sk_iters;   // (total_tiles - dp_tiles) * k_tiles
     int sk_ctas;        // CTAs [0, sk_ctas) share the split iterations evenly
+    const float *bias;  // fused epilogue: C = act(... + bias) on whole tiles
+    int bias_kind, act;
+    int ep;             // bias_kind or act set
 };
 
 template <int WARPS_M_, int WARPS_N_, int CN_, int STAGES_, int MIN_BLOCKS_, int KU_>
@@ -179,7 +183,9 @@ __device__ __forceinline__ void load_stage(const FfmaArgs &a, const float *__res
 }
 
 // One tile over k-tiles [kb, ke). atomic: add alpha * the partial sum into C
-// (C was scaled by beta beforehand) instead of storing.
+// (C was set to beta * C + bias beforehand; the activation comes after the
+// product) instead of storing. Otherwise the store applies the whole
+// epilogue: act(alpha * acc + beta * C + bias).
 template <class C, bool TA, bool TB, bool VEC_B, bool VEC_C>
 __device__ __forceinline__ void process_tile(const FfmaArgs &a, float *As, float *Bs, int tile, int kb,
                                              int ke, bool atomic) {
@@ -296,11 +302,19 @@ __device__ __forceinline__ void process_tile(const FfmaArgs &a, float *As, float
                     v[2] = fmaf(beta, o.z, v[2]);
                     v[3] = fmaf(beta, o.w, v[3]);
                 }
+                if (a.ep) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) v[q] = epilogue_value(v[q], a.bias, a.bias_kind, a.act, row, col + q);
+                }
                 *p = make_float4(v[0], v[1], v[2], v[3]);
             } else {
 #pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    if (col + q < a.N) crow[col + q] = beta != 0.0f ? fmaf(beta, crow[col + q], v[q]) : v[q];
+                for (int q = 0; q < 4; ++q) {
+                    if (col + q >= a.N) continue;
+                    float x = beta != 0.0f ? fmaf(beta, crow[col + q], v[q]) : v[q];
+                    if (a.ep) x = epilogue_value(x, a.bias, a.bias_kind, a.act, row, col + q);
+                    crow[col + q] = x;
+                }
             }
         }
     }
@@ -407,14 +421,17 @@ int launch_cfg(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStream_
     a.dp_tiles = sch.dp_tiles;
     a.sk_iters = sch.sk_iters;
     a.sk_ctas = sch.sk_ctas;
-    if (tiles > sch.dp_tiles) {
-        rc = scale_tiles_launch(p.C, p.M, p.N, p.ldc, p.strideC, p.beta, C::BM, C::BN, a.tiles_n,
-                                a.tiles_per_item, sch.dp_tiles, tiles - sch.dp_tiles, stream, launches);
-        if (rc != SGEMM_OK) return rc;
-    }
+    a.bias = p.bias;
+    a.bias_kind = p.bias_kind;
+    a.act = p.act;
+    a.ep = p.has_epilogue();
+    const int split = tiles - sch.dp_tiles;
+    rc = split_tiles_prepare(p, C::BM, C::BN, a.tiles_n, a.tiles_per_item, sch.dp_tiles, split, stream, launches);
+    if (rc != SGEMM_OK) return rc;
     ffma_kernel<C, TA, TB, VEC_B, VEC_C><<<sch.grid, C::THREADS, C::SMEM_BYTES, stream>>>(a);
     ++*launches;
-    return cudaGetLastError() == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
+    if (cudaGetLastError() != cudaSuccess) return SGEMM_ERR_LAUNCH;
+    return split_tiles_finish(p, C::BM, C::BN, a.tiles_n, a.tiles_per_item, sch.dp_tiles, split, stream, launches);
 }
 
 // Block tile for AUTO: large outputs take the widest register tile (fewest

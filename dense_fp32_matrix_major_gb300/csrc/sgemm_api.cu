@@ -84,6 +84,19 @@ int check_args(int transA, int transB, int64_t M, int64_t N, int64_t K, const fl
     return SGEMM_OK;
 }
 
+// Checks of the fused epilogue's arguments: known bias kind and activation,
+// a bias vector (M or N floats) that exists and does not overlap C.
+int check_epilogue(int64_t M, int64_t N, const float *C, int64_t ldc, const float *bias, int bias_kind,
+                   int act) {
+    if (bias_kind < SGEMM_BIAS_NONE || bias_kind > SGEMM_BIAS_PER_ROW) return SGEMM_ERR_INVALID_ARG;
+    if (act < SGEMM_ACT_NONE || act > SGEMM_ACT_SILU) return SGEMM_ERR_INVALID_ARG;
+    if (bias_kind == SGEMM_BIAS_NONE || M == 0 || N == 0) return SGEMM_OK;
+    const int64_t len = bias_kind == SGEMM_BIAS_PER_COL ? N : M;
+    if (!bias) return SGEMM_ERR_INVALID_ARG;
+    if (overlaps(C, M, N, ldc, bias, 1, len, len)) return SGEMM_ERR_INVALID_ARG;
+    return SGEMM_OK;
+}
+
 // AUTO: the tensor-core path from 2^26 useful multiply-adds up (measured on
 // GB300: it is faster than FFMA from 512^3 on), and
 // only up to K = 8192: its accumulation rounds toward zero, so its error
@@ -135,8 +148,8 @@ int enqueue(const Problem &p, cudaStream_t stream) {
         return SGEMM_OK;
     }
     if (p.K == 0 || p.alpha == 0.0f) {
-        // The empty sum (or alpha = 0): C = beta * C.
-        rc = scale_launch(p.C, p.M, p.N, p.ldc, p.strideC, p.batch, p.beta, dev, stream, &launches);
+        // The empty sum (or alpha = 0): C = act(beta * C + bias).
+        rc = scale_launch(p, dev, stream, &launches);
         if (rc == SGEMM_OK) {
             g_last_variant.store(SGEMM_FFMA);
             g_last_launches.store(launches);
@@ -213,6 +226,24 @@ int sgemm_f32_ex(int transA, int transB, int64_t M, int64_t N, int64_t K, float 
     p.transB = transB;
     p.alpha = alpha;
     p.beta = beta;
+    return sgemm::enqueue(p, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int sgemm_f32_fused(int transA, int transB, int64_t M, int64_t N, int64_t K, float alpha, const float *A,
+                    int64_t lda, const float *B, int64_t ldb, float beta, float *C, int64_t ldc,
+                    const float *bias, int bias_kind, int activation, sgemm_stream_t stream) {
+    int rc = sgemm::check_args(transA, transB, M, N, K, A, lda, B, ldb, C, ldc);
+    if (rc != SGEMM_OK) return rc;
+    rc = sgemm::check_epilogue(M, N, C, ldc, bias, bias_kind, activation);
+    if (rc != SGEMM_OK) return rc;
+    Problem p{M, N, K, A, lda, B, ldb, C, ldc};
+    p.transA = transA;
+    p.transB = transB;
+    p.alpha = alpha;
+    p.beta = beta;
+    p.bias = bias_kind == SGEMM_BIAS_NONE ? nullptr : bias;
+    p.bias_kind = bias_kind;
+    p.act = activation;
     return sgemm::enqueue(p, reinterpret_cast<cudaStream_t>(stream));
 }
 

@@ -36,12 +36,17 @@
 //     copied row for row (16 bytes when aligned), a transposed B is
 //     transposed by 4-byte copies into a swizzled Bs; the epilogue writes
 //     alpha * acc + beta * C and reads C only when beta != 0.
+//   * The fused epilogue (bias, activation; sgemm_f32_fused) is applied in
+//     the same store to whole tiles; split tiles get the bias in the beta
+//     pre-pass and the activation in a pass after the product.
 //
-// This file instantiates op(A) = A, op(B) = B and holds the scaling kernels;
+// This file instantiates op(A) = A, op(B) = B and holds the C passes (beta,
+// bias, activation) that run outside the product kernels;
 // sgemm_ffma_t.cu instantiates the transposed forms.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "epilogue.cuh"
 #include "ffma_impl.cuh"
 
 namespace sgemm {
@@ -49,12 +54,13 @@ namespace {
 
 using namespace ffma;
 
-// C = beta * C over `count` tiles starting at `first_tile` of a bm x bn tile
-// grid (C = 0 when beta = 0: C is not read); tiles run item-major over a
-// batch whose items are strideC elements apart. blockIdx.y picks the tile,
+// C = act(beta * C + bias) over `count` tiles starting at `first_tile` of a
+// bm x bn tile grid (C is not read when beta = 0); tiles run item-major over
+// a batch whose items are strideC elements apart. blockIdx.y picks the tile,
 // blockIdx.x a band of 8 rows; a warp handles one row (float4 when aligned).
-__global__ void scale_tiles_kernel(float *C, int64_t M, int64_t N, int64_t ldc, int64_t strideC, float beta, int bm,
-                                   int bn, int tiles_n, int tiles_per_item, int first_tile) {
+__global__ void tile_pass_kernel(float *C, int64_t M, int64_t N, int64_t ldc, int64_t strideC, float beta,
+                                 const float *bias, int bias_kind, int act, int bm, int bn, int tiles_n,
+                                 int tiles_per_item, int first_tile) {
     const int tile = first_tile + blockIdx.y;
     const int item = tile / tiles_per_item, rest = tile % tiles_per_item;
     C += item * strideC;
@@ -65,36 +71,42 @@ __global__ void scale_tiles_kernel(float *C, int64_t M, int64_t N, int64_t ldc, 
     const int cols = static_cast<int>(min64(bn, N - n0));
     float *p = C + row * ldc + n0;
     const int lane = threadIdx.x & 31;
+    const bool ep = bias_kind != SGEMM_BIAS_NONE || act != SGEMM_ACT_NONE;
+    auto one = [&](float c, int i) {
+        const float x = beta != 0.0f ? beta * c : 0.0f;
+        return ep ? epilogue_value(x, bias, bias_kind, act, row, n0 + i) : x;
+    };
+    int done = 0;
     if ((reinterpret_cast<uintptr_t>(p) & 15) == 0) {
         const int v4 = cols >> 2;
         float4 *p4 = reinterpret_cast<float4 *>(p);
         for (int i = lane; i < v4; i += 32) {
             float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (beta != 0.0f) {
-                v = p4[i];
-                v.x *= beta;
-                v.y *= beta;
-                v.z *= beta;
-                v.w *= beta;
-            }
+            if (beta != 0.0f) v = p4[i];
+            v.x = one(v.x, 4 * i);
+            v.y = one(v.y, 4 * i + 1);
+            v.z = one(v.z, 4 * i + 2);
+            v.w = one(v.w, 4 * i + 3);
             p4[i] = v;
         }
-        for (int i = 4 * v4 + lane; i < cols; i += 32) p[i] = beta != 0.0f ? beta * p[i] : 0.0f;
-    } else {
-        for (int i = lane; i < cols; i += 32) p[i] = beta != 0.0f ? beta * p[i] : 0.0f;
+        done = 4 * v4;
     }
+    for (int i = done + lane; i < cols; i += 32) p[i] = one(beta != 0.0f ? p[i] : 0.0f, i);
 }
 
-// C[0:M, 0:N] = beta * C (0 when beta = 0) for every item of a batch, with a
-// grid-stride loop.
+// C[0:M, 0:N] = act(beta * C + bias) (C not read when beta = 0) for every
+// item of a batch, with a grid-stride loop.
 __global__ void scale_rect_kernel(float *C, int64_t M, int64_t N, int64_t ldc, int64_t strideC, int64_t batch,
-                                  float beta) {
+                                  float beta, const float *bias, int bias_kind, int act) {
     const int64_t per_item = M * N, total = per_item * batch;
+    const bool ep = bias_kind != SGEMM_BIAS_NONE || act != SGEMM_ACT_NONE;
     for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < total;
          e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const int64_t item = e / per_item, r = e % per_item;
-        float *p = C + item * strideC + (r / N) * ldc + r % N;
-        *p = beta != 0.0f ? beta * *p : 0.0f;
+        const int64_t row = r / N, col = r % N;
+        float *p = C + item * strideC + row * ldc + col;
+        const float x = beta != 0.0f ? beta * *p : 0.0f;
+        *p = ep ? epilogue_value(x, bias, bias_kind, act, row, col) : x;
     }
 }
 
@@ -121,23 +133,31 @@ int ffma_launch(const Problem &p, const DeviceInfo &dev, int tile, int sk_mode, 
     }
 }
 
-int scale_tiles_launch(float *C, int64_t M, int64_t N, int64_t ldc, int64_t strideC, float beta, int bm, int bn,
-                       int tiles_n, int tiles_per_item, int first_tile, int count, cudaStream_t stream,
-                       int *launches) {
+int split_tiles_prepare(const Problem &p, int bm, int bn, int tiles_n, int tiles_per_item, int first_tile,
+                        int count, cudaStream_t stream, int *launches) {
     if (count <= 0) return SGEMM_OK;
     const dim3 grid(static_cast<unsigned>((bm + 7) / 8), static_cast<unsigned>(count));
-    scale_tiles_kernel<<<grid, 256, 0, stream>>>(C, M, N, ldc, strideC, beta, bm, bn, tiles_n, tiles_per_item,
-                                                  first_tile);
+    tile_pass_kernel<<<grid, 256, 0, stream>>>(p.C, p.M, p.N, p.ldc, p.strideC, p.beta, p.bias, p.bias_kind,
+                                                SGEMM_ACT_NONE, bm, bn, tiles_n, tiles_per_item, first_tile);
     ++*launches;
     return cudaGetLastError() == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
 }
 
-int scale_launch(float *C, int64_t M, int64_t N, int64_t ldc, int64_t strideC, int64_t batch, float beta,
-                 const DeviceInfo &dev, cudaStream_t stream, int *launches) {
-    const int64_t total = M * N * batch;
+int split_tiles_finish(const Problem &p, int bm, int bn, int tiles_n, int tiles_per_item, int first_tile,
+                       int count, cudaStream_t stream, int *launches) {
+    if (count <= 0 || p.act == SGEMM_ACT_NONE) return SGEMM_OK;
+    const dim3 grid(static_cast<unsigned>((bm + 7) / 8), static_cast<unsigned>(count));
+    tile_pass_kernel<<<grid, 256, 0, stream>>>(p.C, p.M, p.N, p.ldc, p.strideC, 1.0f, nullptr, SGEMM_BIAS_NONE,
+                                                p.act, bm, bn, tiles_n, tiles_per_item, first_tile);
+    ++*launches;
+    return cudaGetLastError() == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
+}
+
+int scale_launch(const Problem &p, const DeviceInfo &dev, cudaStream_t stream, int *launches) {
+    const int64_t total = p.M * p.N * p.batch;
     const int64_t blocks = min64(ceil_div(total, 256), static_cast<int64_t>(dev.sm_count) * 8);
-    scale_rect_kernel<<<static_cast<int>(blocks > 1 ? blocks : 1), 256, 0, stream>>>(C, M, N, ldc, strideC, batch,
-                                                                                     beta);
+    scale_rect_kernel<<<static_cast<int>(blocks > 1 ? blocks : 1), 256, 0, stream>>>(
+        p.C, p.M, p.N, p.ldc, p.strideC, p.batch, p.beta, p.bias, p.bias_kind, p.act);
     ++*launches;
     return cudaGetLastError() == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
 }

@@ -23,6 +23,12 @@ struct Problem {
     float alpha = 1.0f, beta = 0.0f;
     // Strided batch: item b uses A + b*strideA, B + b*strideB, C + b*strideC.
     int64_t batch = 1, strideA = 0, strideB = 0, strideC = 0;
+    // Fused epilogue: C = act(alpha * op(A) op(B) + beta * C + bias), with
+    // bias_kind / act the sgemm_bias / sgemm_activation values of sgemm.h
+    // (the bias is shared by all items of a batch).
+    const float *bias = nullptr;
+    int bias_kind = 0, act = 0;
+    bool has_epilogue() const { return bias_kind != 0 || act != 0; }
 };
 
 // Properties of the current device that the launchers need.
@@ -43,8 +49,8 @@ enum StreamKMode { SK_AUTO = 0, SK_DP_ONLY = 1, SK_HYBRID = 2, SK_ALL = 3 };
 // Work split of a persistent grid over a tiles x k_steps iteration space:
 // tiles [0, dp_tiles) go whole, round-robin over the CTAs; the rest are split
 // along K into sk_iters (tile, k-step) iterations shared evenly by CTAs
-// [0, sk_ctas) (stream-K). A split tile's outputs are zeroed first and its
-// partial sums added with atomics.
+// [0, sk_ctas) (stream-K). A split tile's outputs are set to beta * C (plus
+// the bias) first and its partial sums added with atomics.
 struct Schedule {
     int dp_tiles;
     int sk_ctas;
@@ -88,13 +94,16 @@ inline Schedule make_schedule(int tiles, int64_t k_steps, int slots, int mode, i
     return s;
 }
 
-// Enqueue a kernel that sets C = beta * C (C = 0 when beta = 0, without
-// reading C) over `count` tiles starting at tile `first_tile` of a bm x bn
-// tile grid with tiles_n tiles per row and tiles_per_item tiles per batch
-// item (items strideC elements apart).
-int scale_tiles_launch(float *C, int64_t M, int64_t N, int64_t ldc, int64_t strideC, float beta, int bm, int bn,
-                       int tiles_n, int tiles_per_item, int first_tile, int count, cudaStream_t stream,
-                       int *launches);
+// Passes over the tiles that a schedule splits along K: `count` tiles from
+// tile `first_tile` of a bm x bn tile grid with tiles_n tiles per row and
+// tiles_per_item tiles per batch item. The prepare pass runs before the
+// product and sets C = beta * C + bias (C is not read when beta = 0), so the
+// product can add its partial sums with atomics; the finish pass runs after
+// it and applies the activation (it enqueues nothing when p.act is NONE).
+int split_tiles_prepare(const Problem &p, int bm, int bn, int tiles_n, int tiles_per_item, int first_tile,
+                        int count, cudaStream_t stream, int *launches);
+int split_tiles_finish(const Problem &p, int bm, int bn, int tiles_n, int tiles_per_item, int first_tile,
+                       int count, cudaStream_t stream, int *launches);
 
 // Enqueue the FFMA product. `launches` receives the number of kernels enqueued.
 int ffma_launch(const Problem &p, const DeviceInfo &dev, int tile, int sk_mode, cudaStream_t stream,
@@ -103,10 +112,9 @@ int ffma_launch(const Problem &p, const DeviceInfo &dev, int tile, int sk_mode, 
 int ffma_launch_t(const Problem &p, const DeviceInfo &dev, int tile, int sk_mode, cudaStream_t stream,
                   int *launches);
 
-// Enqueue C[0:M, 0:N] = beta * C (0 when beta = 0): the result when K = 0
-// (the empty sum) or alpha = 0.
-int scale_launch(float *C, int64_t M, int64_t N, int64_t ldc, int64_t strideC, int64_t batch, float beta,
-                 const DeviceInfo &dev, cudaStream_t stream, int *launches);
+// Enqueue C[0:M, 0:N] = act(beta * C + bias) for every item (C not read
+// when beta = 0): the result when K = 0 (the empty sum) or alpha = 0.
+int scale_launch(const Problem &p, const DeviceInfo &dev, cudaStream_t stream, int *launches);
 
 // Tensor-core three-term TF32 variant. Returns SGEMM_ERR_UNSUPPORTED when it
 // cannot run the request.

@@ -49,6 +49,7 @@
 #include <atomic>
 #include <mutex>
 
+#include "epilogue.cuh"
 #include "sgemm.h"
 #include "sgemm_internal.h"
 
@@ -104,6 +105,9 @@ struct Args {
     int64_t strideA = 0, strideB = 0, strideC = 0;
     int tiles_per_item = 1;
     int a_shared = 0, b_shared = 0;
+    // Fused epilogue on whole tiles: C = act(alpha * acc + beta * C + bias).
+    const float *bias = nullptr;
+    int bias_kind = 0, act = 0, ep = 0;
 };
 
 // Item and top-left corner of tile `tile` of the item-major tile order.
@@ -357,8 +361,9 @@ __device__ __forceinline__ void red_add_v4(float *p, float a, float b, float c, 
 }
 
 // Writes 32 accumulator values (columns col0 .. col0 + 31 of one row of C):
-// C = alpha * v + beta * C (C read only when beta != 0), or, for a tile split
-// along K (C already scaled by beta), C += alpha * v with atomics.
+// C = act(alpha * v + beta * C + bias) (C read only when beta != 0), or, for
+// a tile split along K (C already holds beta * C + bias; the activation
+// follows in a later pass), C += alpha * v with atomics.
 template <bool VEC_C>
 __device__ __forceinline__ void store_chunk(const Args &a, float *crow, int64_t row, int64_t col0, const float (&v)[32],
                                             bool atomic) {
@@ -373,6 +378,34 @@ __device__ __forceinline__ void store_chunk(const Args &a, float *crow, int64_t 
 #pragma unroll
             for (int j = 0; j < 32; ++j)
                 if (col0 + j < a.N) atomicAdd(crow + col0 + j, alpha * v[j]);
+        }
+    } else if (a.ep) {
+#pragma unroll
+        for (int j = 0; j < 32; j += 4) {
+            const int64_t col = col0 + j;
+            float o[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) o[q] = alpha * v[j + q];
+            if (VEC_C && col + 3 < a.N) {
+                float4 *p = reinterpret_cast<float4 *>(crow + col);
+                if (beta != 0.0f) {
+                    const float4 c = *p;
+                    o[0] = fmaf(beta, c.x, o[0]);
+                    o[1] = fmaf(beta, c.y, o[1]);
+                    o[2] = fmaf(beta, c.z, o[2]);
+                    o[3] = fmaf(beta, c.w, o[3]);
+                }
+#pragma unroll
+                for (int q = 0; q < 4; ++q) o[q] = epilogue_value(o[q], a.bias, a.bias_kind, a.act, row, col + q);
+                *p = make_float4(o[0], o[1], o[2], o[3]);
+            } else {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    if (col + q >= a.N) continue;
+                    const float x = beta != 0.0f ? fmaf(beta, crow[col + q], o[q]) : o[q];
+                    crow[col + q] = epilogue_value(x, a.bias, a.bias_kind, a.act, row, col + q);
+                }
+            }
         }
     } else if (VEC_C && col0 + 31 < a.N) {
 #pragma unroll
@@ -649,7 +682,7 @@ __global__ void __launch_bounds__(THREADS, 1) tf32x3_kernel(const Args a) {
             const TileAt at = tile_at(a, tile);
             const int64_t m0 = at.m0, n0 = at.n0;
             const int64_t row = m0 + q * 32 + lane;
-            // Stream-K tiles were scaled by beta beforehand: every unit adds.
+            // Stream-K tiles hold beta * C + bias already: every unit adds.
             const bool atomic = tile >= a.dp_tiles;
             float *crow = a.C + at.item * a.strideC + row * a.ldc;
 #pragma unroll 1
@@ -901,7 +934,7 @@ __global__ void __launch_bounds__(tma::THREADS, 1)
             const TileAt at = tile_at(a, tile);
             const int64_t m0 = at.m0, n0 = at.n0;
             const int64_t row = m0 + q * 32 + lane;
-            // Stream-K tiles were scaled by beta beforehand: every unit adds.
+            // Stream-K tiles hold beta * C + bias already: every unit adds.
             const bool atomic = tile >= a.dp_tiles;
             float *crow = a.C + at.item * a.strideC + row * a.ldc;
 #pragma unroll 1
@@ -1168,7 +1201,7 @@ __global__ void __launch_bounds__(tm3::THREADS, 1)
             const TileAt at = tile_at(a, tile);
             const int64_t m0 = at.m0, n0 = at.n0;
             const int64_t row = m0 + q * 32 + lane;
-            // Stream-K tiles were scaled by beta beforehand: every unit adds.
+            // Stream-K tiles hold beta * C + bias already: every unit adds.
             const bool atomic = tile >= a.dp_tiles;
             float *crow = a.C + at.item * a.strideC + row * a.ldc;
 #pragma unroll 1
@@ -1240,12 +1273,10 @@ int launch(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStream_t st
     // One CTA per SM (the stage ring takes most of shared memory). A stream-K
     // share below 4 k-blocks costs more in fix-up than it saves.
     const Schedule sch = make_schedule(tiles, k_blocks, dev.sm_count, sk_mode, 4, 0.25);
-    if (tiles > sch.dp_tiles) {
-        int rc = scale_tiles_launch(p.C, p.M, p.N, p.ldc, p.strideC, p.beta, BM, BN, static_cast<int>(tiles_n),
-                                    static_cast<int>(tiles_m * tiles_n), sch.dp_tiles, tiles - sch.dp_tiles,
-                                    stream, launches);
-        if (rc != SGEMM_OK) return rc;
-    }
+    const int split = tiles - sch.dp_tiles;
+    int rc = split_tiles_prepare(p, BM, BN, static_cast<int>(tiles_n), static_cast<int>(tiles_m * tiles_n),
+                                 sch.dp_tiles, split, stream, launches);
+    if (rc != SGEMM_OK) return rc;
     Args a;
     a.M = p.M;
     a.N = p.N;
@@ -1271,9 +1302,15 @@ int launch(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStream_t st
     a.tiles_per_item = static_cast<int>(tiles_m * tiles_n);
     a.a_shared = p.strideA == 0;
     a.b_shared = p.strideB == 0;
+    a.bias = p.bias;
+    a.bias_kind = p.bias_kind;
+    a.act = p.act;
+    a.ep = p.has_epilogue();
     kernel<<<sch.grid, THREADS, SMEM_BYTES, stream>>>(a);
     ++*launches;
-    return cudaGetLastError() == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
+    if (cudaGetLastError() != cudaSuccess) return SGEMM_ERR_LAUNCH;
+    return split_tiles_finish(p, BM, BN, static_cast<int>(tiles_n), static_cast<int>(tiles_m * tiles_n),
+                              sch.dp_tiles, split, stream, launches);
 }
 
 
@@ -1359,12 +1396,10 @@ int launch_tma(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStream_
     if (tiles_m * tiles_n * p.batch > INT32_MAX / 2) return SGEMM_ERR_UNSUPPORTED;
     const int tiles = static_cast<int>(tiles_m * tiles_n * p.batch);
     const Schedule sch = make_schedule(tiles, k_blocks, dev.sm_count, sk_mode, 4, 0.25);
-    if (tiles > sch.dp_tiles) {
-        int rc = scale_tiles_launch(p.C, p.M, p.N, p.ldc, p.strideC, p.beta, BM, BN, static_cast<int>(tiles_n),
-                                    static_cast<int>(tiles_m * tiles_n), sch.dp_tiles, tiles - sch.dp_tiles,
-                                    stream, launches);
-        if (rc != SGEMM_OK) return rc;
-    }
+    const int split = tiles - sch.dp_tiles;
+    int rc = split_tiles_prepare(p, BM, BN, static_cast<int>(tiles_n), static_cast<int>(tiles_m * tiles_n),
+                                 sch.dp_tiles, split, stream, launches);
+    if (rc != SGEMM_OK) return rc;
     Args a{};
     a.M = p.M;
     a.N = p.N;
@@ -1386,9 +1421,15 @@ int launch_tma(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStream_
     a.tiles_per_item = static_cast<int>(tiles_m * tiles_n);
     a.a_shared = p.strideA == 0;
     a.b_shared = p.strideB == 0;
+    a.bias = p.bias;
+    a.bias_kind = p.bias_kind;
+    a.act = p.act;
+    a.ep = p.has_epilogue();
     kernel<<<sch.grid, threads, smem, stream>>>(mapA, mapB, a);
     ++*launches;
-    return cudaGetLastError() == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
+    if (cudaGetLastError() != cudaSuccess) return SGEMM_ERR_LAUNCH;
+    return split_tiles_finish(p, BM, BN, static_cast<int>(tiles_n), static_cast<int>(tiles_m * tiles_n),
+                              sch.dp_tiles, split, stream, launches);
 }
 
 }  // namespace

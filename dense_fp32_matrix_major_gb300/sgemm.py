@@ -28,6 +28,20 @@ SGEMM_AUTO = 0
 SGEMM_FFMA = 1
 SGEMM_TF32X3 = 2
 
+SGEMM_BIAS_NONE = 0
+SGEMM_BIAS_PER_COL = 1
+SGEMM_BIAS_PER_ROW = 2
+
+SGEMM_ACT_NONE = 0
+SGEMM_ACT_RELU = 1
+SGEMM_ACT_GELU = 2
+SGEMM_ACT_SILU = 3
+
+BIAS_KINDS = {None: SGEMM_BIAS_NONE, "none": SGEMM_BIAS_NONE, "col": SGEMM_BIAS_PER_COL,
+              "row": SGEMM_BIAS_PER_ROW}
+ACTIVATIONS = {None: SGEMM_ACT_NONE, "none": SGEMM_ACT_NONE, "relu": SGEMM_ACT_RELU, "gelu": SGEMM_ACT_GELU,
+               "silu": SGEMM_ACT_SILU}
+
 SGEMM_TUNE_FFMA_TILE = 1
 SGEMM_TUNE_STREAM_K = 2
 SGEMM_TUNE_WATCHDOG_MS = 3
@@ -41,6 +55,8 @@ SIGNATURES = {
                             ctypes.c_float, _vp, _i64, _vp]),
     "sgemm_f32_batched": (_int, [_int, _int, _i64, _i64, _i64, ctypes.c_float, _vp, _i64, _i64, _vp, _i64,
                                  _i64, ctypes.c_float, _vp, _i64, _i64, _i64, _vp]),
+    "sgemm_f32_fused": (_int, [_int, _int, _i64, _i64, _i64, ctypes.c_float, _vp, _i64, _vp, _i64,
+                               ctypes.c_float, _vp, _i64, _vp, _int, _int, _vp]),
     "sgemm_f32_from_host": (_int, [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _vp, _vp, _vp, _vp]),
     "sgemm_set_variant": (_int, [_int]),
     "sgemm_get_variant": (_int, []),
@@ -211,6 +227,47 @@ def gemm(A, B, C=None, *, transA=False, transB=False, alpha=1.0, beta=0.0, strea
                           B.data_ptr(), ldb, float(beta), C.data_ptr(), ldc, _stream_handle(stream))
     if rc:
         raise SgemmError(rc, "sgemm_f32_ex")
+    return C
+
+
+def gemm_fused(A, B, C=None, *, bias=None, bias_kind=None, act=None, transA=False, transB=False, alpha=1.0,
+               beta=0.0, stream=None):
+    """C = act(alpha * op(A) @ op(B) + beta * C + bias) for row-major float32 CUDA tensors.
+
+    Operands as in :func:`gemm`. ``bias`` is a contiguous float32 CUDA
+    vector: N values for ``bias_kind="col"`` (one per column of C) or M
+    values for ``bias_kind="row"``. ``act`` is None, "relu", "gelu" or
+    "silu". Integer codes from sgemm.h are accepted for both.
+    """
+    import torch
+
+    kind = bias_kind if isinstance(bias_kind, int) else BIAS_KINDS[bias_kind]
+    code = act if isinstance(act, int) else ACTIVATIONS[act]
+    lda = _rowmajor_2d(A, "A")
+    ldb = _rowmajor_2d(B, "B")
+    M, K = (A.shape[1], A.shape[0]) if transA else tuple(A.shape)
+    K2, N = (B.shape[1], B.shape[0]) if transB else tuple(B.shape)
+    if K != K2:
+        raise ValueError(f"inner dimensions differ: {K} vs {K2}")
+    if C is None:
+        if beta != 0.0:
+            raise ValueError("beta != 0 needs C")
+        C = torch.empty((M, N), dtype=torch.float32, device=A.device)
+    ldc = _rowmajor_2d(C, "C")
+    if tuple(C.shape) != (M, N):
+        raise ValueError("C has the wrong shape")
+    bias_ptr = 0
+    if kind != SGEMM_BIAS_NONE:
+        if bias is None or bias.dtype != torch.float32 or not bias.is_cuda or not bias.is_contiguous():
+            raise TypeError("bias must be a contiguous float32 CUDA tensor")
+        if bias.numel() != (N if kind == SGEMM_BIAS_PER_COL else M):
+            raise ValueError("bias length must be N (per column) or M (per row)")
+        bias_ptr = bias.data_ptr()
+    rc = lib.sgemm_f32_fused(int(transA), int(transB), M, N, K, float(alpha), A.data_ptr(), lda,
+                             B.data_ptr(), ldb, float(beta), C.data_ptr(), ldc, bias_ptr, kind, code,
+                             _stream_handle(stream))
+    if rc:
+        raise SgemmError(rc, "sgemm_f32_fused")
     return C
 
 

@@ -126,6 +126,49 @@ int sgemm_f32_batched(int transA, int transB, int64_t M, int64_t N, int64_t K, f
                       int64_t lda, int64_t strideA, const float *B, int64_t ldb, int64_t strideB, float beta,
                       float *C, int64_t ldc, int64_t strideC, int64_t batch, sgemm_stream_t stream);
 
+/* Bias forms of the fused epilogue (sgemm_f32_fused). */
+enum sgemm_bias {
+    SGEMM_BIAS_NONE = 0,    /* no bias; `bias` is not read */
+    SGEMM_BIAS_PER_COL = 1, /* N values: bias[j] is added to every element of column j */
+    SGEMM_BIAS_PER_ROW = 2  /* M values: bias[i] is added to every element of row i */
+};
+
+/* Activations of the fused epilogue, applied to each element x. */
+enum sgemm_activation {
+    SGEMM_ACT_NONE = 0,
+    SGEMM_ACT_RELU = 1, /* x < 0 ? 0 : x (NaN stays NaN) */
+    SGEMM_ACT_GELU = 2, /* x * Phi(x) = x / 2 * (1 + erf(x / sqrt(2))), Phi the standard normal CDF */
+    SGEMM_ACT_SILU = 3  /* x / (1 + exp(-x)) */
+};
+
+/*
+ * Product with a fused epilogue:
+ *     C = act(alpha * op(A) * op(B) + beta * C + bias)
+ * The source pages compute the product alone and motivate it as the core
+ * operation of neural-network layers ("CUDA内存优化入门：从Naive到Tiled矩阵
+ * 乘法", section 一); a layer's forward pass is this product followed by a
+ * bias and an activation, and fusing them saves the extra pass over C.
+ *   transA .. ldc   as sgemm_f32_ex.
+ *   bias            device pointer, read only: N floats (SGEMM_BIAS_PER_COL)
+ *                   or M floats (SGEMM_BIAS_PER_ROW), contiguous, any
+ *                   alignment, not overlapping C; ignored for SGEMM_BIAS_NONE.
+ *   bias_kind       an sgemm_bias value.
+ *   activation      an sgemm_activation value.
+ * The bias is added and the activation applied to the fp32 value
+ * alpha * acc + beta * C, once per element, in the kernel that writes C.
+ * Tiles split along K (stream-K) take the bias in the pre-pass that scales C
+ * by beta, and the activation in one more small launch over those tiles
+ * after the product. Accuracy: the error scale becomes |alpha| sum_k |op(A)|
+ * |op(B)| + |beta| |C| + |bias|; the activations are at most 1.13-Lipschitz
+ * (GELU), so the product's bound carries over up to that factor plus a few
+ * fp32 roundings of the activation itself. Same errors as sgemm_f32_ex, plus
+ * SGEMM_ERR_INVALID_ARG for an unknown bias_kind or activation, a null bias
+ * with a bias kind other than NONE, or a bias overlapping C.
+ */
+int sgemm_f32_fused(int transA, int transB, int64_t M, int64_t N, int64_t K, float alpha, const float *A,
+                    int64_t lda, const float *B, int64_t ldb, float beta, float *C, int64_t ldc,
+                    const float *bias, int bias_kind, int activation, sgemm_stream_t stream);
+
 /*
  * C = A * B for matrices that live in HOST memory, through caller-owned
  * device buffers. Enqueues, on `stream`: the copy of A_host into dA and of

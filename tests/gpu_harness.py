@@ -106,6 +106,39 @@ def run_gemm_ex(A: np.ndarray, B: np.ndarray, *, transA=False, transB=False, alp
     return box, flat, rc
 
 
+def run_fused(A: np.ndarray, B: np.ndarray, *, bias=None, bias_kind=0, act=0, transA=False, transB=False,
+              alpha=1.0, beta=0.0, C_init=None, lda=None, ldb=None, ldc=None, offsets=(0, 0, 0),
+              bias_offset=0):
+    """sgemm_f32_fused on numpy inputs in STORED form; the bias vector sits
+    ``bias_offset`` floats into its own guarded buffer. Returns (C, flat C
+    buffer, status)."""
+    import torch
+    from dense_fp32_matrix_major_gb300 import sgemm
+
+    M = A.shape[1] if transA else A.shape[0]
+    K = A.shape[0] if transA else A.shape[1]
+    N = B.shape[0] if transB else B.shape[1]
+    lda = max(A.shape[1], 1) if lda is None else lda
+    ldb = max(B.shape[1], 1) if ldb is None else ldb
+    ldc = max(N, 1) if ldc is None else ldc
+    fa, vA = device_matrix(A, lda, offsets[0])
+    fb, vB = device_matrix(B, ldb, offsets[1])
+    cvals = np.full((M, N), np.nan, dtype=np.float32) if C_init is None else C_init
+    fc, vC = device_matrix(cvals, ldc, offsets[2])
+    bias_ptr = 0
+    if bias is not None:
+        fbias, vbias = device_matrix(np.asarray(bias, np.float32).reshape(1, -1), None, bias_offset, fill=np.nan)
+        bias_ptr = vbias.data_ptr()
+    stream = torch.cuda.current_stream()
+    rc = sgemm.lib.sgemm_f32_fused(int(transA), int(transB), M, N, K, float(alpha), vA.data_ptr(), lda,
+                                   vB.data_ptr(), ldb, float(beta), vC.data_ptr(), ldc, bias_ptr, int(bias_kind),
+                                   int(act), stream.cuda_stream)
+    torch.cuda.synchronize()
+    flat = fc.cpu().numpy()
+    box = vC.cpu().numpy() if M and N else np.zeros((M, N), np.float32)
+    return box, flat, rc
+
+
 def run_batched(As, Bs, *, transA=False, transB=False, alpha=1.0, beta=0.0, C0=None,
                 strideA=None, strideB=None, strideC=None, share_a=False, share_b=False):
     """sgemm_f32_batched on lists of stored-form items (dense rows). Items sit
