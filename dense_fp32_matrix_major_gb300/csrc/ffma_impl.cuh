@@ -269,31 +269,37 @@ __device__ __forceinline__ void process_tile(const FfmaArgs &a, float *As, float
     cp_async_wait<0>();
 
     // Epilogue: rows wm0 + g*32 + tm*4 + r, columns wn0 + c*16 + tn*4 + q.
+    // Everything the stores need, read from the parameters before the first
+    // store (a store through a generic pointer would force re-reads).
     const float alpha = a.alpha, beta = a.beta;
     const bool vec_c = VEC_C || a.vec_c;
+    const int64_t M = a.M, N = a.N, ldc = a.ldc;
+    const float *bias = a.bias;
+    const int bias_kind = a.bias_kind, act = a.act;
+    const bool ep = a.ep;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const int64_t row = m0 + wm0 + (i >> 2) * 32 + tm * 4 + (i & 3);
-        if (row >= a.M) continue;
-        float *crow = Cb + row * a.ldc;
+        if (row >= M) continue;
+        float *crow = Cb + row * ldc;
 #pragma unroll
         for (int c = 0; c < C::CN; ++c) {
             const int64_t col = n0 + wn0 + c * 16 + tn * 4;
-            if (col >= a.N) continue;
+            if (col >= N) continue;
             float v[4];
 #pragma unroll
             for (int q = 0; q < 4; ++q) v[q] = alpha * acc[i][c * 4 + q];
             if (atomic) {
-                if (vec_c && col + 3 < a.N) {
+                if (vec_c && col + 3 < N) {
                     asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(crow + col), "f"(v[0]),
                                  "f"(v[1]), "f"(v[2]), "f"(v[3])
                                  : "memory");
                 } else {
 #pragma unroll
                     for (int q = 0; q < 4; ++q)
-                        if (col + q < a.N) atomicAdd(crow + col + q, v[q]);
+                        if (col + q < N) atomicAdd(crow + col + q, v[q]);
                 }
-            } else if (vec_c && col + 3 < a.N) {
+            } else if (vec_c && col + 3 < N) {
                 float4 *p = reinterpret_cast<float4 *>(crow + col);
                 if (beta != 0.0f) {
                     const float4 o = *p;
@@ -302,17 +308,17 @@ __device__ __forceinline__ void process_tile(const FfmaArgs &a, float *As, float
                     v[2] = fmaf(beta, o.z, v[2]);
                     v[3] = fmaf(beta, o.w, v[3]);
                 }
-                if (a.ep) {
+                if (ep) {
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) v[q] = epilogue_value(v[q], a.bias, a.bias_kind, a.act, row, col + q);
+                    for (int q = 0; q < 4; ++q) v[q] = epilogue_value(v[q], bias, bias_kind, act, row, col + q);
                 }
                 *p = make_float4(v[0], v[1], v[2], v[3]);
             } else {
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
-                    if (col + q >= a.N) continue;
+                    if (col + q >= N) continue;
                     float x = beta != 0.0f ? fmaf(beta, crow[col + q], v[q]) : v[q];
-                    if (a.ep) x = epilogue_value(x, a.bias, a.bias_kind, a.act, row, col + q);
+                    if (ep) x = epilogue_value(x, bias, bias_kind, act, row, col + q);
                     crow[col + q] = x;
                 }
             }

@@ -314,6 +314,25 @@ __device__ __forceinline__ void tmem_load32(uint32_t taddr, float (&v)[32]) {
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 16 consecutive accumulator columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_load16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                   "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                   "+r"(r[15])
+                 :
+                 : "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
 __device__ __forceinline__ uint32_t tf32_rna_bits(float x) {
     uint32_t r;
     asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
@@ -360,54 +379,98 @@ __device__ __forceinline__ void red_add_v4(float *p, float a, float b, float c, 
                  : "memory");
 }
 
+// Fused epilogue for 16 values of one row: C[col0 + j] = ACT(alpha * v[j] +
+// beta * C[col0 + j] + bias_j) for the columns below N (C read only when
+// beta != 0), stores only when `valid` (row < M). The bias of column j is
+// bl (per row or absent) or, per column, lane (base + j)'s value of bl (the
+// warp loaded bias[chunk column + lane] in one coalesced load): the whole
+// warp runs the shuffles, so no lane may have left before.
+template <bool VEC_C, int ACT>
+__device__ __forceinline__ void store16_ep(float *crow, bool valid, int64_t col0, int base, int64_t N, float alpha,
+                                           float beta, bool col_bias, float bl, const float (&v)[16]) {
+    if (VEC_C && col0 + 15 < N) {
+#pragma unroll
+        for (int j = 0; j < 16; j += 4) {
+            float4 bb = make_float4(bl, bl, bl, bl);
+            if (col_bias) {
+                bb.x = __shfl_sync(0xffffffffu, bl, base + j);
+                bb.y = __shfl_sync(0xffffffffu, bl, base + j + 1);
+                bb.z = __shfl_sync(0xffffffffu, bl, base + j + 2);
+                bb.w = __shfl_sync(0xffffffffu, bl, base + j + 3);
+            }
+            if (!valid) continue;
+            float4 *p = reinterpret_cast<float4 *>(crow + col0 + j);
+            float4 o = make_float4(alpha * v[j], alpha * v[j + 1], alpha * v[j + 2], alpha * v[j + 3]);
+            if (beta != 0.0f) {
+                const float4 c = *p;
+                o.x = fmaf(beta, c.x, o.x);
+                o.y = fmaf(beta, c.y, o.y);
+                o.z = fmaf(beta, c.z, o.z);
+                o.w = fmaf(beta, c.w, o.w);
+            }
+            o.x = activate(o.x + bb.x, ACT);
+            o.y = activate(o.y + bb.y, ACT);
+            o.z = activate(o.z + bb.z, ACT);
+            o.w = activate(o.w + bb.w, ACT);
+            *p = o;
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const float b = col_bias ? __shfl_sync(0xffffffffu, bl, base + j) : bl;
+            if (!valid || col0 + j >= N) continue;
+            float x = alpha * v[j];
+            if (beta != 0.0f) x = fmaf(beta, crow[col0 + j], x);
+            crow[col0 + j] = activate(x + b, ACT);
+        }
+    }
+}
+
+// The 16 columns col0 .. col0 + 15 (= chunk column base .. base + 15) of one
+// row; called by all 32 lanes of the warp (see store16_ep).
+template <bool VEC_C>
+__device__ __forceinline__ void store16_fused(const Args &a, float *crow, int64_t row, int64_t col0, int base,
+                                              float bl, const float (&v)[16]) {
+    const int64_t N = a.N;
+    if (col0 >= N) return;  // uniform over the warp
+    const bool valid = row < a.M;
+    const float alpha = a.alpha, beta = a.beta;
+    const bool cb = a.bias_kind == SGEMM_BIAS_PER_COL;
+    switch (a.act) {
+        case SGEMM_ACT_RELU:
+            store16_ep<VEC_C, SGEMM_ACT_RELU>(crow, valid, col0, base, N, alpha, beta, cb, bl, v);
+            break;
+        case SGEMM_ACT_GELU:
+            store16_ep<VEC_C, SGEMM_ACT_GELU>(crow, valid, col0, base, N, alpha, beta, cb, bl, v);
+            break;
+        case SGEMM_ACT_SILU:
+            store16_ep<VEC_C, SGEMM_ACT_SILU>(crow, valid, col0, base, N, alpha, beta, cb, bl, v);
+            break;
+        default: store16_ep<VEC_C, SGEMM_ACT_NONE>(crow, valid, col0, base, N, alpha, beta, cb, bl, v); break;
+    }
+}
+
 // Writes 32 accumulator values (columns col0 .. col0 + 31 of one row of C):
-// C = act(alpha * v + beta * C + bias) (C read only when beta != 0), or, for
-// a tile split along K (C already holds beta * C + bias; the activation
-// follows in a later pass), C += alpha * v with atomics.
+// C = alpha * v + beta * C (C read only when beta != 0), or, for a tile split
+// along K (C already holds beta * C + bias; the activation follows in a
+// later pass), C += alpha * v with atomics.
 template <bool VEC_C>
 __device__ __forceinline__ void store_chunk(const Args &a, float *crow, int64_t row, int64_t col0, const float (&v)[32],
                                             bool atomic) {
-    if (row >= a.M || col0 >= a.N) return;
+    const int64_t N = a.N;
+    if (row >= a.M || col0 >= N) return;
     const float alpha = a.alpha, beta = a.beta;
     if (atomic) {
-        if (VEC_C && col0 + 31 < a.N) {
+        if (VEC_C && col0 + 31 < N) {
 #pragma unroll
             for (int j = 0; j < 32; j += 4)
                 red_add_v4(crow + col0 + j, alpha * v[j], alpha * v[j + 1], alpha * v[j + 2], alpha * v[j + 3]);
         } else {
 #pragma unroll
             for (int j = 0; j < 32; ++j)
-                if (col0 + j < a.N) atomicAdd(crow + col0 + j, alpha * v[j]);
+                if (col0 + j < N) atomicAdd(crow + col0 + j, alpha * v[j]);
         }
-    } else if (a.ep) {
-#pragma unroll
-        for (int j = 0; j < 32; j += 4) {
-            const int64_t col = col0 + j;
-            float o[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) o[q] = alpha * v[j + q];
-            if (VEC_C && col + 3 < a.N) {
-                float4 *p = reinterpret_cast<float4 *>(crow + col);
-                if (beta != 0.0f) {
-                    const float4 c = *p;
-                    o[0] = fmaf(beta, c.x, o[0]);
-                    o[1] = fmaf(beta, c.y, o[1]);
-                    o[2] = fmaf(beta, c.z, o[2]);
-                    o[3] = fmaf(beta, c.w, o[3]);
-                }
-#pragma unroll
-                for (int q = 0; q < 4; ++q) o[q] = epilogue_value(o[q], a.bias, a.bias_kind, a.act, row, col + q);
-                *p = make_float4(o[0], o[1], o[2], o[3]);
-            } else {
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    if (col + q >= a.N) continue;
-                    const float x = beta != 0.0f ? fmaf(beta, crow[col + q], o[q]) : o[q];
-                    crow[col + q] = epilogue_value(x, a.bias, a.bias_kind, a.act, row, col + q);
-                }
-            }
-        }
-    } else if (VEC_C && col0 + 31 < a.N) {
+    } else if (VEC_C && col0 + 31 < N) {
 #pragma unroll
         for (int j = 0; j < 32; j += 4) {
             float4 *p = reinterpret_cast<float4 *>(crow + col0 + j);
@@ -424,8 +487,43 @@ __device__ __forceinline__ void store_chunk(const Args &a, float *crow, int64_t 
     } else {
 #pragma unroll
         for (int j = 0; j < 32; ++j)
-            if (col0 + j < a.N)
-                crow[col0 + j] = beta != 0.0f ? fmaf(beta, crow[col0 + j], alpha * v[j]) : alpha * v[j];
+            if (col0 + j < N) crow[col0 + j] = beta != 0.0f ? fmaf(beta, crow[col0 + j], alpha * v[j]) : alpha * v[j];
+    }
+}
+
+// Epilogue of one 32-column chunk of the accumulator at TMEM address taddr
+// (this thread's lane): loads it and writes C. release: arrive on mbarrier
+// release_bar once the chunk is out of TMEM (the accumulator may be reused).
+// With a fused bias / activation on a whole tile the chunk goes in two
+// 16-column halves, which leaves the activation the registers it needs.
+template <bool VEC_C>
+__device__ __forceinline__ void epilogue_chunk(const Args &a, uint32_t taddr, float *crow, int64_t row, int64_t col0,
+                                               bool atomic, bool release, uint32_t release_bar) {
+    if (a.ep && !atomic) {
+        // Bias of this chunk: lane l holds column col0 + l's value (per
+        // column, one coalesced load issued before the TMEM loads) or the
+        // row's value (per row).
+        const int lane = static_cast<int>(threadIdx.x & 31);
+        float bl = 0.0f;
+        if (a.bias_kind == SGEMM_BIAS_PER_COL && col0 + lane < a.N) bl = __ldg(a.bias + col0 + lane);
+        if (a.bias_kind == SGEMM_BIAS_PER_ROW && row < a.M) bl = __ldg(a.bias + row);
+        float v[16];
+        tmem_load16(taddr, v);
+        store16_fused<VEC_C>(a, crow, row, col0, 0, bl, v);
+        tmem_load16(taddr + 16, v);
+        if (release) {
+            tc_fence_before();
+            mbar_arrive(release_bar);
+        }
+        store16_fused<VEC_C>(a, crow, row, col0 + 16, 16, bl, v);
+    } else {
+        float v[32];
+        tmem_load32(taddr, v);
+        if (release) {
+            tc_fence_before();
+            mbar_arrive(release_bar);
+        }
+        store_chunk<VEC_C>(a, crow, row, col0, v, atomic);
     }
 }
 
@@ -686,12 +784,10 @@ __global__ void __launch_bounds__(THREADS, 1) tf32x3_kernel(const Args a) {
             const bool atomic = tile >= a.dp_tiles;
             float *crow = a.C + at.item * a.strideC + row * a.ldc;
 #pragma unroll 1
-            for (int ch = 0; ch < BN / 32; ++ch) {
-                float v[32];
-                tmem_load32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * BN + ch * 32),
-                            v);
-                store_chunk<VEC_C>(a, crow, row, n0 + ch * 32, v, atomic);
-            }
+            for (int ch = 0; ch < BN / 32; ++ch)
+                epilogue_chunk<VEC_C>(
+                    a, tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * BN + ch * 32),
+                    crow, row, n0 + ch * 32, atomic, false, 0);
             tc_fence_before();
             mbar_arrive(bar(6 + buf));
             ++unit;
@@ -938,12 +1034,10 @@ __global__ void __launch_bounds__(tma::THREADS, 1)
             const bool atomic = tile >= a.dp_tiles;
             float *crow = a.C + at.item * a.strideC + row * a.ldc;
 #pragma unroll 1
-            for (int ch = 0; ch < BN / 32; ++ch) {
-                float v[32];
-                tmem_load32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * BN + ch * 32),
-                            v);
-                store_chunk<VEC_C>(a, crow, row, n0 + ch * 32, v, atomic);
-            }
+            for (int ch = 0; ch < BN / 32; ++ch)
+                epilogue_chunk<VEC_C>(
+                    a, tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * BN + ch * 32),
+                    crow, row, n0 + ch * 32, atomic, false, 0);
             tc_fence_before();
             mbar_arrive(bar(6 + buf));
             ++unit;
@@ -1205,15 +1299,9 @@ __global__ void __launch_bounds__(tm3::THREADS, 1)
             const bool atomic = tile >= a.dp_tiles;
             float *crow = a.C + at.item * a.strideC + row * a.ldc;
 #pragma unroll 1
-            for (int ch = 0; ch < BN / 32; ++ch) {
-                float v[32];
-                tmem_load32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(ch * 32), v);
-                if (ch == BN / 32 - 1) {
-                    tc_fence_before();
-                    mbar_arrive(bar(9));  // accumulator read out: the next unit may start
-                }
-                store_chunk<VEC_C>(a, crow, row, n0 + ch * 32, v, atomic);
-            }
+            for (int ch = 0; ch < BN / 32; ++ch)  // the last chunk frees the accumulator for the next unit
+                epilogue_chunk<VEC_C>(a, tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(ch * 32),
+                                      crow, row, n0 + ch * 32, atomic, ch == BN / 32 - 1, bar(9));
             ++unit;
         });
     }
