@@ -49,9 +49,9 @@
 #include <atomic>
 #include <mutex>
 
-#include "epilogue.cuh"
 #include "sgemm.h"
 #include "sgemm_internal.h"
+#include "tc_common.cuh"
 
 namespace sgemm {
 
@@ -62,492 +62,22 @@ namespace {
 
 std::atomic<int64_t> g_watchdog_ms{2000};
 // Tensor-core kernel for operands that TMA can load: 0 = LDG kernel only,
-// 1 = TMA kernel, 2 = TMA kernel with A in TMEM (fastest; the default).
+// 1 = TMA kernel, 2 = TMA kernel with A in TMEM (the default), 3 = the
+// SM-pair kernel of sgemm_tf32x3_pair.cu (op(A) = A, op(B) = B; the
+// transposed forms keep kernel 2).
 std::atomic<int> g_use_tma{2};
 
-constexpr int BM = 128, BN = 256, BK = 32;  // BK fp32 = 128 bytes = one swizzle row
+using namespace tc;
+
 constexpr int STAGES = 2;
-constexpr int A_TILE = BM * BK * 4;               // bytes of one A tile (hi or lo)
-constexpr int B_TILE = BN * BK * 4;               // bytes of one B tile (hi or lo)
 constexpr int STAGE_BYTES = 2 * A_TILE + 2 * B_TILE;  // A_hi, A_lo, B_hi, B_lo
 constexpr int PRODUCER_WARPS = 8;
-constexpr int EPILOGUE_WARPS = 4;
 constexpr int THREADS = 32 * (1 + PRODUCER_WARPS + EPILOGUE_WARPS);
 constexpr int PRODUCER_THREADS = 32 * PRODUCER_WARPS;
-constexpr int TMEM_COLS = 512;  // two 256-column fp32 accumulators
-constexpr int BAR_BYTES = 128;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + BAR_BYTES + 1024;  // + slack to align to 1024
 constexpr int A_TASKS = BM * (BK / 4);  // 16-byte chunks per A tile
 constexpr int B_TASKS = BN * (BK / 4);
 static_assert(A_TASKS % PRODUCER_THREADS == 0 && B_TASKS % PRODUCER_THREADS == 0, "even producer split");
-
-// Watchdog codes (which wait gave up).
-enum : int { WD_PRODUCER = 1, WD_MMA_FULL = 2, WD_MMA_ACC = 3, WD_EPILOGUE = 4, WD_DRAIN = 5, WD_SELFTEST = 6 };
-
-struct Args {
-    int64_t M, N, K;
-    const float *A;
-    int64_t lda;
-    const float *B;
-    int64_t ldb;
-    float *C;
-    int64_t ldc;
-    int tiles_n, k_blocks, dp_tiles;
-    int sk_ctas;
-    int64_t sk_iters;
-    uint64_t timeout_ns;
-    int *watchdog;
-    float alpha = 1.0f, beta = 0.0f;  // C = alpha * op(A) op(B) + beta * C; beta == 0: C not read
-    // Strided batch: tiles run item-major, tiles_per_item per product; item b
-    // uses A + b*strideA, B + b*strideB, C + b*strideC. In the TMA kernels the
-    // item is the third tensor-map coordinate (0 for an operand shared by all
-    // items, stride 0).
-    int64_t strideA = 0, strideB = 0, strideC = 0;
-    int tiles_per_item = 1;
-    int a_shared = 0, b_shared = 0;
-    // Fused epilogue on whole tiles: C = act(alpha * acc + beta * C + bias).
-    const float *bias = nullptr;
-    int bias_kind = 0, act = 0, ep = 0;
-};
-
-// Item and top-left corner of tile `tile` of the item-major tile order.
-struct TileAt {
-    int item;
-    int64_t m0, n0;
-};
-
-__device__ __forceinline__ TileAt tile_at(const Args &a, int tile) {
-    const int rest = tile % a.tiles_per_item;
-    return TileAt{tile / a.tiles_per_item, static_cast<int64_t>(rest / a.tiles_n) * BM,
-                  static_cast<int64_t>(rest % a.tiles_n) * BN};
-}
-
-// Instruction descriptor of tcgen05.mma kind::tf32: D fp32 (bits 4-5 = 1),
-// A and B tf32 (bits 7-9 and 10-12 = 2), both K-major (bits 15, 16 = 0),
-// N >> 3 in bits 17-22, M >> 4 in bits 24-28.
-constexpr uint32_t kIdesc = (1u << 4) | (2u << 7) | (2u << 10) | (static_cast<uint32_t>(BN >> 3) << 17) |
-                            (static_cast<uint32_t>(BM >> 4) << 24);
-
-// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
-// 128 bytes, 8-row groups 1024 bytes apart. Bits 0-13 start address >> 4,
-// 16-29 leading byte offset >> 4 (unused for this layout), 32-45 stride byte
-// offset >> 4, bit 46 descriptor version 1, bits 61-63 swizzle mode (2 = 128 B).
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
-    return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>(1) << 16) |
-           (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
-           (static_cast<uint64_t>(2) << 61);
-}
-
-__device__ __forceinline__ uint32_t tf32_rna_bits(float x);
-
-__device__ __forceinline__ uint32_t smem_u32(const void *p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ uint64_t global_timer() {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n"
-        " .reg .pred p;\n"
-        " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-        " selp.u32 %0, 1, 0, p;\n"
-        "}\n"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// Wait for the phase with the given parity to complete, within the time
-// limit; false if the limit passed or another role already aborted.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const Args &a, volatile int *abort_flag,
-                                          int code) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = global_timer();
-    for (uint32_t n = 1;; ++n) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((n & 63) == 0) {
-            if (*abort_flag) return false;
-            if (global_timer() - t0 > a.timeout_ns) {
-                *abort_flag = 1;
-                atomicCAS(a.watchdog, 0, code);
-                return false;
-            }
-        }
-    }
-}
-
-__device__ __forceinline__ void fence_proxy_async_smem() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t accumulate) {
-    asm volatile(
-        "{\n"
-        " .reg .pred p;\n"
-        " setp.ne.b32 p, %4, 0;\n"
-        " tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n"
-        "}\n" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(kIdesc), "r"(accumulate)
-        : "memory");
-}
-
-// MMA with the A operand in TMEM (128 lanes = rows, 8 columns = the k-slice).
-__device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t accumulate) {
-    asm volatile(
-        "{\n"
-        " .reg .pred p;\n"
-        " setp.ne.b32 p, %4, 0;\n"
-        " tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n"
-        "}\n" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(kIdesc), "r"(accumulate)
-        : "memory");
-}
-
-// 16 consecutive TMEM columns of this thread's lane.
-__device__ __forceinline__ void tmem_store16(uint32_t taddr, const float (&v)[16]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
-        "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
-        "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
-        "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
-        "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
-        "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
-        "r"(__float_as_uint(v[15]))
-        : "memory");
-}
-
-// 8 consecutive TMEM columns of this thread's lane.
-__device__ __forceinline__ void tmem_store8(uint32_t taddr, const float (&v)[8]) {
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
-                 "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
-                 "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
-                 "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7]))
-                 : "memory");
-}
-
-__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-
-// 3-D tiled TMA load of the box at (x, y, z) (x innermost, in elements; z is
-// the batch item) into shared memory, completing its bytes of transactions
-// on the mbarrier.
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int x, int y, int z,
-                                            uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
-        "[%5];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
-        : "memory");
-}
-
-__device__ __forceinline__ float ld_shared_f32(uint32_t addr) {
-    float v;
-    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-    return v;
-}
-
-__device__ __forceinline__ float4 ld_shared_v4(uint32_t addr) {
-    float4 v;
-    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "r"(addr)
-                 : "memory");
-    return v;
-}
-
-// Low part of a value whose high part the tensor core takes by truncation.
-__device__ __forceinline__ float lo_of(float x) {
-    const float hi = __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
-    return __uint_as_float(tf32_rna_bits(x - hi));
-}
-
-__device__ __forceinline__ void tc_commit(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-                 : "memory");
-}
-
-// 32 consecutive accumulator columns of this thread's lane.
-__device__ __forceinline__ void tmem_load32(uint32_t taddr, float (&v)[32]) {
-    uint32_t r[32];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr));
-    // The registers are valid only after wait::ld; tying them to the wait keeps
-    // every use after it.
-    asm volatile("tcgen05.wait::ld.sync.aligned;"
-                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
-                   "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
-                   "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]),
-                   "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]),
-                   "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
-                 :
-                 : "memory");
-#pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-// 16 consecutive accumulator columns of this thread's TMEM lane.
-__device__ __forceinline__ void tmem_load16(uint32_t taddr, float (&v)[16]) {
-    uint32_t r[16];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;"
-                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
-                   "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
-                   "+r"(r[15])
-                 :
-                 : "memory");
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-__device__ __forceinline__ uint32_t tf32_rna_bits(float x) {
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return r;
-}
-
-// hi + lo split of one value: hi keeps the sign, the exponent and the top 10
-// mantissa bits of x (an exact tf32, so it never overflows), and lo is
-// x - hi (exact in fp32) rounded to tf32. Non-finite x gives a NaN lo, so the
-// products that use it are NaN.
-__device__ __forceinline__ void split_tf32(float x, float &hi, float &lo) {
-    hi = __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
-    lo = __uint_as_float(tf32_rna_bits(x - hi));
-}
-
-__device__ __forceinline__ void split_store(uint32_t hi_addr, uint32_t lo_addr, float a, float b, float c,
-                                            float d);
-
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, float a, float b, float c, float d) {
-    asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
-                 : "memory");
-}
-
-// Split four values and store the high parts at hi_addr, the low parts at lo_addr.
-__device__ __forceinline__ void split_store(uint32_t hi_addr, uint32_t lo_addr, float a, float b, float c,
-                                            float d) {
-    float h0, h1, h2, h3, l0, l1, l2, l3;
-    split_tf32(a, h0, l0);
-    split_tf32(b, h1, l1);
-    split_tf32(c, h2, l2);
-    split_tf32(d, h3, l3);
-    st_shared_v4(hi_addr, h0, h1, h2, h3);
-    st_shared_v4(lo_addr, l0, l1, l2, l3);
-}
-
-// Byte offset of 16-byte chunk `chunk` of row `row` in a 128-byte-swizzled tile.
-__device__ __forceinline__ uint32_t sw128_offset(int row, int chunk) {
-    return static_cast<uint32_t>(row * 128 + ((chunk ^ (row & 7)) << 4));
-}
-
-// Atomic add of four consecutive floats at a 16-byte aligned address.
-__device__ __forceinline__ void red_add_v4(float *p, float a, float b, float c, float d) {
-    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d)
-                 : "memory");
-}
-
-// Fused epilogue for 16 values of one row: C[col0 + j] = ACT(alpha * v[j] +
-// beta * C[col0 + j] + bias_j) for the columns below N (C read only when
-// beta != 0), stores only when `valid` (row < M). The bias of column j is
-// bl (per row or absent) or, per column, lane (base + j)'s value of bl (the
-// warp loaded bias[chunk column + lane] in one coalesced load): the whole
-// warp runs the shuffles, so no lane may have left before.
-template <bool VEC_C, int ACT>
-__device__ __forceinline__ void store16_ep(float *crow, bool valid, int64_t col0, int base, int64_t N, float alpha,
-                                           float beta, bool col_bias, float bl, const float (&v)[16]) {
-    if (VEC_C && col0 + 15 < N) {
-#pragma unroll
-        for (int j = 0; j < 16; j += 4) {
-            float4 bb = make_float4(bl, bl, bl, bl);
-            if (col_bias) {
-                bb.x = __shfl_sync(0xffffffffu, bl, base + j);
-                bb.y = __shfl_sync(0xffffffffu, bl, base + j + 1);
-                bb.z = __shfl_sync(0xffffffffu, bl, base + j + 2);
-                bb.w = __shfl_sync(0xffffffffu, bl, base + j + 3);
-            }
-            if (!valid) continue;
-            float4 *p = reinterpret_cast<float4 *>(crow + col0 + j);
-            float4 o = make_float4(alpha * v[j], alpha * v[j + 1], alpha * v[j + 2], alpha * v[j + 3]);
-            if (beta != 0.0f) {
-                const float4 c = *p;
-                o.x = fmaf(beta, c.x, o.x);
-                o.y = fmaf(beta, c.y, o.y);
-                o.z = fmaf(beta, c.z, o.z);
-                o.w = fmaf(beta, c.w, o.w);
-            }
-            o.x = activate(o.x + bb.x, ACT);
-            o.y = activate(o.y + bb.y, ACT);
-            o.z = activate(o.z + bb.z, ACT);
-            o.w = activate(o.w + bb.w, ACT);
-            *p = o;
-        }
-    } else {
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            const float b = col_bias ? __shfl_sync(0xffffffffu, bl, base + j) : bl;
-            if (!valid || col0 + j >= N) continue;
-            float x = alpha * v[j];
-            if (beta != 0.0f) x = fmaf(beta, crow[col0 + j], x);
-            crow[col0 + j] = activate(x + b, ACT);
-        }
-    }
-}
-
-// The 16 columns col0 .. col0 + 15 (= chunk column base .. base + 15) of one
-// row; called by all 32 lanes of the warp (see store16_ep).
-template <bool VEC_C>
-__device__ __forceinline__ void store16_fused(const Args &a, float *crow, int64_t row, int64_t col0, int base,
-                                              float bl, const float (&v)[16]) {
-    const int64_t N = a.N;
-    if (col0 >= N) return;  // uniform over the warp
-    const bool valid = row < a.M;
-    const float alpha = a.alpha, beta = a.beta;
-    const bool cb = a.bias_kind == SGEMM_BIAS_PER_COL;
-    switch (a.act) {
-        case SGEMM_ACT_RELU:
-            store16_ep<VEC_C, SGEMM_ACT_RELU>(crow, valid, col0, base, N, alpha, beta, cb, bl, v);
-            break;
-        case SGEMM_ACT_GELU:
-            store16_ep<VEC_C, SGEMM_ACT_GELU>(crow, valid, col0, base, N, alpha, beta, cb, bl, v);
-            break;
-        case SGEMM_ACT_SILU:
-            store16_ep<VEC_C, SGEMM_ACT_SILU>(crow, valid, col0, base, N, alpha, beta, cb, bl, v);
-            break;
-        default: store16_ep<VEC_C, SGEMM_ACT_NONE>(crow, valid, col0, base, N, alpha, beta, cb, bl, v); break;
-    }
-}
-
-// Writes 32 accumulator values (columns col0 .. col0 + 31 of one row of C):
-// C = alpha * v + beta * C (C read only when beta != 0), or, for a tile split
-// along K (C already holds beta * C + bias; the activation follows in a
-// later pass), C += alpha * v with atomics.
-template <bool VEC_C>
-__device__ __forceinline__ void store_chunk(const Args &a, float *crow, int64_t row, int64_t col0, const float (&v)[32],
-                                            bool atomic) {
-    const int64_t N = a.N;
-    if (row >= a.M || col0 >= N) return;
-    const float alpha = a.alpha, beta = a.beta;
-    if (atomic) {
-        if (VEC_C && col0 + 31 < N) {
-#pragma unroll
-            for (int j = 0; j < 32; j += 4)
-                red_add_v4(crow + col0 + j, alpha * v[j], alpha * v[j + 1], alpha * v[j + 2], alpha * v[j + 3]);
-        } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-                if (col0 + j < N) atomicAdd(crow + col0 + j, alpha * v[j]);
-        }
-    } else if (VEC_C && col0 + 31 < N) {
-#pragma unroll
-        for (int j = 0; j < 32; j += 4) {
-            float4 *p = reinterpret_cast<float4 *>(crow + col0 + j);
-            float4 o = make_float4(alpha * v[j], alpha * v[j + 1], alpha * v[j + 2], alpha * v[j + 3]);
-            if (beta != 0.0f) {
-                const float4 c = *p;
-                o.x = fmaf(beta, c.x, o.x);
-                o.y = fmaf(beta, c.y, o.y);
-                o.z = fmaf(beta, c.z, o.z);
-                o.w = fmaf(beta, c.w, o.w);
-            }
-            *p = o;
-        }
-    } else {
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-            if (col0 + j < N) crow[col0 + j] = beta != 0.0f ? fmaf(beta, crow[col0 + j], alpha * v[j]) : alpha * v[j];
-    }
-}
-
-// Epilogue of one 32-column chunk of the accumulator at TMEM address taddr
-// (this thread's lane): loads it and writes C. release: arrive on mbarrier
-// release_bar once the chunk is out of TMEM (the accumulator may be reused).
-// With a fused bias / activation on a whole tile the chunk goes in two
-// 16-column halves, which leaves the activation the registers it needs.
-template <bool VEC_C>
-__device__ __forceinline__ void epilogue_chunk(const Args &a, uint32_t taddr, float *crow, int64_t row, int64_t col0,
-                                               bool atomic, bool release, uint32_t release_bar) {
-    if (a.ep && !atomic) {
-        // Bias of this chunk: lane l holds column col0 + l's value (per
-        // column, one coalesced load issued before the TMEM loads) or the
-        // row's value (per row).
-        const int lane = static_cast<int>(threadIdx.x & 31);
-        float bl = 0.0f;
-        if (a.bias_kind == SGEMM_BIAS_PER_COL && col0 + lane < a.N) bl = __ldg(a.bias + col0 + lane);
-        if (a.bias_kind == SGEMM_BIAS_PER_ROW && row < a.M) bl = __ldg(a.bias + row);
-        float v[16];
-        tmem_load16(taddr, v);
-        store16_fused<VEC_C>(a, crow, row, col0, 0, bl, v);
-        tmem_load16(taddr + 16, v);
-        if (release) {
-            tc_fence_before();
-            mbar_arrive(release_bar);
-        }
-        store16_fused<VEC_C>(a, crow, row, col0 + 16, 16, bl, v);
-    } else {
-        float v[32];
-        tmem_load32(taddr, v);
-        if (release) {
-            tc_fence_before();
-            mbar_arrive(release_bar);
-        }
-        store_chunk<VEC_C>(a, crow, row, col0, v, atomic);
-    }
-}
-
-// Calls f(tile, kb, ke) for this CTA's units of work, in order.
-template <class F>
-__device__ __forceinline__ void for_each_unit(const Args &a, volatile int *abort_flag, F &&f) {
-    for (int t = blockIdx.x; t < a.dp_tiles; t += gridDim.x) {
-        if (*abort_flag) return;
-        f(t, 0, a.k_blocks);
-    }
-    if (static_cast<int>(blockIdx.x) < a.sk_ctas) {
-        int64_t it = a.sk_iters * blockIdx.x / a.sk_ctas;
-        const int64_t end = a.sk_iters * (blockIdx.x + 1) / a.sk_ctas;
-        while (it < end) {
-            if (*abort_flag) return;
-            const int tile = a.dp_tiles + static_cast<int>(it / a.k_blocks);
-            const int kb = static_cast<int>(it % a.k_blocks);
-            const int64_t rest = end - it;
-            const int ke = static_cast<int>(rest < a.k_blocks - kb ? kb + rest : a.k_blocks);
-            f(tile, kb, ke);
-            it += ke - kb;
-        }
-    }
-}
 
 template <bool VEC_A, bool VEC_B, bool VEC_C>
 __global__ void __launch_bounds__(THREADS, 1) tf32x3_kernel(const Args a) {
@@ -1418,25 +948,6 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
-// A batch of row-major rows x cols fp32 matrices with row stride ld and item
-// stride `stride` (elements; 0 = one matrix shared by all items), boxes of
-// box_cols x box_rows x 1, out-of-range elements read as zero.
-bool encode_map(CUtensorMap *map, const float *ptr, int64_t rows, int64_t cols, int64_t ld, int64_t batch,
-                int64_t stride, uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle swizzle) {
-    auto enc = tensor_map_encoder();
-    if (!enc) return false;
-    const int64_t items = stride == 0 ? 1 : batch;
-    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
-                                static_cast<cuuint64_t>(items)};
-    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld) * sizeof(float),
-                                   static_cast<cuuint64_t>(stride == 0 ? ld * rows : stride) * sizeof(float)};
-    const cuuint32_t box[3] = {box_cols, box_rows, 1};
-    const cuuint32_t estr[3] = {1, 1, 1};
-    return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(ptr), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 // TMA requirements: 16-byte aligned bases and row strides, coordinates that
 // fit int32.
 bool tma_ok(const Problem &p) {
@@ -1522,6 +1033,28 @@ int launch_tma(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStream_
 
 }  // namespace
 
+namespace tc {
+
+// A batch of row-major rows x cols fp32 matrices as a rank-3 tensor map (see
+// tc_common.cuh).
+bool encode_map(CUtensorMap *map, const float *ptr, int64_t rows, int64_t cols, int64_t ld, int64_t batch,
+                int64_t stride, uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle swizzle) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    const int64_t items = stride == 0 ? 1 : batch;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
+                                static_cast<cuuint64_t>(items)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld) * sizeof(float),
+                                   static_cast<cuuint64_t>(stride == 0 ? ld * rows : stride) * sizeof(float)};
+    const cuuint32_t box[3] = {box_cols, box_rows, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(ptr), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace tc
+
 int *watchdog_flag_device_ptr() {
     static std::once_flag once[kMaxDevices];
     static int *ptrs[kMaxDevices];
@@ -1571,7 +1104,7 @@ int watchdog_selftest_launch(int64_t wait_ms, cudaStream_t stream) {
 }
 
 int tf32x3_set_kernel(int64_t mode) {
-    if (mode < 0 || mode > 2) return SGEMM_ERR_INVALID_ARG;
+    if (mode < 0 || mode > 3) return SGEMM_ERR_INVALID_ARG;
     g_use_tma.store(static_cast<int>(mode));
     return SGEMM_OK;
 }
@@ -1607,7 +1140,8 @@ int tf32x3_launch(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStre
         return vc ? launch_tma<true, true, false, true>(p, dev, sk_mode, stream, launches)
                   : launch_tma<true, false, false, true>(p, dev, sk_mode, stream, launches);
     }
-    if (mode == 2 && tma_ok(p))
+    if (mode == 3 && tma_ok(p)) return tf32x3_pair_launch(p, dev, sk_mode, stream, launches);
+    if (mode >= 2 && tma_ok(p))
         return vc ? launch_tma<true, true>(p, dev, sk_mode, stream, launches)
                   : launch_tma<true, false>(p, dev, sk_mode, stream, launches);
     if (mode >= 1 && tma_ok(p))

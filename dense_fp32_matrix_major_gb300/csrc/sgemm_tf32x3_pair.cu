@@ -1,0 +1,446 @@
+// Tensor-core SGEMM on SM pairs: tcgen05.mma.cta_group::2 (kind::tf32) with
+// the three-term TF32 split of sgemm_tf32x3.cu, for op(A) = A, op(B) = B with
+// 16-byte aligned rows.
+//
+// The product is the plain sum of "CUDA算子优化(4)：矩阵乘法", section
+// "矩阵乘法的数学定义"; the pages give no tensor-core design (they name
+// tensor cores once, "CUDA内存优化入门：从Naive到Tiled矩阵乘法", section 八).
+//
+// Why pairs. On one SM the 128 x 256 kernel moves about 256 KB through
+// shared memory per 32-deep k-block (TMA writes of the raw tiles, the
+// converters' reads and their hi / lo writes of B, and the tensor core's
+// reads of B, 8 KB per 128 x 256 x 8 MMA), which holds the tensor pipe near
+// 83% of its rate. Two CTAs on two SMs of a cluster share one 256 x 256 tile:
+// each holds 128 rows of A (in its TMEM) and 128 columns of B (in its shared
+// memory), and one MMA of 256 x 256 x 8 issued by the even CTA reads both
+// halves. Per SM that halves B's traffic: about 144 KB per k-block for the
+// same flops, under what the shared-memory pipe sustains.
+//
+// Roles in each CTA (18 warps):
+//   * warp 0: in the even CTA, one thread issues the pair's MMAs (4 k-slices
+//     x 3 products per k-block, lo*hi + hi*lo + hi*hi) and commits them to
+//     the mbarriers of both CTAs (multicast); idle in the odd CTA.
+//   * warp 1: TMA of this CTA's A rows (128 x 32, 128-byte swizzled) and B
+//     columns (32 x 128, unswizzled) into a 4-slot raw ring.
+//   * warps 2-9 (converters): split A into hi / lo and write them to this
+//     CTA's TMEM (the A operand), transpose and split B into K-major,
+//     128-byte-swizzled hi / lo tiles in a 3-stage shared ring, then one lane
+//     per warp arrives on the even CTA's stage-full mbarrier.
+//   * warps 10-17 (epilogue): two per TMEM lane quarter, each reading 128 of
+//     the accumulator's 256 columns for its 32 rows, storing C (plain, fused
+//     epilogue, or atomic adds for tiles split along K), then one lane per
+//     warp frees the accumulator on the even CTA's mbarrier.
+// Every wait is bounded in time as in the single-SM kernels; the pair meets
+// at cluster barriers only at the start (mbarriers initialised) and at the
+// end (before the TMEM of both is released).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "sgemm.h"
+#include "sgemm_internal.h"
+#include "tc_common.cuh"
+
+namespace sgemm {
+namespace {
+
+using namespace tc;
+
+namespace pr {
+
+constexpr int PM = 256, PN = 256;  // C tile of a pair
+constexpr int HM = 128, HN = 128;  // this CTA's rows of A, columns of B
+constexpr int OP_STAGES = 3, RAW_SLOTS = 4;
+constexpr int B_HALF = HN * BK * 4;   // 16 KB: one of B hi / B lo, or raw B
+constexpr int A_RAW = HM * BK * 4;    // 16 KB
+constexpr int OP_STAGE = 2 * B_HALF;  // hi | lo
+constexpr int SLOT = A_RAW + B_HALF;  // raw A | raw B
+constexpr int RAW0 = OP_STAGES * OP_STAGE;
+constexpr int BAR_OFFSET = RAW0 + RAW_SLOTS * SLOT;
+constexpr int PBAR_BYTES = 256;
+constexpr int SMEM_BYTES = BAR_OFFSET + PBAR_BYTES + 1024;
+constexpr int CONV_WARPS = 8, EPI_WARPS = 8;
+constexpr int CONV_THREADS = 32 * CONV_WARPS;
+constexpr int EPI_WARP0 = 2 + CONV_WARPS;
+constexpr int THREADS = 32 * (EPI_WARP0 + EPI_WARPS);
+constexpr uint32_t TMEM_A = PN;  // A stages after the 256-column accumulator
+// Instruction descriptor: D fp32, A and B tf32, both K-major, N = 256, M = 256.
+constexpr uint32_t kIdesc2 = (1u << 4) | (2u << 7) | (2u << 10) | (static_cast<uint32_t>(PN >> 3) << 17) |
+                             (static_cast<uint32_t>(PM >> 4) << 24);
+// mbarrier indices
+constexpr int RAW_FULL = 0, RAW_FREE = RAW_FULL + RAW_SLOTS, OP_FULL = RAW_FREE + RAW_SLOTS,
+              OP_EMPTY = OP_FULL + OP_STAGES, ACC_FULL = OP_EMPTY + OP_STAGES, ACC_EMPTY = ACC_FULL + 1,
+              DRAIN = ACC_EMPTY + 1, NBARS = DRAIN + 1;
+static_assert(NBARS * 8 + 16 <= PBAR_BYTES, "barrier block");
+static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
+static_assert(TMEM_A + OP_STAGES * 64 <= TMEM_COLS, "TMEM columns");
+static_assert((HN / 4) * (BK / 4) == CONV_THREADS, "one 4 x 4 B block per converter thread");
+
+}  // namespace pr
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Arrive on the mbarrier at this CTA's shared offset `bar` in CTA `cta` of
+// the cluster, releasing this thread's prior writes at cluster scope.
+__device__ __forceinline__ void mbar_arrive_at(uint32_t bar, uint32_t cta) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(bar), "r"(cta));
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote) : "memory");
+}
+
+// One 256 x 256 x 8 product of the pair: A (128 rows per CTA) from TMEM, B
+// (128 columns per CTA) from shared memory.
+__device__ __forceinline__ void tc_mma2_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t accumulate) {
+    asm volatile(
+        "{\n"
+        " .reg .pred p;\n"
+        " setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::2.kind::tf32 [%0], [%1], %2, %3, p;\n"
+        "}\n" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(pr::kIdesc2), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive on the mbarrier at offset `bar` of both CTAs once the pair's MMAs
+// issued so far have completed.
+__device__ __forceinline__ void tc_commit2(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            bar),
+        "h"(static_cast<uint16_t>(3))
+        : "memory");
+}
+
+template <bool VEC_C>
+__global__ void __launch_bounds__(pr::THREADS, 1)
+    tf32x3_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const Args a) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *smem = smem_raw + (base - raw);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + pr::BAR_OFFSET);
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + pr::NBARS);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + pr::NBARS + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_rank();
+    const int pair = static_cast<int>(blockIdx.x >> 1), pairs = static_cast<int>(gridDim.x >> 1);
+    auto bar = [&](int i) { return smem_u32(bars + i); };
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < pr::RAW_SLOTS; ++s) {
+            mbar_init(bar(pr::RAW_FULL + s), 1);
+            mbar_init(bar(pr::RAW_FREE + s), pr::CONV_THREADS);
+        }
+        for (int s = 0; s < pr::OP_STAGES; ++s) {
+            mbar_init(bar(pr::OP_FULL + s), 2 * pr::CONV_WARPS);  // one lane per converter warp of both CTAs
+            mbar_init(bar(pr::OP_EMPTY + s), 1);
+        }
+        mbar_init(bar(pr::ACC_FULL), 1);
+        mbar_init(bar(pr::ACC_EMPTY), 2 * pr::EPI_WARPS);
+        mbar_init(bar(pr::DRAIN), 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0) {
+        // Both CTAs allocate: the pair's MMAs use the same columns in each.
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_holder)),
+                     "r"(TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // the peer's mbarriers exist before anyone arrives on them
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ MMA issuer
+        if (rank == 0 && lane == 0) {
+            uint32_t it = 0, unit = 0;
+            for_each_unit_of(a, abort_flag, pair, pairs, [&](int, int kb, int ke) {
+                if (!mbar_wait<true>(bar(pr::ACC_EMPTY), (unit & 1) ^ 1, a, abort_flag, WD_MMA_ACC)) return;
+                tc_fence_after();
+                for (int kblk = kb; kblk < ke; ++kblk, ++it) {
+                    const int s = static_cast<int>(it % pr::OP_STAGES);
+                    const uint32_t ph = (it / pr::OP_STAGES) & 1;
+                    if (!mbar_wait<true>(bar(pr::OP_FULL + s), ph, a, abort_flag, WD_MMA_FULL)) return;
+                    tc_fence_after();
+                    const uint32_t st = base + static_cast<uint32_t>(s * pr::OP_STAGE);
+                    const uint64_t b_hi = sw128_desc(st), b_lo = sw128_desc(st + pr::B_HALF);
+                    const uint32_t a_hi = tmem_base + pr::TMEM_A + static_cast<uint32_t>(64 * s);
+                    const uint32_t a_lo = a_hi + 32;
+#pragma unroll
+                    for (int ks = 0; ks < BK / 8; ++ks) {
+                        const uint64_t adv = static_cast<uint64_t>(ks * 2);
+                        const uint32_t ac = static_cast<uint32_t>(ks * 8);
+                        const uint32_t first = (kblk == kb && ks == 0) ? 0u : 1u;
+                        tc_mma2_ts(tmem_base, a_lo + ac, b_hi + adv, first);
+                        tc_mma2_ts(tmem_base, a_hi + ac, b_lo + adv, 1u);
+                        tc_mma2_ts(tmem_base, a_hi + ac, b_hi + adv, 1u);
+                    }
+                    tc_commit2(bar(pr::OP_EMPTY + s));
+                }
+                tc_commit2(bar(pr::ACC_FULL));
+                ++unit;
+            });
+            tc_commit2(bar(pr::DRAIN));
+            const bool was_aborted = *abort_flag != 0;
+            if (!mbar_wait(bar(pr::DRAIN), 0, a, abort_flag, WD_DRAIN) && was_aborted) {
+                const uint64_t t0 = global_timer();
+                while (!mbar_try_wait(bar(pr::DRAIN), 0) && global_timer() - t0 < a.timeout_ns) {
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ TMA issuer
+        if (lane == 0) {
+            uint32_t it = 0;
+            bool ok = true;
+            for_each_unit_of(a, abort_flag, pair, pairs, [&](int tile, int kb, int ke) {
+                if (!ok) return;
+                const TileAt at = tile_at<pr::PM, pr::PN>(a, tile);
+                const int m0 = static_cast<int>(at.m0) + pr::HM * static_cast<int>(rank);
+                const int n0 = static_cast<int>(at.n0) + pr::HN * static_cast<int>(rank);
+                const int za = a.a_shared ? 0 : at.item, zb = a.b_shared ? 0 : at.item;
+                for (int kblk = kb; kblk < ke; ++kblk, ++it) {
+                    const int slot = static_cast<int>(it % pr::RAW_SLOTS);
+                    const uint32_t ph = (it / pr::RAW_SLOTS) & 1;
+                    if (!mbar_wait(bar(pr::RAW_FREE + slot), ph ^ 1, a, abort_flag, WD_PRODUCER)) {
+                        ok = false;
+                        return;
+                    }
+                    const uint32_t sl = base + pr::RAW0 + static_cast<uint32_t>(slot * pr::SLOT);
+                    mbar_arrive_expect_tx(bar(pr::RAW_FULL + slot), pr::SLOT);
+                    tma_load_3d(sl, &tmA, kblk * BK, m0, za, bar(pr::RAW_FULL + slot));
+                    tma_load_3d(sl + pr::A_RAW, &tmB, n0, kblk * BK, zb, bar(pr::RAW_FULL + slot));
+                }
+            });
+        }
+    } else if (warp < pr::EPI_WARP0) {
+        // ------------------------------------------------------------ converters
+        const int ct = threadIdx.x - 64;
+        const int l = ct & 7, tb = ct >> 3;                 // 32 groups of eight lanes
+        const int g = (tb >> 3) * 8 + l, c = (l + tb) & 7;  // this thread's 4 x 4 B block
+        const int q = warp & 3, part = (warp - 2) >> 2;     // TMEM lane quarter, k-columns 16*part..+15
+        const int arow = 32 * q + lane;                     // A row this thread converts
+        uint32_t it = 0;
+        bool ok = true;
+        for_each_unit_of(a, abort_flag, pair, pairs, [&](int, int kb, int ke) {
+            if (!ok) return;
+            for (int kblk = kb; kblk < ke; ++kblk, ++it) {
+                const int slot = static_cast<int>(it % pr::RAW_SLOTS);
+                const int s = static_cast<int>(it % pr::OP_STAGES);
+                if (!mbar_wait(bar(pr::RAW_FULL + slot), (it / pr::RAW_SLOTS) & 1, a, abort_flag, WD_PRODUCER)) {
+                    ok = false;
+                    return;
+                }
+                const uint32_t sl = base + pr::RAW0 + static_cast<uint32_t>(slot * pr::SLOT);
+                // A: 16 k-values of row arow (chunks 4*part .. 4*part+3 of the swizzled row).
+                float4 av[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) av[j] = ld_shared_v4(sl + sw128_offset(arow, 4 * part + j));
+                // B: rows 4c..4c+3, columns 4g..4g+3 of the unswizzled 32 x 128 staging tile.
+                float4 bq[4];
+#pragma unroll
+                for (int qq = 0; qq < 4; ++qq)
+                    bq[qq] = ld_shared_v4(sl + pr::A_RAW + static_cast<uint32_t>((4 * c + qq) * pr::HN * 4 + g * 16));
+                fence_proxy_async_smem();  // order these loads before the next TMA into the slot
+                mbar_arrive(bar(pr::RAW_FREE + slot));
+                // The stage is free once the pair's MMAs three k-blocks back are done.
+                if (!mbar_wait<true>(bar(pr::OP_EMPTY + s), ((it / pr::OP_STAGES) & 1) ^ 1, a, abort_flag,
+                                     WD_PRODUCER)) {
+                    ok = false;
+                    return;
+                }
+                tc_fence_after();
+                const uint32_t st = base + static_cast<uint32_t>(s * pr::OP_STAGE);
+                // Column j of the 4 x 4 block is chunk c of operand row 4g + j.
+                uint32_t off = sw128_offset(4 * g + 0, c);
+                split_store(st + off, st + pr::B_HALF + off, bq[0].x, bq[1].x, bq[2].x, bq[3].x);
+                off = sw128_offset(4 * g + 1, c);
+                split_store(st + off, st + pr::B_HALF + off, bq[0].y, bq[1].y, bq[2].y, bq[3].y);
+                off = sw128_offset(4 * g + 2, c);
+                split_store(st + off, st + pr::B_HALF + off, bq[0].z, bq[1].z, bq[2].z, bq[3].z);
+                off = sw128_offset(4 * g + 3, c);
+                split_store(st + off, st + pr::B_HALF + off, bq[0].w, bq[1].w, bq[2].w, bq[3].w);
+                float hi[16], lo[16];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    split_tf32(av[j].x, hi[4 * j], lo[4 * j]);
+                    split_tf32(av[j].y, hi[4 * j + 1], lo[4 * j + 1]);
+                    split_tf32(av[j].z, hi[4 * j + 2], lo[4 * j + 2]);
+                    split_tf32(av[j].w, hi[4 * j + 3], lo[4 * j + 3]);
+                }
+                const uint32_t ta = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + pr::TMEM_A +
+                                    static_cast<uint32_t>(64 * s + 16 * part);
+                tmem_store16(ta, hi);
+                tmem_store16(ta + 32, lo);
+                tmem_wait_st();
+                fence_proxy_async_smem();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_at(bar(pr::OP_FULL + s), 0);
+            }
+        });
+    } else {
+        // -------------------------------------------------------------- epilogue
+        const int q = warp & 3;                      // TMEM lane quarter this warp may access
+        const int half = (warp - pr::EPI_WARP0) >> 2;  // accumulator columns 128*half .. +127
+        uint32_t unit = 0;
+        for_each_unit_of(a, abort_flag, pair, pairs, [&](int tile, int kb, int ke) {
+            if (!mbar_wait<true>(bar(pr::ACC_FULL), unit & 1, a, abort_flag, WD_EPILOGUE)) return;
+            tc_fence_after();
+            const TileAt at = tile_at<pr::PM, pr::PN>(a, tile);
+            const int64_t row = at.m0 + pr::HM * static_cast<int64_t>(rank) + q * 32 + lane;
+            // Stream-K tiles hold beta * C + bias already: every unit adds.
+            const bool atomic = tile >= a.dp_tiles;
+            float *crow = a.C + at.item * a.strideC + row * a.ldc;
+#pragma unroll 1
+            for (int cc = 0; cc < 4; ++cc) {
+                const int ch = 4 * half + cc;
+                epilogue_chunk_then<VEC_C>(
+                    a, tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(ch * 32), crow, row,
+                    at.n0 + ch * 32, atomic, cc == 3, [&] {
+                        // This warp's columns are out of TMEM: one lane frees them on
+                        // the even CTA's accumulator barrier.
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive_at(bar(pr::ACC_EMPTY), 0);
+                    });
+            }
+            ++unit;
+        });
+    }
+
+    // The odd CTA's TMEM is written by the even CTA's MMAs: wait for them to
+    // drain before the pair releases it.
+    tc_fence_before();
+    __syncthreads();
+    if (rank != 0 && threadIdx.x == 0) {
+        if (!mbar_wait<true>(bar(pr::DRAIN), 0, a, abort_flag, WD_DRAIN)) {
+            const uint64_t t0 = global_timer();
+            while (!mbar_try_wait<true>(bar(pr::DRAIN), 0) && global_timer() - t0 < a.timeout_ns) {
+            }
+        }
+    }
+    __syncthreads();
+    cluster_sync();
+    tc_fence_after();
+    if (warp == 0) {
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS)
+                     : "memory");
+    }
+}
+
+constexpr int kMaxDevices = 64;
+std::once_flag g_pair_once[kMaxDevices][2];
+cudaError_t g_pair_err[kMaxDevices][2];
+int g_pair_clusters[kMaxDevices][2];
+
+template <bool VEC_C>
+int launch_pair(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStream_t stream, int *launches) {
+    auto kernel = tf32x3_pair_kernel<VEC_C>;
+    constexpr int idx = VEC_C ? 1 : 0;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg{};
+    cfg.blockDim = dim3(pr::THREADS);
+    cfg.dynamicSmemBytes = pr::SMEM_BYTES;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    std::call_once(g_pair_once[dev.device][idx], [&] {
+        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, pr::SMEM_BYTES);
+        int n = 0;
+        if (e == cudaSuccess) {
+            cudaLaunchConfig_t q = cfg;
+            q.gridDim = dim3(2 * (dev.sm_count / 2));
+            e = cudaOccupancyMaxActiveClusters(&n, kernel, &q);
+        }
+        g_pair_err[dev.device][idx] = e;
+        g_pair_clusters[dev.device][idx] = n;
+    });
+    const int clusters = g_pair_clusters[dev.device][idx];
+    if (g_pair_err[dev.device][idx] != cudaSuccess || clusters < 1) {
+        cudaGetLastError();
+        return SGEMM_ERR_LAUNCH;
+    }
+    int *flag = watchdog_flag_device_ptr();
+    if (!flag) return SGEMM_ERR_LAUNCH;
+    alignas(64) CUtensorMap mapA, mapB;
+    if (!encode_map(&mapA, p.A, p.M, p.K, p.lda, p.batch, p.strideA, BK, pr::HM, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_map(&mapB, p.B, p.K, p.N, p.ldb, p.batch, p.strideB, pr::HN, BK, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return SGEMM_ERR_LAUNCH;
+
+    const int64_t tiles_m = (p.M + pr::PM - 1) / pr::PM, tiles_n = (p.N + pr::PN - 1) / pr::PN;
+    const int64_t k_blocks = (p.K + BK - 1) / BK;
+    if (tiles_m * tiles_n * p.batch > INT32_MAX / 2 || k_blocks > INT32_MAX / 2) return SGEMM_ERR_UNSUPPORTED;
+    const int tiles = static_cast<int>(tiles_m * tiles_n * p.batch);
+    // One pair per two SMs, as many pairs as fit at once. A stream-K share
+    // below 4 k-blocks costs more in fix-up than it saves.
+    const Schedule sch = make_schedule(tiles, k_blocks, clusters, sk_mode, 4, 0.25);
+    const int split = tiles - sch.dp_tiles;
+    int rc = split_tiles_prepare(p, pr::PM, pr::PN, static_cast<int>(tiles_n), static_cast<int>(tiles_m * tiles_n),
+                                 sch.dp_tiles, split, stream, launches);
+    if (rc != SGEMM_OK) return rc;
+    Args a{};
+    a.M = p.M;
+    a.N = p.N;
+    a.K = p.K;
+    a.C = p.C;
+    a.ldc = p.ldc;
+    a.tiles_n = static_cast<int>(tiles_n);
+    a.k_blocks = static_cast<int>(k_blocks);
+    a.dp_tiles = sch.dp_tiles;
+    a.sk_ctas = sch.sk_ctas;
+    a.sk_iters = sch.sk_iters;
+    a.timeout_ns = static_cast<uint64_t>(watchdog_ms()) * 1000000ull;
+    a.watchdog = flag;
+    a.alpha = p.alpha;
+    a.beta = p.beta;
+    a.strideA = p.strideA;
+    a.strideB = p.strideB;
+    a.strideC = p.strideC;
+    a.tiles_per_item = static_cast<int>(tiles_m * tiles_n);
+    a.a_shared = p.strideA == 0;
+    a.b_shared = p.strideB == 0;
+    a.bias = p.bias;
+    a.bias_kind = p.bias_kind;
+    a.act = p.act;
+    a.ep = p.has_epilogue();
+    cfg.gridDim = dim3(2 * sch.grid);
+    if (cudaLaunchKernelEx(&cfg, kernel, mapA, mapB, a) != cudaSuccess) {
+        cudaGetLastError();
+        return SGEMM_ERR_LAUNCH;
+    }
+    ++*launches;
+    return split_tiles_finish(p, pr::PM, pr::PN, static_cast<int>(tiles_n), static_cast<int>(tiles_m * tiles_n),
+                              sch.dp_tiles, split, stream, launches);
+}
+
+}  // namespace
+
+int tf32x3_pair_launch(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStream_t stream, int *launches) {
+    if (dev.device < 0 || dev.device >= kMaxDevices) return SGEMM_ERR_DEVICE;
+    const bool vc = (p.ldc % 4 == 0) && (p.strideC % 4 == 0) && (reinterpret_cast<uintptr_t>(p.C) % 16 == 0);
+    return vc ? launch_pair<true>(p, dev, sk_mode, stream, launches)
+              : launch_pair<false>(p, dev, sk_mode, stream, launches);
+}
+
+}  // namespace sgemm

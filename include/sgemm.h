@@ -235,7 +235,10 @@ int sgemm_watchdog_selftest(int64_t wait_ms, sgemm_stream_t stream);
  *   SGEMM_TUNE_TF32X3_KERNEL  tensor-core kernel for operands whose base
  *                            addresses and row strides are 16-byte aligned:
  *                            0 = per-thread loads, 1 = TMA, 2 = TMA with A's
- *                            operands in tensor memory (default)
+ *                            operands in tensor memory (default), 3 = the
+ *                            SM-pair kernel (tcgen05 cta_group::2, clusters of
+ *                            two CTAs; op(A) = A, op(B) = B only, the
+ *                            transposed forms keep kernel 2)
  * Returns SGEMM_OK or SGEMM_ERR_INVALID_ARG. sgemm_get_tuning returns the
  * value, or -1 for an unknown key.
  */

@@ -22,7 +22,8 @@ KINDS = {None: 0, "col": 1, "row": 2}
 ACTS = {None: 0, "relu": 1, "gelu": 2, "silu": 3}
 # (variant, FFMA tile, stream-K mode, tensor-core kernel)
 SETTINGS = [("ffma", 1, 1, 2), ("ffma", 2, 3, 2), ("ffma", 3, 2, 2), ("tf32x3", 0, 1, 2),
-            ("tf32x3", 0, 3, 2), ("tf32x3", 0, 3, 1), ("tf32x3", 0, 3, 0), ("auto", 0, 0, 2)]
+            ("tf32x3", 0, 3, 2), ("tf32x3", 0, 3, 1), ("tf32x3", 0, 3, 0), ("tf32x3", 0, 1, 3),
+            ("tf32x3", 0, 3, 3), ("auto", 0, 0, 2)]
 
 
 @pytest.fixture(scope="module")

@@ -18,12 +18,13 @@ pytestmark = pytest.mark.gpu
 
 # (variant, ffma tile, stream-K mode, tensor-core kernel) settings every
 # small-shape test runs under. Tensor-core kernels: 0 = per-thread loads,
-# 1 = TMA, 2 = TMA with A in tensor memory (default).
+# 1 = TMA, 2 = TMA with A in tensor memory (default), 3 = SM pairs.
 SETTINGS = [
     ("auto", 0, 0, 2),
     ("ffma", 1, 1, 2), ("ffma", 1, 3, 2), ("ffma", 2, 2, 2), ("ffma", 3, 0, 2), ("ffma", 2, 3, 2),
     ("tf32x3", 0, 0, 2), ("tf32x3", 0, 1, 2), ("tf32x3", 0, 3, 2),
     ("tf32x3", 0, 0, 1), ("tf32x3", 0, 3, 1), ("tf32x3", 0, 0, 0), ("tf32x3", 0, 3, 0),
+    ("tf32x3", 0, 0, 3), ("tf32x3", 0, 1, 3), ("tf32x3", 0, 3, 3),
 ]
 SETTING_IDS = [f"{s[0]}-t{s[1]}-sk{s[2]}-k{s[3]}" for s in SETTINGS]
 
@@ -169,7 +170,8 @@ def _config_error(C, A, B, w):
 
 
 @pytest.mark.parametrize("w", wl.ALL, ids=lambda w: w.name)
-@pytest.mark.parametrize("variant,tc", [("auto", 2), ("ffma", 2), ("tf32x3", 2), ("tf32x3", 1), ("tf32x3", 0)])
+@pytest.mark.parametrize("variant,tc", [("auto", 2), ("ffma", 2), ("tf32x3", 2), ("tf32x3", 1), ("tf32x3", 0),
+                                        ("tf32x3", 3)])
 def test_benchmark_configs(lib, w, variant, tc):
     _apply(lib, (variant, 0, 0, tc))
     A, B = wl.make_inputs(w)
