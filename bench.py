@@ -157,13 +157,18 @@ def _traffic_record(kernel_key: str):
     rec = recs.get(kernel_key)
     if not rec:
         return None
-    src = os.path.join(ROOT, rec["source"])
+    h = hashlib.sha256()
     try:
-        with open(src, "rb") as f:
-            digest = hashlib.sha256(f.read()).hexdigest()[:16]
+        for rel in rec["sources"]:
+            with open(os.path.join(ROOT, rel), "rb") as f:
+                h.update(f.read())
     except OSError:
         return None
-    return rec["dram_bytes_per_launch"] if digest == rec["source_sha256_16"] else None
+    return rec["dram_bytes_per_launch"] if h.hexdigest()[:16] == rec["sources_sha256_16"] else None
+
+
+# Kernel names by the library's SGEMM_TUNE_LAST_TC_KERNEL value.
+TC_KERNELS = {1: "tf32x3_kernel", 2: "tf32x3_tma_kernel", 3: "tf32x3_tmem_kernel", 4: "tf32x3_pair_kernel"}
 
 
 # -------------------------------------------------------------- our arm
@@ -203,6 +208,7 @@ def run_ours(args, w, torch, dist):
     torch.cuda.synchronize()
     variant_used = sgemm.variant_name(sgemm.last_variant_used())
     launches_per_step = sgemm.last_launch_count()
+    tc_kernel = TC_KERNELS.get(sgemm.get_tuning(sgemm.SGEMM_TUNE_LAST_TC_KERNEL), "tf32x3")
 
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
@@ -249,16 +255,16 @@ def run_ours(args, w, torch, dist):
     if variant_used == "tf32x3":
         peak, peak_src = _tf32x3_peak_tflops()
         bound = "tensor"
-        kernel_key = "tf32x3"
+        kernel_key = tc_kernel
     else:
         peak = sm_count * FP32_LANES_PER_SM * 2 * sm_max * 1e6 / 1e12
         peak_src = f"{sm_count} SMs x 128 FP32 lanes x 2 x {sm_max:.0f} MHz (recipe unit counts)"
         bound = "alu"
-        kernel_key = "ffma"
+        kernel_key = "ffma_kernel"
     achieved = w.flops / (ms * 1e-3) / 1e12
     roofline = {
         "bound": bound, "achieved": round(achieved, 3), "peak": round(peak, 3), "unit": "TFLOP/s",
-        "frac": round(achieved / peak, 4), "traffic": _traffic_record(kernel_key),
+        "frac": round(achieved / peak, 4), "traffic": _traffic_record(kernel_key), "kernel": kernel_key,
         "peak_source": peak_src,
         "algorithmic_flops_per_launch": w.flops,
         "timing": "CUDA events around each sgemm_f32 call on its stream (includes the small "
@@ -464,7 +470,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--variant", default="auto", choices=["auto", "ffma", "tf32x3"])
     ap.add_argument("--workload", default=wl.C5_HEAD.name, choices=sorted(wl.BY_NAME))
-    ap.add_argument("--tc-kernel", type=int, default=None, choices=[0, 1, 2],
+    ap.add_argument("--tc-kernel", type=int, default=None, choices=[0, 1, 2, 3, 4],
                     help="tensor-core kernel for 16-byte-aligned operands (library tuning key)")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)

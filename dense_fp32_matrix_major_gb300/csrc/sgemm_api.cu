@@ -375,6 +375,7 @@ int64_t sgemm_get_tuning(int key) {
         case SGEMM_TUNE_STREAM_K: return sgemm::g_tune_sk.load();
         case SGEMM_TUNE_WATCHDOG_MS: return sgemm::watchdog_ms();
         case SGEMM_TUNE_TF32X3_KERNEL: return sgemm::tf32x3_get_kernel();
+        case SGEMM_TUNE_LAST_TC_KERNEL: return sgemm::tf32x3_last_kernel();
         default: return -1;
     }
 }

@@ -133,6 +133,7 @@ int watchdog_set_ms(int64_t ms);
 int tf32x3_set_kernel(int64_t mode);
 int watchdog_selftest_launch(int64_t wait_ms, cudaStream_t stream);
 int64_t tf32x3_get_kernel();
+int64_t tf32x3_last_kernel();  // 1-4: the tensor-core kernel of the last TF32X3 launch
 int *watchdog_flag_device_ptr();  // device address of the current device's flag, or nullptr
 
 }  // namespace sgemm

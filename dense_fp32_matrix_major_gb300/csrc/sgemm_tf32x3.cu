@@ -61,11 +61,12 @@ __device__ int g_watchdog_code;
 namespace {
 
 std::atomic<int64_t> g_watchdog_ms{2000};
-// Tensor-core kernel for operands that TMA can load: 0 = LDG kernel only,
-// 1 = TMA kernel, 2 = TMA kernel with A in TMEM (the default), 3 = the
-// SM-pair kernel of sgemm_tf32x3_pair.cu (op(A) = A, op(B) = B; the
-// transposed forms keep kernel 2).
-std::atomic<int> g_use_tma{2};
+// Tensor-core kernel (tuning key SGEMM_TUNE_TF32X3_KERNEL): 0 = automatic,
+// 1 = per-thread loads only, 2 = TMA kernel, 3 = TMA kernel with A in TMEM,
+// 4 = the SM-pair kernel of sgemm_tf32x3_pair.cu (op(A) = A, op(B) = B; the
+// transposed forms take kernel 3).
+std::atomic<int> g_use_tma{0};
+std::atomic<int> g_last_tc_kernel{0};
 
 using namespace tc;
 
@@ -1104,12 +1105,14 @@ int watchdog_selftest_launch(int64_t wait_ms, cudaStream_t stream) {
 }
 
 int tf32x3_set_kernel(int64_t mode) {
-    if (mode < 0 || mode > 3) return SGEMM_ERR_INVALID_ARG;
+    if (mode < 0 || mode > 4) return SGEMM_ERR_INVALID_ARG;
     g_use_tma.store(static_cast<int>(mode));
     return SGEMM_OK;
 }
 
 int64_t tf32x3_get_kernel() { return g_use_tma.load(); }
+
+int64_t tf32x3_last_kernel() { return g_last_tc_kernel.load(); }
 
 int watchdog_set_ms(int64_t ms) {
     if (ms < 1 || ms > 60000) return SGEMM_ERR_INVALID_ARG;
@@ -1131,6 +1134,7 @@ int tf32x3_launch(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStre
     if (p.transA || p.transB) {
         // Transposed forms: the tensor-memory kernel (TMA loads needed).
         if (!tma_ok(p)) return SGEMM_ERR_UNSUPPORTED;
+        g_last_tc_kernel.store(3);
         if (p.transA && p.transB)
             return vc ? launch_tma<true, true, true, true>(p, dev, sk_mode, stream, launches)
                       : launch_tma<true, false, true, true>(p, dev, sk_mode, stream, launches);
@@ -1140,13 +1144,28 @@ int tf32x3_launch(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStre
         return vc ? launch_tma<true, true, false, true>(p, dev, sk_mode, stream, launches)
                   : launch_tma<true, false, false, true>(p, dev, sk_mode, stream, launches);
     }
-    if (mode == 3 && tma_ok(p)) return tf32x3_pair_launch(p, dev, sk_mode, stream, launches);
-    if (mode >= 2 && tma_ok(p))
+    if (tma_ok(p) && mode != 1) {
+        // Automatic: the SM-pair kernel where its 256 x 256 tiles are filled
+        // and the product is large enough for its shorter per-SM operand
+        // traffic to pay (measured on GB300: from about 2^31 multiply-adds
+        // on; below that the single-SM kernel's smaller tiles win).
+        const double work = static_cast<double>(p.M) * static_cast<double>(p.N) * static_cast<double>(p.K) *
+                            static_cast<double>(p.batch);
+        const bool pair = mode == 4 || (mode == 0 && p.M >= 256 && p.N >= 256 && work >= 2147483648.0);
+        if (pair) {
+            g_last_tc_kernel.store(4);
+            return tf32x3_pair_launch(p, dev, sk_mode, stream, launches);
+        }
+        if (mode == 2) {
+            g_last_tc_kernel.store(2);
+            return vc ? launch_tma<false, true>(p, dev, sk_mode, stream, launches)
+                      : launch_tma<false, false>(p, dev, sk_mode, stream, launches);
+        }
+        g_last_tc_kernel.store(3);
         return vc ? launch_tma<true, true>(p, dev, sk_mode, stream, launches)
                   : launch_tma<true, false>(p, dev, sk_mode, stream, launches);
-    if (mode >= 1 && tma_ok(p))
-        return vc ? launch_tma<false, true>(p, dev, sk_mode, stream, launches)
-                  : launch_tma<false, false>(p, dev, sk_mode, stream, launches);
+    }
+    g_last_tc_kernel.store(1);
     const bool va = (p.lda % 4 == 0) && (p.strideA % 4 == 0) && (reinterpret_cast<uintptr_t>(p.A) % 16 == 0);
     const bool vb = (p.ldb % 4 == 0) && (p.strideB % 4 == 0) && (reinterpret_cast<uintptr_t>(p.B) % 16 == 0);
     const int idx = (va ? 4 : 0) + (vb ? 2 : 0) + (vc ? 1 : 0);

@@ -16,20 +16,24 @@
 // halves. Per SM that halves B's traffic: about 144 KB per k-block for the
 // same flops, under what the shared-memory pipe sustains.
 //
-// Roles in each CTA (18 warps):
+// Roles in each CTA (23 warps):
 //   * warp 0: in the even CTA, one thread issues the pair's MMAs (4 k-slices
 //     x 3 products per k-block, lo*hi + hi*lo + hi*hi) and commits them to
 //     the mbarriers of both CTAs (multicast); idle in the odd CTA.
-//   * warp 1: TMA of this CTA's A rows (128 x 32, 128-byte swizzled) and B
-//     columns (32 x 128, unswizzled) into a 4-slot raw ring.
-//   * warps 2-9 (converters): split A into hi / lo and write them to this
-//     CTA's TMEM (the A operand), transpose and split B into K-major,
-//     128-byte-swizzled hi / lo tiles in a 3-stage shared ring, then one lane
-//     per warp arrives on the even CTA's stage-full mbarrier.
-//   * warps 10-17 (epilogue): two per TMEM lane quarter, each reading 128 of
-//     the accumulator's 256 columns for its 32 rows, storing C (plain, fused
-//     epilogue, or atomic adds for tiles split along K), then one lane per
-//     warp frees the accumulator on the even CTA's mbarrier.
+//   * warps 1 and 22: TMA of this CTA's A rows (128 x 32, 128-byte swizzled)
+//     and B columns (32 x 128, unswizzled) into a 4-slot raw ring.
+//   * warps 2-17 (converters, two groups of 8 taking alternate k-blocks):
+//     split A into hi / lo and write them to this CTA's TMEM (the A
+//     operand), transpose and split B into K-major, 128-byte-swizzled hi / lo
+//     tiles in a 3-stage shared ring, then one lane per warp arrives on the
+//     even CTA's stage-full mbarrier.
+//   * warps 18-21 (epilogue): one per TMEM lane quarter, reading the
+//     accumulator's 256 columns for its 32 rows in 32 x 32 chunks, each
+//     staged in shared memory and written by one TMA bulk store (or bulk
+//     reduce-add for tiles split along K); chunks crossing the last row or
+//     column, C that TMA cannot address, or beta != 0 take per-thread stores. After the last chunk's
+//     TMEM load one lane per warp frees the accumulator on the even CTA's
+//     mbarrier.
 // Every wait is bounded in time as in the single-SM kernels; the pair meets
 // at cluster barriers only at the start (mbarriers initialised) and at the
 // end (before the TMEM of both is released).
@@ -53,19 +57,30 @@ namespace pr {
 
 constexpr int PM = 256, PN = 256;  // C tile of a pair
 constexpr int HM = 128, HN = 128;  // this CTA's rows of A, columns of B
-constexpr int OP_STAGES = 3, RAW_SLOTS = 4;
+constexpr int OP_STAGES = 3, RAW_SLOTS = 3;
 constexpr int B_HALF = HN * BK * 4;   // 16 KB: one of B hi / B lo, or raw B
 constexpr int A_RAW = HM * BK * 4;    // 16 KB
 constexpr int OP_STAGE = 2 * B_HALF;  // hi | lo
 constexpr int SLOT = A_RAW + B_HALF;  // raw A | raw B
 constexpr int RAW0 = OP_STAGES * OP_STAGE;
-constexpr int BAR_OFFSET = RAW0 + RAW_SLOTS * SLOT;
+// C staging: per epilogue warp two 32 x 32 fp32 chunks (128-byte swizzled
+// rows) that TMA stores or reduce-adds into C.
+constexpr int C_CHUNK = 32 * 32 * 4;
+constexpr int C_STAGE0 = RAW0 + RAW_SLOTS * SLOT;
+// Converters: two groups of 8 warps taking alternate k-blocks (one group's
+// chain of waits, loads, stores and arrivals takes longer than one k-block
+// of MMA, so one group alone would hold the tensor pipe back).
+constexpr int GROUP_WARPS = 8, CONV_GROUPS = 2, CONV_WARPS = GROUP_WARPS * CONV_GROUPS, EPI_WARPS = 4;
+constexpr int CONV_THREADS = 32 * GROUP_WARPS;  // threads converting one k-block
+constexpr int EPI_WARP0 = 2 + CONV_WARPS;
+// A second TMA issuer: a warp keeps only about one box in processing at a
+// time (measured on GB300: ~0.4 us per box of 16-64 KB, whatever the ring
+// depth), so A and B come from separate warps.
+constexpr int TMA_B_WARP = EPI_WARP0 + EPI_WARPS;
+constexpr int THREADS = 32 * (TMA_B_WARP + 1);
+constexpr int BAR_OFFSET = C_STAGE0 + EPI_WARPS * 2 * C_CHUNK;
 constexpr int PBAR_BYTES = 256;
 constexpr int SMEM_BYTES = BAR_OFFSET + PBAR_BYTES + 1024;
-constexpr int CONV_WARPS = 8, EPI_WARPS = 8;
-constexpr int CONV_THREADS = 32 * CONV_WARPS;
-constexpr int EPI_WARP0 = 2 + CONV_WARPS;
-constexpr int THREADS = 32 * (EPI_WARP0 + EPI_WARPS);
 constexpr uint32_t TMEM_A = PN;  // A stages after the 256-column accumulator
 // Instruction descriptor: D fp32, A and B tf32, both K-major, N = 256, M = 256.
 constexpr uint32_t kIdesc2 = (1u << 4) | (2u << 7) | (2u << 10) | (static_cast<uint32_t>(PN >> 3) << 17) |
@@ -122,9 +137,52 @@ __device__ __forceinline__ void tc_commit2(uint32_t bar) {
         : "memory");
 }
 
+// Fused-epilogue values of 16 accumulator columns (chunk columns base ..
+// base + 15) written to the staging row of this lane: ACT(alpha * v + bias),
+// the bias per row (bl) or per column (lane (base + j)'s bl, by shuffle).
+template <int ACT>
+__device__ __forceinline__ void stage16_ep(uint32_t buf, int lane, int base, float alpha, bool col_bias, float bl,
+                                           const float (&v)[16]) {
+#pragma unroll
+    for (int j = 0; j < 16; j += 4) {
+        float b[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) b[t] = col_bias ? __shfl_sync(0xffffffffu, bl, base + j + t) : bl;
+        st_shared_v4(buf + sw128_offset(lane, (base + j) >> 2), activate(alpha * v[j] + b[0], ACT),
+                     activate(alpha * v[j + 1] + b[1], ACT), activate(alpha * v[j + 2] + b[2], ACT),
+                     activate(alpha * v[j + 3] + b[3], ACT));
+    }
+}
+
+__device__ __forceinline__ void stage16_fused(int act, uint32_t buf, int lane, int base, float alpha, bool col_bias,
+                                              float bl, const float (&v)[16]) {
+    switch (act) {
+        case SGEMM_ACT_RELU: stage16_ep<SGEMM_ACT_RELU>(buf, lane, base, alpha, col_bias, bl, v); break;
+        case SGEMM_ACT_GELU: stage16_ep<SGEMM_ACT_GELU>(buf, lane, base, alpha, col_bias, bl, v); break;
+        case SGEMM_ACT_SILU: stage16_ep<SGEMM_ACT_SILU>(buf, lane, base, alpha, col_bias, bl, v); break;
+        default: stage16_ep<SGEMM_ACT_NONE>(buf, lane, base, alpha, col_bias, bl, v); break;
+    }
+}
+
+// A chunk that crosses the last row or column of C: per-thread stores, and
+// on the tile's last chunk the accumulator release (one lane per warp, on
+// the even CTA's barrier acc_empty). Out of line: it is rare, and inlined it
+// would compete for registers with the interior path.
+template <bool VEC_C>
+__device__ __noinline__ void edge_chunk(const Args &a, uint32_t taddr, float *crow, int64_t row, int64_t col0,
+                                        bool atomic, bool last, uint32_t acc_empty) {
+    const int lane = static_cast<int>(threadIdx.x & 31);
+    epilogue_chunk_then<VEC_C>(a, taddr, crow, row, col0, atomic, last, [&] {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_at(acc_empty, 0);
+    });
+}
+
 template <bool VEC_C>
 __global__ void __launch_bounds__(pr::THREADS, 1)
-    tf32x3_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const Args a) {
+    tf32x3_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                       const __grid_constant__ CUtensorMap tmC, const Args a) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -140,11 +198,11 @@ __global__ void __launch_bounds__(pr::THREADS, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < pr::RAW_SLOTS; ++s) {
-            mbar_init(bar(pr::RAW_FULL + s), 1);
+            mbar_init(bar(pr::RAW_FULL + s), 2);  // one expect_tx arrival per TMA issuer
             mbar_init(bar(pr::RAW_FREE + s), pr::CONV_THREADS);
         }
         for (int s = 0; s < pr::OP_STAGES; ++s) {
-            mbar_init(bar(pr::OP_FULL + s), 2 * pr::CONV_WARPS);  // one lane per converter warp of both CTAs
+            mbar_init(bar(pr::OP_FULL + s), 2 * pr::GROUP_WARPS);  // one lane per converter warp of both CTAs
             mbar_init(bar(pr::OP_EMPTY + s), 1);
         }
         mbar_init(bar(pr::ACC_FULL), 1);
@@ -204,9 +262,10 @@ __global__ void __launch_bounds__(pr::THREADS, 1)
                 }
             }
         }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ TMA issuer
+    } else if (warp == 1 || warp == pr::TMA_B_WARP) {
+        // ---------------------------------------------------- TMA issuers (A, B)
         if (lane == 0) {
+            const bool is_a = warp == 1;
             uint32_t it = 0;
             bool ok = true;
             for_each_unit_of(a, abort_flag, pair, pairs, [&](int tile, int kb, int ke) {
@@ -223,24 +282,31 @@ __global__ void __launch_bounds__(pr::THREADS, 1)
                         return;
                     }
                     const uint32_t sl = base + pr::RAW0 + static_cast<uint32_t>(slot * pr::SLOT);
-                    mbar_arrive_expect_tx(bar(pr::RAW_FULL + slot), pr::SLOT);
-                    tma_load_3d(sl, &tmA, kblk * BK, m0, za, bar(pr::RAW_FULL + slot));
-                    tma_load_3d(sl + pr::A_RAW, &tmB, n0, kblk * BK, zb, bar(pr::RAW_FULL + slot));
+                    if (is_a) {
+                        mbar_arrive_expect_tx(bar(pr::RAW_FULL + slot), pr::A_RAW);
+                        tma_load_3d(sl, &tmA, kblk * BK, m0, za, bar(pr::RAW_FULL + slot));
+                    } else {
+                        mbar_arrive_expect_tx(bar(pr::RAW_FULL + slot), pr::B_HALF);
+                        tma_load_3d(sl + pr::A_RAW, &tmB, n0, kblk * BK, zb, bar(pr::RAW_FULL + slot));
+                    }
                 }
             });
         }
     } else if (warp < pr::EPI_WARP0) {
         // ------------------------------------------------------------ converters
-        const int ct = threadIdx.x - 64;
+        const int cw = warp - 2;                            // 0 .. 15
+        const uint32_t group = static_cast<uint32_t>(cw >> 3);  // k-blocks with it % 2 == group
+        const int ct = threadIdx.x - 64 - 256 * static_cast<int>(group);
         const int l = ct & 7, tb = ct >> 3;                 // 32 groups of eight lanes
         const int g = (tb >> 3) * 8 + l, c = (l + tb) & 7;  // this thread's 4 x 4 B block
-        const int q = warp & 3, part = (warp - 2) >> 2;     // TMEM lane quarter, k-columns 16*part..+15
+        const int q = warp & 3, part = (cw >> 2) & 1;       // TMEM lane quarter, k-columns 16*part..+15
         const int arow = 32 * q + lane;                     // A row this thread converts
         uint32_t it = 0;
         bool ok = true;
         for_each_unit_of(a, abort_flag, pair, pairs, [&](int, int kb, int ke) {
             if (!ok) return;
             for (int kblk = kb; kblk < ke; ++kblk, ++it) {
+                if ((it & 1) != group) continue;
                 const int slot = static_cast<int>(it % pr::RAW_SLOTS);
                 const int s = static_cast<int>(it % pr::OP_STAGES);
                 if (!mbar_wait(bar(pr::RAW_FULL + slot), (it / pr::RAW_SLOTS) & 1, a, abort_flag, WD_PRODUCER)) {
@@ -276,18 +342,22 @@ __global__ void __launch_bounds__(pr::THREADS, 1)
                 split_store(st + off, st + pr::B_HALF + off, bq[0].z, bq[1].z, bq[2].z, bq[3].z);
                 off = sw128_offset(4 * g + 3, c);
                 split_store(st + off, st + pr::B_HALF + off, bq[0].w, bq[1].w, bq[2].w, bq[3].w);
-                float hi[16], lo[16];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    split_tf32(av[j].x, hi[4 * j], lo[4 * j]);
-                    split_tf32(av[j].y, hi[4 * j + 1], lo[4 * j + 1]);
-                    split_tf32(av[j].z, hi[4 * j + 2], lo[4 * j + 2]);
-                    split_tf32(av[j].w, hi[4 * j + 3], lo[4 * j + 3]);
-                }
                 const uint32_t ta = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + pr::TMEM_A +
                                     static_cast<uint32_t>(64 * s + 16 * part);
-                tmem_store16(ta, hi);
-                tmem_store16(ta + 32, lo);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {  // 8 values at a time: fewer live registers
+                    float hi[8], lo[8];
+                    split_tf32(av[2 * h].x, hi[0], lo[0]);
+                    split_tf32(av[2 * h].y, hi[1], lo[1]);
+                    split_tf32(av[2 * h].z, hi[2], lo[2]);
+                    split_tf32(av[2 * h].w, hi[3], lo[3]);
+                    split_tf32(av[2 * h + 1].x, hi[4], lo[4]);
+                    split_tf32(av[2 * h + 1].y, hi[5], lo[5]);
+                    split_tf32(av[2 * h + 1].z, hi[6], lo[6]);
+                    split_tf32(av[2 * h + 1].w, hi[7], lo[7]);
+                    tmem_store8(ta + 8 * h, hi);
+                    tmem_store8(ta + 32 + 8 * h, lo);
+                }
                 tmem_wait_st();
                 fence_proxy_async_smem();
                 tc_fence_before();
@@ -297,32 +367,88 @@ __global__ void __launch_bounds__(pr::THREADS, 1)
         });
     } else {
         // -------------------------------------------------------------- epilogue
-        const int q = warp & 3;                      // TMEM lane quarter this warp may access
-        const int half = (warp - pr::EPI_WARP0) >> 2;  // accumulator columns 128*half .. +127
-        uint32_t unit = 0;
+        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        const uint32_t stage0 = base + pr::C_STAGE0 + static_cast<uint32_t>((warp - pr::EPI_WARP0) * 2 * pr::C_CHUNK);
+        uint32_t unit = 0, nchunk = 0;
+        auto release = [&] {
+            // The accumulator is out of TMEM: one lane per warp frees it on the
+            // even CTA's barrier.
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_at(bar(pr::ACC_EMPTY), 0);
+        };
         for_each_unit_of(a, abort_flag, pair, pairs, [&](int tile, int kb, int ke) {
             if (!mbar_wait<true>(bar(pr::ACC_FULL), unit & 1, a, abort_flag, WD_EPILOGUE)) return;
             tc_fence_after();
             const TileAt at = tile_at<pr::PM, pr::PN>(a, tile);
-            const int64_t row = at.m0 + pr::HM * static_cast<int64_t>(rank) + q * 32 + lane;
+            const int64_t row0 = at.m0 + pr::HM * static_cast<int64_t>(rank) + q * 32;
+            const int64_t row = row0 + lane;
             // Stream-K tiles hold beta * C + bias already: every unit adds.
             const bool atomic = tile >= a.dp_tiles;
-            float *crow = a.C + at.item * a.strideC + row * a.ldc;
+            if (a.c_tma) {
+                // Each 32 x 32 chunk inside the matrix: TMEM -> registers ->
+                // (epilogue) -> swizzled staging rows -> one TMA store (or
+                // reduce-add) of the chunk. Chunks that cross the last row or
+                // column use the per-thread stores.
+                const bool fused = a.ep && !atomic;
+                const bool col_bias = a.bias_kind == SGEMM_BIAS_PER_COL;
+                const float alpha = a.alpha;
+                const float rb = (a.bias_kind == SGEMM_BIAS_PER_ROW && row < a.M) ? __ldg(a.bias + row) : 0.0f;
+                float *crow = a.C + at.item * a.strideC + row * a.ldc;
 #pragma unroll 1
-            for (int cc = 0; cc < 4; ++cc) {
-                const int ch = 4 * half + cc;
-                epilogue_chunk_then<VEC_C>(
-                    a, tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(ch * 32), crow, row,
-                    at.n0 + ch * 32, atomic, cc == 3, [&] {
-                        // This warp's columns are out of TMEM: one lane frees them on
-                        // the even CTA's accumulator barrier.
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive_at(bar(pr::ACC_EMPTY), 0);
-                    });
+                for (int ch = 0; ch < pr::PN / 32; ++ch) {
+                    const uint32_t taddr =
+                        tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(ch * 32);
+                    const int64_t col0 = at.n0 + ch * 32;
+                    const bool last = ch == pr::PN / 32 - 1;
+                    if (col0 + 32 > a.N || row0 + 32 > a.M) {
+                        edge_chunk<VEC_C>(a, taddr, crow, row, col0, atomic, last, bar(pr::ACC_EMPTY));
+                        continue;
+                    }
+                    const uint32_t buf = stage0 + (nchunk & 1) * pr::C_CHUNK;
+                    ++nchunk;
+                    // Per-column bias of this chunk: lane l holds column col0 + l.
+                    const float bl = (fused && col_bias) ? __ldg(a.bias + col0 + lane) : rb;
+                    if (lane == 0) bulk_wait_read<1>();  // the store two chunks back has read this buffer
+                    __syncwarp();
+                    if (fused) {
+                        float v[16];
+                        tmem_load16(taddr, v);
+                        stage16_fused(a.act, buf, lane, 0, alpha, col_bias, bl, v);
+                        tmem_load16(taddr + 16, v);
+                        if (last) release();
+                        stage16_fused(a.act, buf, lane, 16, alpha, col_bias, bl, v);
+                    } else {
+                        float v[32];
+                        tmem_load32(taddr, v);
+                        if (last) release();
+#pragma unroll
+                        for (int j = 0; j < 32; j += 4)
+                            st_shared_v4(buf + sw128_offset(lane, j >> 2), alpha * v[j], alpha * v[j + 1],
+                                         alpha * v[j + 2], alpha * v[j + 3]);
+                    }
+                    fence_proxy_async_smem();  // staging writes -> visible to the TMA engine
+                    __syncwarp();
+                    if (lane == 0) {
+                        const int x = static_cast<int>(col0), y = static_cast<int>(row0);
+                        if (atomic)
+                            tma_reduce_add_3d(&tmC, x, y, at.item, buf);
+                        else
+                            tma_store_3d(&tmC, x, y, at.item, buf);
+                        bulk_commit();
+                    }
+                }
+            } else {
+                float *crow = a.C + at.item * a.strideC + row * a.ldc;
+#pragma unroll 1
+                for (int ch = 0; ch < pr::PN / 32; ++ch)
+                    epilogue_chunk_then<VEC_C>(
+                        a, tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(ch * 32), crow,
+                        row, at.n0 + ch * 32, atomic, ch == pr::PN / 32 - 1, release);
             }
             ++unit;
         });
+        if (lane == 0) bulk_wait<0>();  // every store of this warp has landed
     }
 
     // The odd CTA's TMEM is written by the even CTA's MMAs: wait for them to
@@ -383,10 +509,15 @@ int launch_pair(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStream
     }
     int *flag = watchdog_flag_device_ptr();
     if (!flag) return SGEMM_ERR_LAUNCH;
-    alignas(64) CUtensorMap mapA, mapB;
+    alignas(64) CUtensorMap mapA, mapB, mapC;
     if (!encode_map(&mapA, p.A, p.M, p.K, p.lda, p.batch, p.strideA, BK, pr::HM, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_map(&mapB, p.B, p.K, p.N, p.ldb, p.batch, p.strideB, pr::HN, BK, CU_TENSOR_MAP_SWIZZLE_NONE))
         return SGEMM_ERR_LAUNCH;
+    // C through TMA when its rows allow 16-byte aligned boxes and C is not
+    // read (beta = 0; split tiles are reduce-added either way).
+    const bool c_tma = VEC_C && p.beta == 0.0f &&
+                       encode_map(&mapC, p.C, p.M, p.N, p.ldc, p.batch, p.strideC, 32, 32, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (!c_tma) mapC = mapA;  // not read by the kernel
 
     const int64_t tiles_m = (p.M + pr::PM - 1) / pr::PM, tiles_n = (p.N + pr::PN - 1) / pr::PN;
     const int64_t k_blocks = (p.K + BK - 1) / BK;
@@ -424,8 +555,9 @@ int launch_pair(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStream
     a.bias_kind = p.bias_kind;
     a.act = p.act;
     a.ep = p.has_epilogue();
+    a.c_tma = c_tma ? 1 : 0;
     cfg.gridDim = dim3(2 * sch.grid);
-    if (cudaLaunchKernelEx(&cfg, kernel, mapA, mapB, a) != cudaSuccess) {
+    if (cudaLaunchKernelEx(&cfg, kernel, mapA, mapB, mapC, a) != cudaSuccess) {
         cudaGetLastError();
         return SGEMM_ERR_LAUNCH;
     }

@@ -46,6 +46,7 @@ SGEMM_TUNE_FFMA_TILE = 1
 SGEMM_TUNE_STREAM_K = 2
 SGEMM_TUNE_WATCHDOG_MS = 3
 SGEMM_TUNE_TF32X3_KERNEL = 4
+SGEMM_TUNE_LAST_TC_KERNEL = 5
 
 # Every symbol that include/sgemm.h declares, with its ctypes signature.
 _i64, _int, _vp, _cp = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_char_p

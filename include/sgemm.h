@@ -232,13 +232,17 @@ int sgemm_watchdog_selftest(int64_t wait_ms, sgemm_stream_t stream);
  *                            3 = stream-K over all tiles
  *   SGEMM_TUNE_WATCHDOG_MS   milliseconds a bounded wait polls before it gives
  *                            up (1 .. 60000; default 2000)
- *   SGEMM_TUNE_TF32X3_KERNEL  tensor-core kernel for operands whose base
- *                            addresses and row strides are 16-byte aligned:
- *                            0 = per-thread loads, 1 = TMA, 2 = TMA with A's
- *                            operands in tensor memory (default), 3 = the
- *                            SM-pair kernel (tcgen05 cta_group::2, clusters of
- *                            two CTAs; op(A) = A, op(B) = B only, the
- *                            transposed forms keep kernel 2)
+ *   SGEMM_TUNE_TF32X3_KERNEL  tensor-core kernel: 0 = automatic (default):
+ *                            the SM-pair kernel for op(A) = A, op(B) = B with
+ *                            16-byte aligned bases and row strides, M and N
+ *                            >= 256 and at least 2^31 multiply-adds, else the
+ *                            TMA kernel with A in tensor memory where the
+ *                            rows are 16-byte aligned, else per-thread loads;
+ *                            1 = per-thread loads, 2 = TMA, 3 = TMA with A's
+ *                            operands in tensor memory, 4 = SM pairs (tcgen05
+ *                            cta_group::2 on clusters of two CTAs). Kernels
+ *                            2-4 need 16-byte aligned rows (else kernel 1
+ *                            runs); the transposed forms always take kernel 3.
  * Returns SGEMM_OK or SGEMM_ERR_INVALID_ARG. sgemm_get_tuning returns the
  * value, or -1 for an unknown key.
  */
@@ -246,7 +250,9 @@ enum sgemm_tuning_key {
     SGEMM_TUNE_FFMA_TILE = 1,
     SGEMM_TUNE_STREAM_K = 2,
     SGEMM_TUNE_WATCHDOG_MS = 3,
-    SGEMM_TUNE_TF32X3_KERNEL = 4
+    SGEMM_TUNE_TF32X3_KERNEL = 4,
+    SGEMM_TUNE_LAST_TC_KERNEL = 5  /* read only: the tensor-core kernel (1-4) the
+                                      last SGEMM_TF32X3 call on this process ran */
 };
 int sgemm_set_tuning(int key, int64_t value);
 int64_t sgemm_get_tuning(int key);

@@ -24,7 +24,7 @@ def lib():
     sgemm.set_variant(0)
     sgemm.set_tuning(sgemm.SGEMM_TUNE_FFMA_TILE, 0)
     sgemm.set_tuning(sgemm.SGEMM_TUNE_STREAM_K, 0)
-    sgemm.set_tuning(sgemm.SGEMM_TUNE_TF32X3_KERNEL, 2)
+    sgemm.set_tuning(sgemm.SGEMM_TUNE_TF32X3_KERNEL, 0)
 
 
 def _stored(M, N, K, transA, transB, dist, seed):

@@ -17,14 +17,14 @@ from tests.gpu_harness import TOL, outside_box_intact, oracle_error, run_sgemm, 
 pytestmark = pytest.mark.gpu
 
 # (variant, ffma tile, stream-K mode, tensor-core kernel) settings every
-# small-shape test runs under. Tensor-core kernels: 0 = per-thread loads,
-# 1 = TMA, 2 = TMA with A in tensor memory (default), 3 = SM pairs.
+# small-shape test runs under. Tensor-core kernels: 0 = automatic,
+# 1 = per-thread loads, 2 = TMA, 3 = TMA with A in tensor memory, 4 = SM pairs.
 SETTINGS = [
-    ("auto", 0, 0, 2),
-    ("ffma", 1, 1, 2), ("ffma", 1, 3, 2), ("ffma", 2, 2, 2), ("ffma", 3, 0, 2), ("ffma", 2, 3, 2),
-    ("tf32x3", 0, 0, 2), ("tf32x3", 0, 1, 2), ("tf32x3", 0, 3, 2),
-    ("tf32x3", 0, 0, 1), ("tf32x3", 0, 3, 1), ("tf32x3", 0, 0, 0), ("tf32x3", 0, 3, 0),
-    ("tf32x3", 0, 0, 3), ("tf32x3", 0, 1, 3), ("tf32x3", 0, 3, 3),
+    ("auto", 0, 0, 0),
+    ("ffma", 1, 1, 0), ("ffma", 1, 3, 0), ("ffma", 2, 2, 0), ("ffma", 3, 0, 0), ("ffma", 2, 3, 0),
+    ("tf32x3", 0, 0, 0), ("tf32x3", 0, 0, 3), ("tf32x3", 0, 1, 3), ("tf32x3", 0, 3, 3),
+    ("tf32x3", 0, 0, 2), ("tf32x3", 0, 3, 2), ("tf32x3", 0, 0, 1), ("tf32x3", 0, 3, 1),
+    ("tf32x3", 0, 0, 4), ("tf32x3", 0, 1, 4), ("tf32x3", 0, 3, 4),
 ]
 SETTING_IDS = [f"{s[0]}-t{s[1]}-sk{s[2]}-k{s[3]}" for s in SETTINGS]
 
@@ -40,12 +40,12 @@ def lib():
     sgemm.set_variant(0)
     sgemm.set_tuning(sgemm.SGEMM_TUNE_FFMA_TILE, 0)
     sgemm.set_tuning(sgemm.SGEMM_TUNE_STREAM_K, 0)
-    sgemm.set_tuning(sgemm.SGEMM_TUNE_TF32X3_KERNEL, 2)
+    sgemm.set_tuning(sgemm.SGEMM_TUNE_TF32X3_KERNEL, 0)
 
 
 def _apply(lib, setting):
     variant, tile, sk = setting[:3]
-    tc = setting[3] if len(setting) > 3 else 2
+    tc = setting[3] if len(setting) > 3 else 0
     lib.set_variant(variant)
     lib.set_tuning(lib.SGEMM_TUNE_FFMA_TILE, tile)
     lib.set_tuning(lib.SGEMM_TUNE_STREAM_K, sk)
@@ -170,8 +170,8 @@ def _config_error(C, A, B, w):
 
 
 @pytest.mark.parametrize("w", wl.ALL, ids=lambda w: w.name)
-@pytest.mark.parametrize("variant,tc", [("auto", 2), ("ffma", 2), ("tf32x3", 2), ("tf32x3", 1), ("tf32x3", 0),
-                                        ("tf32x3", 3)])
+@pytest.mark.parametrize("variant,tc", [("auto", 0), ("ffma", 0), ("tf32x3", 3), ("tf32x3", 2), ("tf32x3", 1),
+                                        ("tf32x3", 4)])
 def test_benchmark_configs(lib, w, variant, tc):
     _apply(lib, (variant, 0, 0, tc))
     A, B = wl.make_inputs(w)
