@@ -61,6 +61,11 @@ using namespace ffma;
 __global__ void tile_pass_kernel(float *C, int64_t M, int64_t N, int64_t ldc, int64_t strideC, float beta,
                                  const float *bias, int bias_kind, int act, int bm, int bn, int tiles_n,
                                  int tiles_per_item, int first_tile) {
+    // Launched behind a product (the activation pass) this waits for it; the
+    // product launched behind this pass (the beta pre-pass) may start its
+    // main loop at once and waits only before it writes C.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;");
     const int tile = first_tile + blockIdx.y;
     const int item = tile / tiles_per_item, rest = tile % tiles_per_item;
     C += item * strideC;

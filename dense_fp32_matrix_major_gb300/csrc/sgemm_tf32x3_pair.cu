@@ -369,6 +369,9 @@ __global__ void __launch_bounds__(pr::THREADS, 1)
         // -------------------------------------------------------------- epilogue
         const int q = warp & 3;  // TMEM lane quarter this warp may access
         const uint32_t stage0 = base + pr::C_STAGE0 + static_cast<uint32_t>((warp - pr::EPI_WARP0) * 2 * pr::C_CHUNK);
+        // C may still be in the beta pre-pass launched just before this
+        // kernel (programmatic dependent launch): only the epilogue waits.
+        asm volatile("griddepcontrol.wait;" ::: "memory");
         uint32_t unit = 0, nchunk = 0;
         auto release = [&] {
             // The accumulator is out of TMEM: one lane per warp frees it on the
@@ -480,11 +483,13 @@ template <bool VEC_C>
 int launch_pair(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStream_t stream, int *launches) {
     auto kernel = tf32x3_pair_kernel<VEC_C>;
     constexpr int idx = VEC_C ? 1 : 0;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg{};
     cfg.blockDim = dim3(pr::THREADS);
     cfg.dynamicSmemBytes = pr::SMEM_BYTES;
@@ -557,6 +562,10 @@ int launch_pair(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStream
     a.ep = p.has_epilogue();
     a.c_tma = c_tma ? 1 : 0;
     cfg.gridDim = dim3(2 * sch.grid);
+    // Behind our own beta pre-pass (which touches only C, and which started
+    // after everything before it in the stream had finished) the main loop
+    // may overlap it; the epilogue waits for it (griddepcontrol.wait).
+    cfg.numAttrs = split > 0 ? 2 : 1;
     if (cudaLaunchKernelEx(&cfg, kernel, mapA, mapB, mapC, a) != cudaSuccess) {
         cudaGetLastError();
         return SGEMM_ERR_LAUNCH;
