@@ -1147,11 +1147,11 @@ int tf32x3_launch(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStre
     if (tma_ok(p) && mode != 1) {
         // Automatic: the SM-pair kernel where its 256 x 256 tiles are filled
         // and the product is large enough for its shorter per-SM operand
-        // traffic to pay (measured on GB300: from about 2^31 multiply-adds
-        // on; below that the single-SM kernel's smaller tiles win).
+        // traffic to pay (measured on GB300: faster from 1024^3 = 2^30
+        // multiply-adds on, even at 512^3).
         const double work = static_cast<double>(p.M) * static_cast<double>(p.N) * static_cast<double>(p.K) *
                             static_cast<double>(p.batch);
-        const bool pair = mode == 4 || (mode == 0 && p.M >= 256 && p.N >= 256 && work >= 2147483648.0);
+        const bool pair = mode == 4 || (mode == 0 && p.M >= 256 && p.N >= 256 && work >= 1073741824.0);
         if (pair) {
             g_last_tc_kernel.store(4);
             return tf32x3_pair_launch(p, dev, sk_mode, stream, launches);

@@ -19,21 +19,24 @@
 // Roles in each CTA (23 warps):
 //   * warp 0: in the even CTA, one thread issues the pair's MMAs (4 k-slices
 //     x 3 products per k-block, lo*hi + hi*lo + hi*hi) and commits them to
-//     the mbarriers of both CTAs (multicast); idle in the odd CTA.
+//     the mbarriers of both CTAs (multicast); in the odd CTA, one thread
+//     forwards "stage filled" to the even CTA (one cluster-scope arrival per
+//     k-block instead of one per converter warp).
 //   * warps 1 and 22: TMA of this CTA's A rows (128 x 32, 128-byte swizzled)
-//     and B columns (32 x 128, unswizzled) into a 4-slot raw ring.
+//     and B columns (32 x 128, unswizzled) into a 2-slot raw ring.
 //   * warps 2-17 (converters, two groups of 8 taking alternate k-blocks):
 //     split A into hi / lo and write them to this CTA's TMEM (the A
 //     operand), transpose and split B into K-major, 128-byte-swizzled hi / lo
-//     tiles in a 3-stage shared ring, then one lane per warp arrives on the
-//     even CTA's stage-full mbarrier.
+//     tiles in a 4-stage shared ring, then one lane per warp arrives on a
+//     local mbarrier (the even CTA's stage-full barrier, or the odd CTA's
+//     forwarding barrier).
 //   * warps 18-21 (epilogue): one per TMEM lane quarter, reading the
 //     accumulator's 256 columns for its 32 rows in 32 x 32 chunks, each
 //     staged in shared memory and written by one TMA bulk store (or bulk
 //     reduce-add for tiles split along K); chunks crossing the last row or
-//     column, C that TMA cannot address, or beta != 0 take per-thread stores. After the last chunk's
-//     TMEM load one lane per warp frees the accumulator on the even CTA's
-//     mbarrier.
+//     column, C that TMA cannot address, or beta != 0 take per-thread
+//     stores. After the last chunk's TMEM load one lane per warp frees the
+//     accumulator on the even CTA's mbarrier.
 // Every wait is bounded in time as in the single-SM kernels; the pair meets
 // at cluster barriers only at the start (mbarriers initialised) and at the
 // end (before the TMEM of both is released).
@@ -57,7 +60,10 @@ namespace pr {
 
 constexpr int PM = 256, PN = 256;  // C tile of a pair
 constexpr int HM = 128, HN = 128;  // this CTA's rows of A, columns of B
-constexpr int OP_STAGES = 3, RAW_SLOTS = 3;
+// Four operand stages: a stage is refilled only after the MMAs that read it
+// have completed, and completions trail issue by the tensor pipe's queue,
+// so three stages left the MMA issuer waiting ~480 cycles per k-block.
+constexpr int OP_STAGES = 4, RAW_SLOTS = 2;
 constexpr int B_HALF = HN * BK * 4;   // 16 KB: one of B hi / B lo, or raw B
 constexpr int A_RAW = HM * BK * 4;    // 16 KB
 constexpr int OP_STAGE = 2 * B_HALF;  // hi | lo
@@ -88,7 +94,7 @@ constexpr uint32_t kIdesc2 = (1u << 4) | (2u << 7) | (2u << 10) | (static_cast<u
 // mbarrier indices
 constexpr int RAW_FULL = 0, RAW_FREE = RAW_FULL + RAW_SLOTS, OP_FULL = RAW_FREE + RAW_SLOTS,
               OP_EMPTY = OP_FULL + OP_STAGES, ACC_FULL = OP_EMPTY + OP_STAGES, ACC_EMPTY = ACC_FULL + 1,
-              DRAIN = ACC_EMPTY + 1, NBARS = DRAIN + 1;
+              DRAIN = ACC_EMPTY + 1, OP_FWD = DRAIN + 1, NBARS = OP_FWD + OP_STAGES;
 static_assert(NBARS * 8 + 16 <= PBAR_BYTES, "barrier block");
 static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
 static_assert(TMEM_A + OP_STAGES * 64 <= TMEM_COLS, "TMEM columns");
@@ -199,10 +205,14 @@ __global__ void __launch_bounds__(pr::THREADS, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < pr::RAW_SLOTS; ++s) {
             mbar_init(bar(pr::RAW_FULL + s), 2);  // one expect_tx arrival per TMA issuer
-            mbar_init(bar(pr::RAW_FREE + s), pr::CONV_THREADS);
+            mbar_init(bar(pr::RAW_FREE + s), pr::GROUP_WARPS);  // one lane per converter warp
         }
         for (int s = 0; s < pr::OP_STAGES; ++s) {
-            mbar_init(bar(pr::OP_FULL + s), 2 * pr::GROUP_WARPS);  // one lane per converter warp of both CTAs
+            // Even CTA: its own converter warps plus one forwarded arrival for
+            // the odd CTA's warps (OP_FWD there), so the converters never pay
+            // a cluster-scope release.
+            mbar_init(bar(pr::OP_FULL + s), pr::GROUP_WARPS + 1);
+            mbar_init(bar(pr::OP_FWD + s), pr::GROUP_WARPS);
             mbar_init(bar(pr::OP_EMPTY + s), 1);
         }
         mbar_init(bar(pr::ACC_FULL), 1);
@@ -261,6 +271,22 @@ __global__ void __launch_bounds__(pr::THREADS, 1)
                 while (!mbar_try_wait(bar(pr::DRAIN), 0) && global_timer() - t0 < a.timeout_ns) {
                 }
             }
+        }
+        if (rank != 0 && lane == 0) {
+            // Forwarder: once this CTA's converters have filled stage s, one
+            // cluster-scope arrival tells the even CTA's MMA issuer.
+            uint32_t it = 0;
+            bool ok = true;
+            for_each_unit_of(a, abort_flag, pair, pairs, [&](int, int kb, int ke) {
+                for (int kblk = kb; kblk < ke && ok; ++kblk, ++it) {
+                    const int s = static_cast<int>(it % pr::OP_STAGES);
+                    if (!mbar_wait(bar(pr::OP_FWD + s), (it / pr::OP_STAGES) & 1, a, abort_flag, WD_PRODUCER)) {
+                        ok = false;
+                        return;
+                    }
+                    mbar_arrive_at(bar(pr::OP_FULL + s), 0);
+                }
+            });
         }
     } else if (warp == 1 || warp == pr::TMA_B_WARP) {
         // ---------------------------------------------------- TMA issuers (A, B)
@@ -324,8 +350,9 @@ __global__ void __launch_bounds__(pr::THREADS, 1)
                 for (int qq = 0; qq < 4; ++qq)
                     bq[qq] = ld_shared_v4(sl + pr::A_RAW + static_cast<uint32_t>((4 * c + qq) * pr::HN * 4 + g * 16));
                 fence_proxy_async_smem();  // order these loads before the next TMA into the slot
-                mbar_arrive(bar(pr::RAW_FREE + slot));
-                // The stage is free once the pair's MMAs three k-blocks back are done.
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(pr::RAW_FREE + slot));
+                // The stage is free once the pair's MMAs four k-blocks back are done.
                 if (!mbar_wait<true>(bar(pr::OP_EMPTY + s), ((it / pr::OP_STAGES) & 1) ^ 1, a, abort_flag,
                                      WD_PRODUCER)) {
                     ok = false;
@@ -362,7 +389,7 @@ __global__ void __launch_bounds__(pr::THREADS, 1)
                 fence_proxy_async_smem();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive_at(bar(pr::OP_FULL + s), 0);
+                if (lane == 0) mbar_arrive(bar((rank == 0 ? pr::OP_FULL : pr::OP_FWD) + s));
             }
         });
     } else {
