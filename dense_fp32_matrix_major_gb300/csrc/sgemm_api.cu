@@ -276,6 +276,53 @@ int sgemm_f32_batched(int transA, int transB, int64_t M, int64_t N, int64_t K, f
     return sgemm::enqueue(p, reinterpret_cast<cudaStream_t>(stream));
 }
 
+namespace sgemm {
+namespace {
+
+// Streams and events of the pipelined host-buffer product, made once per
+// device on first use and kept for the process; `lock` serialises the
+// enqueueing of pipelined calls on one device (the events are re-recorded
+// by every call).
+constexpr int kMaxPanels = 8;
+struct HostPipe {
+    std::once_flag once;
+    int status = SGEMM_ERR_LAUNCH;
+    cudaStream_t compute = nullptr, d2h = nullptr;
+    cudaEvent_t fork = nullptr, done = nullptr, b_in[kMaxPanels] = {}, c_out[kMaxPanels] = {};
+    std::mutex lock;
+};
+HostPipe g_pipe[kMaxDevices];
+
+HostPipe *host_pipe(int device) {
+    HostPipe &hp = g_pipe[device];
+    std::call_once(hp.once, [&hp] {
+        const unsigned f = cudaEventDisableTiming;
+        bool ok = cudaStreamCreateWithFlags(&hp.compute, cudaStreamNonBlocking) == cudaSuccess &&
+                  cudaStreamCreateWithFlags(&hp.d2h, cudaStreamNonBlocking) == cudaSuccess &&
+                  cudaEventCreateWithFlags(&hp.fork, f) == cudaSuccess &&
+                  cudaEventCreateWithFlags(&hp.done, f) == cudaSuccess;
+        for (int j = 0; ok && j < kMaxPanels; ++j)
+            ok = cudaEventCreateWithFlags(&hp.b_in[j], f) == cudaSuccess &&
+                 cudaEventCreateWithFlags(&hp.c_out[j], f) == cudaSuccess;
+        if (!ok) cudaGetLastError();
+        hp.status = ok ? SGEMM_OK : SGEMM_ERR_LAUNCH;
+    });
+    return hp.status == SGEMM_OK ? &hp : nullptr;
+}
+
+// Width of the column panels of the pipelined host-buffer product, or 0 for
+// one product without panels: panels pay only when the copies are long
+// enough to hide a panel's product behind the next panel's copy.
+int64_t panel_width(int64_t M, int64_t N, int64_t K) {
+    const double work = static_cast<double>(M) * static_cast<double>(N) * static_cast<double>(K);
+    if (N < 512 || work < 1073741824.0) return 0;
+    const int64_t w = ((N + 3) / 4 + 255) / 256 * 256;  // about four panels, 256-column multiples
+    return w < N ? w : 0;
+}
+
+}  // namespace
+}  // namespace sgemm
+
 int sgemm_f32_from_host(int64_t M, int64_t N, int64_t K, const float *A_host, int64_t lda,
                         const float *B_host, int64_t ldb, float *C_host, int64_t ldc, float *dA, float *dB,
                         float *dC, sgemm_stream_t stream) {
@@ -284,15 +331,55 @@ int sgemm_f32_from_host(int64_t M, int64_t N, int64_t K, const float *A_host, in
     if ((M > 0 && K > 0 && !A_host) || (K > 0 && N > 0 && !B_host) || (M > 0 && N > 0 && !C_host))
         return SGEMM_ERR_INVALID_ARG;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (M > 0 && K > 0 && copy_rows(dA, A_host, M, K, lda, cudaMemcpyHostToDevice, s) != cudaSuccess)
-        return cudaGetLastError(), SGEMM_ERR_LAUNCH;
-    if (K > 0 && N > 0 && copy_rows(dB, B_host, K, N, ldb, cudaMemcpyHostToDevice, s) != cudaSuccess)
-        return cudaGetLastError(), SGEMM_ERR_LAUNCH;
-    Problem p{M, N, K, dA, lda, dB, ldb, dC, ldc};
-    rc = sgemm::enqueue(p, s);
-    if (rc != SGEMM_OK) return rc;
-    if (M > 0 && N > 0 && copy_rows(C_host, dC, M, N, ldc, cudaMemcpyDeviceToHost, s) != cudaSuccess)
-        return cudaGetLastError(), SGEMM_ERR_LAUNCH;
+    const int64_t w = (M > 0 && K > 0) ? sgemm::panel_width(M, N, K) : 0;
+    int device = -1;
+    sgemm::HostPipe *hp = nullptr;
+    if (w > 0 && cudaGetDevice(&device) == cudaSuccess && device >= 0 && device < sgemm::kMaxDevices)
+        hp = sgemm::host_pipe(device);
+    cudaGetLastError();
+    if (!hp) {
+        // One product: copies in, product, copy out, all in order on `stream`.
+        if (M > 0 && K > 0 && copy_rows(dA, A_host, M, K, lda, cudaMemcpyHostToDevice, s) != cudaSuccess)
+            return cudaGetLastError(), SGEMM_ERR_LAUNCH;
+        if (K > 0 && N > 0 && copy_rows(dB, B_host, K, N, ldb, cudaMemcpyHostToDevice, s) != cudaSuccess)
+            return cudaGetLastError(), SGEMM_ERR_LAUNCH;
+        Problem p{M, N, K, dA, lda, dB, ldb, dC, ldc};
+        rc = sgemm::enqueue(p, s);
+        if (rc != SGEMM_OK) return rc;
+        if (M > 0 && N > 0 && copy_rows(C_host, dC, M, N, ldc, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+            return cudaGetLastError(), SGEMM_ERR_LAUNCH;
+        return SGEMM_OK;
+    }
+    // Column panels: A, then B panel by panel in on `stream`; panel j's
+    // product on the compute stream once its B panel is in; its C panel out
+    // on the copy-out stream once the product is done. `stream` waits for the
+    // last copy out, so the call keeps the one-stream semantics.
+    std::lock_guard<std::mutex> guard(hp->lock);
+    const size_t f = sizeof(float);
+    const int64_t panels = (N + w - 1) / w;
+    auto fail = [] { return cudaGetLastError(), SGEMM_ERR_LAUNCH; };
+    if (cudaEventRecord(hp->fork, s) != cudaSuccess || cudaStreamWaitEvent(hp->compute, hp->fork, 0) != cudaSuccess ||
+        cudaStreamWaitEvent(hp->d2h, hp->fork, 0) != cudaSuccess)
+        return fail();
+    if (copy_rows(dA, A_host, M, K, lda, cudaMemcpyHostToDevice, s) != cudaSuccess) return fail();
+    for (int64_t j = 0; j < panels; ++j) {
+        const int64_t c0 = j * w, wj = (N - c0 < w) ? N - c0 : w;
+        if (cudaMemcpy2DAsync(dB + c0, ldb * f, B_host + c0, ldb * f, wj * f, K, cudaMemcpyHostToDevice, s) !=
+                cudaSuccess ||
+            cudaEventRecord(hp->b_in[j], s) != cudaSuccess ||
+            cudaStreamWaitEvent(hp->compute, hp->b_in[j], 0) != cudaSuccess)
+            return fail();
+        Problem p{M, wj, K, dA, lda, dB + c0, ldb, dC + c0, ldc};
+        rc = sgemm::enqueue(p, hp->compute);
+        if (rc != SGEMM_OK) return rc;
+        if (cudaEventRecord(hp->c_out[j], hp->compute) != cudaSuccess ||
+            cudaStreamWaitEvent(hp->d2h, hp->c_out[j], 0) != cudaSuccess ||
+            cudaMemcpy2DAsync(C_host + c0, ldc * f, dC + c0, ldc * f, wj * f, M, cudaMemcpyDeviceToHost, hp->d2h) !=
+                cudaSuccess)
+            return fail();
+    }
+    if (cudaEventRecord(hp->done, hp->d2h) != cudaSuccess || cudaStreamWaitEvent(s, hp->done, 0) != cudaSuccess)
+        return fail();
     return SGEMM_OK;
 }
 

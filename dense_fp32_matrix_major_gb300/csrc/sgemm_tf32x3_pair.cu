@@ -77,6 +77,9 @@ constexpr int C_STAGE0 = RAW0 + RAW_SLOTS * SLOT;
 // chain of waits, loads, stores and arrivals takes longer than one k-block
 // of MMA, so one group alone would hold the tensor pipe back).
 constexpr int GROUP_WARPS = 8, CONV_GROUPS = 2, CONV_WARPS = GROUP_WARPS * CONV_GROUPS, EPI_WARPS = 4;
+// Epilogue: EPI_WARPS / 4 warps per TMEM lane quarter, each reading an equal
+// share of the accumulator's 32-column chunks; C_BUFS staging chunks each.
+constexpr int EPI_PER_QUAD = EPI_WARPS / 4, CHUNKS_PER_WARP = (PN / 32) / EPI_PER_QUAD, C_BUFS = 2;
 constexpr int CONV_THREADS = 32 * GROUP_WARPS;  // threads converting one k-block
 constexpr int EPI_WARP0 = 2 + CONV_WARPS;
 // A second TMA issuer: a warp keeps only about one box in processing at a
@@ -84,7 +87,7 @@ constexpr int EPI_WARP0 = 2 + CONV_WARPS;
 // depth), so A and B come from separate warps.
 constexpr int TMA_B_WARP = EPI_WARP0 + EPI_WARPS;
 constexpr int THREADS = 32 * (TMA_B_WARP + 1);
-constexpr int BAR_OFFSET = C_STAGE0 + EPI_WARPS * 2 * C_CHUNK;
+constexpr int BAR_OFFSET = C_STAGE0 + EPI_WARPS * C_BUFS * C_CHUNK;
 constexpr int PBAR_BYTES = 256;
 constexpr int SMEM_BYTES = BAR_OFFSET + PBAR_BYTES + 1024;
 constexpr uint32_t TMEM_A = PN;  // A stages after the 256-column accumulator
@@ -332,7 +335,7 @@ __global__ void __launch_bounds__(pr::THREADS, 1)
         for_each_unit_of(a, abort_flag, pair, pairs, [&](int, int kb, int ke) {
             if (!ok) return;
             for (int kblk = kb; kblk < ke; ++kblk, ++it) {
-                if ((it & 1) != group) continue;
+                if (it % pr::CONV_GROUPS != group) continue;
                 const int slot = static_cast<int>(it % pr::RAW_SLOTS);
                 const int s = static_cast<int>(it % pr::OP_STAGES);
                 if (!mbar_wait(bar(pr::RAW_FULL + slot), (it / pr::RAW_SLOTS) & 1, a, abort_flag, WD_PRODUCER)) {
@@ -395,7 +398,10 @@ __global__ void __launch_bounds__(pr::THREADS, 1)
     } else {
         // -------------------------------------------------------------- epilogue
         const int q = warp & 3;  // TMEM lane quarter this warp may access
-        const uint32_t stage0 = base + pr::C_STAGE0 + static_cast<uint32_t>((warp - pr::EPI_WARP0) * 2 * pr::C_CHUNK);
+        const uint32_t stage0 =
+            base + pr::C_STAGE0 + static_cast<uint32_t>((warp - pr::EPI_WARP0) * pr::C_BUFS * pr::C_CHUNK);
+        const int ch0 = ((warp - pr::EPI_WARP0) >> 2) * pr::CHUNKS_PER_WARP;  // this warp's chunks
+        const int ch_end = ch0 + pr::CHUNKS_PER_WARP;
         // C may still be in the beta pre-pass launched just before this
         // kernel (programmatic dependent launch): only the epilogue waits.
         asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -426,20 +432,20 @@ __global__ void __launch_bounds__(pr::THREADS, 1)
                 const float rb = (a.bias_kind == SGEMM_BIAS_PER_ROW && row < a.M) ? __ldg(a.bias + row) : 0.0f;
                 float *crow = a.C + at.item * a.strideC + row * a.ldc;
 #pragma unroll 1
-                for (int ch = 0; ch < pr::PN / 32; ++ch) {
+                for (int ch = ch0; ch < ch_end; ++ch) {
                     const uint32_t taddr =
                         tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(ch * 32);
                     const int64_t col0 = at.n0 + ch * 32;
-                    const bool last = ch == pr::PN / 32 - 1;
+                    const bool last = ch == ch_end - 1;
                     if (col0 + 32 > a.N || row0 + 32 > a.M) {
                         edge_chunk<VEC_C>(a, taddr, crow, row, col0, atomic, last, bar(pr::ACC_EMPTY));
                         continue;
                     }
-                    const uint32_t buf = stage0 + (nchunk & 1) * pr::C_CHUNK;
+                    const uint32_t buf = stage0 + (nchunk % pr::C_BUFS) * pr::C_CHUNK;
                     ++nchunk;
                     // Per-column bias of this chunk: lane l holds column col0 + l.
                     const float bl = (fused && col_bias) ? __ldg(a.bias + col0 + lane) : rb;
-                    if (lane == 0) bulk_wait_read<1>();  // the store two chunks back has read this buffer
+                    if (lane == 0) bulk_wait_read<pr::C_BUFS - 1>();  // the store C_BUFS chunks back has read this buffer
                     __syncwarp();
                     if (fused) {
                         float v[16];
@@ -471,10 +477,10 @@ __global__ void __launch_bounds__(pr::THREADS, 1)
             } else {
                 float *crow = a.C + at.item * a.strideC + row * a.ldc;
 #pragma unroll 1
-                for (int ch = 0; ch < pr::PN / 32; ++ch)
+                for (int ch = ch0; ch < ch_end; ++ch)
                     epilogue_chunk_then<VEC_C>(
                         a, tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(ch * 32), crow,
-                        row, at.n0 + ch * 32, atomic, ch == pr::PN / 32 - 1, release);
+                        row, at.n0 + ch * 32, atomic, ch == ch_end - 1, release);
             }
             ++unit;
         });

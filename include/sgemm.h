@@ -178,6 +178,16 @@ int sgemm_f32_fused(int transA, int transB, int64_t M, int64_t N, int64_t K, flo
  * Host buffers should be page-locked (cudaHostAlloc) for the copies to be
  * asynchronous; the caller synchronises the stream before reading C_host.
  * Same sizes, strides, errors and results as sgemm_f32.
+ * Products of at least 2^30 multiply-adds with N >= 512 are pipelined over
+ * about four column panels of B and C: A and the B panels are copied in on
+ * `stream`, panel j's product runs on a library stream as soon as its B
+ * panel is in, and its C panel is copied out on a second library stream, so
+ * copies in, products and copies out overlap. `stream` waits for the last
+ * copy out, so the call behaves as if everything ran in order on `stream`.
+ * The two library streams and their events are created on the first
+ * pipelined call on a device and kept for the process (no memory is
+ * allocated); concurrent pipelined calls on one device are serialised while
+ * they enqueue.
  */
 int sgemm_f32_from_host(int64_t M, int64_t N, int64_t K, const float *A_host, int64_t lda,
                         const float *B_host, int64_t ldb, float *C_host, int64_t ldc, float *dA,

@@ -201,6 +201,33 @@ def test_from_host_entry_point(lib):
     assert sampled_error(Ch.numpy(), A, B, r, c) <= TOL
 
 
+@pytest.mark.parametrize("w", [wl.C5_HEAD, wl.C4_2048], ids=lambda w: w.name)
+def test_from_host_pipelined_on_side_stream(lib, w):
+    """Large products go through the column-panel pipeline (library streams);
+    the call on a side stream must still order everything before that
+    stream's later work, and every panel, the last one included, is right."""
+    import torch
+
+    A, B = wl.make_inputs(w)
+    Ah = torch.from_numpy(A).pin_memory()
+    Bh = torch.from_numpy(B).pin_memory()
+    Ch = torch.full((w.M, w.N), float("nan")).pin_memory()
+    dA, dB, dC = (torch.empty_like(t, device="cuda") for t in (Ah, Bh, Ch))
+    lib.set_variant(0)
+    side = torch.cuda.Stream()
+    for _ in range(2):  # a second call reuses the library's streams and events
+        Ch.fill_(float("nan"))
+        lib.sgemm_f32_from_host(Ah, Bh, Ch, dA, dB, dC, stream=side)
+        side.synchronize()
+        C = Ch.numpy()
+        assert np.all(np.isfinite(C))
+        r, c = wl.sample_positions(w.M, w.N, 1500, seed=2)
+        assert sampled_error(C, A, B, r, c) <= TOL
+        # Every column (all panels), densely, on a band of rows.
+        C64, S = oracle.sgemm_f64_rows(A, B, 0, 16)
+        assert oracle.normalized_error(C[:16], C64, S) <= TOL
+
+
 def test_repeat_calls_are_stable(lib):
     """Stream-K adds partial sums with atomics: repeated runs stay within the bound."""
     _apply(lib, ("ffma", 1, 3))
