@@ -316,7 +316,7 @@ HostPipe *host_pipe(int device) {
 int64_t panel_width(int64_t M, int64_t N, int64_t K) {
     const double work = static_cast<double>(M) * static_cast<double>(N) * static_cast<double>(K);
     if (N < 512 || work < 1073741824.0) return 0;
-    const int64_t w = ((N + 3) / 4 + 255) / 256 * 256;  // about four panels, 256-column multiples
+    const int64_t w = ((N + 7) / 8 + 255) / 256 * 256;  // at most eight panels, 256-column multiples
     return w < N ? w : 0;
 }
 

@@ -179,7 +179,7 @@ int sgemm_f32_fused(int transA, int transB, int64_t M, int64_t N, int64_t K, flo
  * asynchronous; the caller synchronises the stream before reading C_host.
  * Same sizes, strides, errors and results as sgemm_f32.
  * Products of at least 2^30 multiply-adds with N >= 512 are pipelined over
- * about four column panels of B and C: A and the B panels are copied in on
+ * up to eight column panels of B and C (widths in multiples of 256): A and the B panels are copied in on
  * `stream`, panel j's product runs on a library stream as soon as its B
  * panel is in, and its C panel is copied out on a second library stream, so
  * copies in, products and copies out overlap. `stream` waits for the last
