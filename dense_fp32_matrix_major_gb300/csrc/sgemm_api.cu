@@ -98,10 +98,10 @@ int check_epilogue(int64_t M, int64_t N, const float *C, int64_t ldc, const floa
 }
 
 // AUTO: the tensor-core path from 2^26 useful multiply-adds up (measured on
-// GB300: it is faster than FFMA from 512^3 on), and
-// only up to K = 8192: its accumulation rounds toward zero, so its error
-// grows with K (2.9e-6 of the 1e-5 bound at K = 4096); beyond that the FFMA
-// path keeps the bound at any K. "Useful" discounts the padding of the
+// GB300: it is faster than FFMA from 512^3 on), at any K: its accumulation
+// rounds toward zero, so beyond K = 8192 it splits every tile along K into
+// units of K <= 4096 (2.9e-6 of the 1e-5 bound) added with round-to-nearest
+// fp32 adds. "Useful" discounts the padding of the
 // tensor-core path's 128 x 256 tiles, which matters for batches of small
 // products (the FFMA path has 64 x 64 tiles for those).
 int auto_variant(const Problem &p, const DeviceInfo &dev) {
@@ -110,7 +110,7 @@ int auto_variant(const Problem &p, const DeviceInfo &dev) {
     const double fill = static_cast<double>(p.M) * static_cast<double>(p.N) / (m_pad * n_pad);
     const double work = static_cast<double>(p.M) * static_cast<double>(p.N) * static_cast<double>(p.K) *
                         static_cast<double>(p.batch) * fill;
-    if (work >= 67108864.0 && p.K <= 8192 && tf32x3_supports(p, dev)) return SGEMM_TF32X3;
+    if (work >= 67108864.0 && tf32x3_supports(p, dev)) return SGEMM_TF32X3;
     return SGEMM_FFMA;
 }
 

@@ -891,7 +891,8 @@ int launch(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStream_t st
     const int tiles = static_cast<int>(tiles_m * tiles_n * p.batch);
     // One CTA per SM (the stage ring takes most of shared memory). A stream-K
     // share below 4 k-blocks costs more in fix-up than it saves.
-    const Schedule sch = make_schedule(tiles, k_blocks, dev.sm_count, sk_mode, 4, 0.25);
+    const bool long_k = k_blocks > 2 * KB_CAP;  // every tile split, units of <= KB_CAP k-blocks
+    const Schedule sch = make_schedule(tiles, k_blocks, dev.sm_count, long_k ? SK_ALL : sk_mode, 4, 0.25);
     const int split = tiles - sch.dp_tiles;
     int rc = split_tiles_prepare(p, BM, BN, static_cast<int>(tiles_n), static_cast<int>(tiles_m * tiles_n),
                                  sch.dp_tiles, split, stream, launches);
@@ -925,6 +926,7 @@ int launch(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStream_t st
     a.bias_kind = p.bias_kind;
     a.act = p.act;
     a.ep = p.has_epilogue();
+    a.kb_cap = long_k ? KB_CAP : 0;
     kernel<<<sch.grid, THREADS, SMEM_BYTES, stream>>>(a);
     ++*launches;
     if (cudaGetLastError() != cudaSuccess) return SGEMM_ERR_LAUNCH;
@@ -995,7 +997,8 @@ int launch_tma(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStream_
     const int64_t k_blocks = (p.K + BK - 1) / BK;
     if (tiles_m * tiles_n * p.batch > INT32_MAX / 2) return SGEMM_ERR_UNSUPPORTED;
     const int tiles = static_cast<int>(tiles_m * tiles_n * p.batch);
-    const Schedule sch = make_schedule(tiles, k_blocks, dev.sm_count, sk_mode, 4, 0.25);
+    const bool long_k = k_blocks > 2 * KB_CAP;  // every tile split, units of <= KB_CAP k-blocks
+    const Schedule sch = make_schedule(tiles, k_blocks, dev.sm_count, long_k ? SK_ALL : sk_mode, 4, 0.25);
     const int split = tiles - sch.dp_tiles;
     int rc = split_tiles_prepare(p, BM, BN, static_cast<int>(tiles_n), static_cast<int>(tiles_m * tiles_n),
                                  sch.dp_tiles, split, stream, launches);
@@ -1025,6 +1028,7 @@ int launch_tma(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStream_
     a.bias_kind = p.bias_kind;
     a.act = p.act;
     a.ep = p.has_epilogue();
+    a.kb_cap = long_k ? KB_CAP : 0;
     kernel<<<sch.grid, threads, smem, stream>>>(mapA, mapB, a);
     ++*launches;
     if (cudaGetLastError() != cudaSuccess) return SGEMM_ERR_LAUNCH;

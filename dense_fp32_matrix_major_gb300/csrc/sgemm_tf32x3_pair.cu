@@ -563,7 +563,8 @@ int launch_pair(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStream
     const int tiles = static_cast<int>(tiles_m * tiles_n * p.batch);
     // One pair per two SMs, as many pairs as fit at once. A stream-K share
     // below 4 k-blocks costs more in fix-up than it saves.
-    const Schedule sch = make_schedule(tiles, k_blocks, clusters, sk_mode, 4, 0.25);
+    const bool long_k = k_blocks > 2 * KB_CAP;  // every tile split, units of <= KB_CAP k-blocks
+    const Schedule sch = make_schedule(tiles, k_blocks, clusters, long_k ? SK_ALL : sk_mode, 4, 0.25);
     const int split = tiles - sch.dp_tiles;
     int rc = split_tiles_prepare(p, pr::PM, pr::PN, static_cast<int>(tiles_n), static_cast<int>(tiles_m * tiles_n),
                                  sch.dp_tiles, split, stream, launches);
@@ -593,6 +594,7 @@ int launch_pair(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStream
     a.bias_kind = p.bias_kind;
     a.act = p.act;
     a.ep = p.has_epilogue();
+    a.kb_cap = long_k ? KB_CAP : 0;
     a.c_tma = c_tma ? 1 : 0;
     cfg.gridDim = dim3(2 * sch.grid);
     // Behind our own beta pre-pass (which touches only C, and which started

@@ -22,6 +22,12 @@ constexpr int B_TILE = BN * BK * 4;         // bytes of one B tile (hi or lo)
 constexpr int EPILOGUE_WARPS = 4;
 constexpr int TMEM_COLS = 512;
 constexpr int BAR_BYTES = 128;
+// The tensor core's fp32 accumulation in TMEM rounds toward zero, so its
+// error grows with the number of k-blocks one accumulator sums. Products
+// with more than 2 * KB_CAP k-blocks (K > 8192) are split along K into
+// units of at most KB_CAP k-blocks (K = 4096, normalised error ~3e-6), whose
+// partial sums are added into C with round-to-nearest fp32 adds.
+constexpr int KB_CAP = 128;
 
 // Watchdog codes (which wait gave up).
 enum : int { WD_PRODUCER = 1, WD_MMA_FULL = 2, WD_MMA_ACC = 3, WD_EPILOGUE = 4, WD_DRAIN = 5, WD_SELFTEST = 6 };
@@ -53,6 +59,9 @@ struct Args {
     // Kernels with a C tensor map: write C through shared memory with TMA
     // bulk stores (and bulk reduce-adds for split tiles).
     int c_tma = 0;
+    // Longest run of k-blocks one unit may accumulate in TMEM (0: no limit);
+    // split units start at multiples of it (see for_each_unit_of).
+    int kb_cap = 0;
 };
 
 // Item and top-left corner of tile `tile` of the item-major tile order.
@@ -526,7 +535,8 @@ __device__ __forceinline__ void epilogue_chunk(const Args &a, uint32_t taddr, fl
 
 // Calls f(tile, kb, ke) for the units of work of worker `index` of `count`
 // (whole tiles round-robin, then its even share of the split iterations), in
-// order.
+// order. With a.kb_cap a split unit also ends at every multiple of kb_cap
+// k-blocks, so no unit accumulates more than kb_cap k-blocks in TMEM.
 template <class F>
 __device__ __forceinline__ void for_each_unit_of(const Args &a, volatile int *abort_flag, int index, int count, F &&f) {
     for (int t = index; t < a.dp_tiles; t += count) {
@@ -541,7 +551,11 @@ __device__ __forceinline__ void for_each_unit_of(const Args &a, volatile int *ab
             const int tile = a.dp_tiles + static_cast<int>(it / a.k_blocks);
             const int kb = static_cast<int>(it % a.k_blocks);
             const int64_t rest = end - it;
-            const int ke = static_cast<int>(rest < a.k_blocks - kb ? kb + rest : a.k_blocks);
+            int ke = static_cast<int>(rest < a.k_blocks - kb ? kb + rest : a.k_blocks);
+            if (a.kb_cap > 0) {
+                const int lim = (kb / a.kb_cap + 1) * a.kb_cap;
+                if (ke > lim) ke = lim;
+            }
             f(tile, kb, ke);
             it += ke - kb;
         }

@@ -250,6 +250,30 @@ def test_tf32x3_long_k_margin(lib):
     assert sampled_error(C, A, B, r, c) <= TOL
 
 
+@pytest.mark.parametrize("variant,tc", [("auto", 0), ("tf32x3", 1), ("tf32x3", 3), ("tf32x3", 4)])
+@pytest.mark.parametrize("K", [8193, 20000, 40000])
+def test_tf32x3_beyond_k_8192(lib, variant, tc, K):
+    """Past K = 8192 the tensor-core kernels split every tile along K into
+    units of at most 4096, so the error stays at the K = 4096 level however
+    long K gets (without the split it grows about linearly with K)."""
+    _apply(lib, (variant, 0, 0, tc))
+    M, N = 256, 512
+    A, B = wl.make_pair(M, N, K, "normal", K)
+    C, flat, rc = run_sgemm(A, B)
+    assert rc == 0
+    assert lib.variant_name(lib.last_variant_used()) == "tf32x3"
+    assert outside_box_intact(flat, M, N, N, 0)
+    r, c = wl.sample_positions(M, N, 1500, seed=K)
+    err = sampled_error(C, A, B, r, c)
+    assert err <= 5e-6, err  # half the bound: the split keeps the K = 4096 error
+    # Integer inputs stay exact through the split and the atomic adds.
+    Ai, Bi = wl.make_pair(M, N, K, "int4", K + 1)
+    Ci, _, rc = run_sgemm(Ai, Bi)
+    assert rc == 0
+    exact = (Ai.astype(np.int64)[:8] @ Bi.astype(np.int64)).astype(np.float32)
+    assert np.array_equal(Ci[:8], exact)
+
+
 def test_nonfinite_inputs_propagate(lib):
     """Non-finite inputs reach exactly the outputs that use them.
 
