@@ -149,13 +149,28 @@ int split_tiles_prepare(const Problem &p, int bm, int bn, int tiles_n, int tiles
 }
 
 int split_tiles_finish(const Problem &p, int bm, int bn, int tiles_n, int tiles_per_item, int first_tile,
-                       int count, cudaStream_t stream, int *launches) {
+                       int count, cudaStream_t stream, int *launches, bool after_signal) {
     if (count <= 0 || p.act == SGEMM_ACT_NONE) return SGEMM_OK;
-    const dim3 grid(static_cast<unsigned>((bm + 7) / 8), static_cast<unsigned>(count));
-    tile_pass_kernel<<<grid, 256, 0, stream>>>(p.C, p.M, p.N, p.ldc, p.strideC, 1.0f, nullptr, SGEMM_BIAS_NONE,
-                                                p.act, bm, bn, tiles_n, tiles_per_item, first_tile);
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>((bm + 7) / 8), static_cast<unsigned>(count));
+    cfg.blockDim = dim3(256);
+    cfg.stream = stream;
+    // Behind a product that signals griddepcontrol.launch_dependents this
+    // pass may be scheduled during the product's tail; it waits for the
+    // whole product (griddepcontrol.wait) before it touches C.
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = after_signal ? 1 : 0;
+    if (cudaLaunchKernelEx(&cfg, tile_pass_kernel, p.C, p.M, p.N, p.ldc, p.strideC, 1.0f,
+                           static_cast<const float *>(nullptr), static_cast<int>(SGEMM_BIAS_NONE), p.act, bm, bn,
+                           tiles_n, tiles_per_item, first_tile) != cudaSuccess) {
+        cudaGetLastError();
+        return SGEMM_ERR_LAUNCH;
+    }
     ++*launches;
-    return cudaGetLastError() == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
+    return SGEMM_OK;
 }
 
 int scale_launch(const Problem &p, const DeviceInfo &dev, cudaStream_t stream, int *launches) {

@@ -102,8 +102,11 @@ inline Schedule make_schedule(int tiles, int64_t k_steps, int slots, int mode, i
 // it and applies the activation (it enqueues nothing when p.act is NONE).
 int split_tiles_prepare(const Problem &p, int bm, int bn, int tiles_n, int tiles_per_item, int first_tile,
                         int count, cudaStream_t stream, int *launches);
+// after_signal: the product just enqueued executes
+// griddepcontrol.launch_dependents, so the finish pass is launched as its
+// programmatic dependent (its launch overlaps the product's tail).
 int split_tiles_finish(const Problem &p, int bm, int bn, int tiles_n, int tiles_per_item, int first_tile,
-                       int count, cudaStream_t stream, int *launches);
+                       int count, cudaStream_t stream, int *launches, bool after_signal = false);
 
 // Enqueue the FFMA product. `launches` receives the number of kernels enqueued.
 int ffma_launch(const Problem &p, const DeviceInfo &dev, int tile, int sk_mode, cudaStream_t stream,

@@ -236,6 +236,9 @@ __global__ void __launch_bounds__(pr::THREADS, 1)
     cluster_sync();  // the peer's mbarriers exist before anyone arrives on them
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
+    // A pass launched behind this kernel (the activation of split tiles) may
+    // be scheduled now; it waits for this grid to finish before touching C.
+    if (a.signal_dependents && threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;");
 
     if (warp == 0) {
         // ------------------------------------------------------------ MMA issuer
@@ -595,6 +598,7 @@ int launch_pair(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStream
     a.act = p.act;
     a.ep = p.has_epilogue();
     a.kb_cap = long_k ? KB_CAP : 0;
+    a.signal_dependents = (split > 0 && p.act != SGEMM_ACT_NONE) ? 1 : 0;
     a.c_tma = c_tma ? 1 : 0;
     cfg.gridDim = dim3(2 * sch.grid);
     // Behind our own beta pre-pass (which touches only C, and which started
@@ -607,7 +611,7 @@ int launch_pair(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStream
     }
     ++*launches;
     return split_tiles_finish(p, pr::PM, pr::PN, static_cast<int>(tiles_n), static_cast<int>(tiles_m * tiles_n),
-                              sch.dp_tiles, split, stream, launches);
+                              sch.dp_tiles, split, stream, launches, a.signal_dependents != 0);
 }
 
 }  // namespace

@@ -62,6 +62,9 @@ struct Args {
     // Longest run of k-blocks one unit may accumulate in TMEM (0: no limit);
     // split units start at multiples of it (see for_each_unit_of).
     int kb_cap = 0;
+    // A pass (the activation of split tiles) follows as a programmatic
+    // dependent: signal griddepcontrol.launch_dependents.
+    int signal_dependents = 0;
 };
 
 // Item and top-left corner of tile `tile` of the item-major tile order.
