@@ -47,6 +47,7 @@ GB300_MAX_SM_MHZ = 2070.0
 # Fallback denominators (no measured-peaks file): dense bf16 1.9 PFLOP/s burst,
 # HBM 6.8 TB/s; TF32 runs at 1.1 / 2.25 of the bf16 rate (nominal ratio).
 FALLBACK_BF16_TFLOPS = 1900.0
+FALLBACK_HBM_GBS = 6800.0
 TF32_OVER_BF16 = 1.1 / 2.25
 
 
@@ -144,6 +145,13 @@ def _tf32x3_peak_tflops():
     if peaks and peaks.get("bf16_tflops"):
         return float(peaks["bf16_tflops"]) * TF32_OVER_BF16 / 3.0, "measured bf16 x 1.1/2.25 / 3"
     return FALLBACK_BF16_TFLOPS * TF32_OVER_BF16 / 3.0, "fallback bf16 1.9 PF x 1.1/2.25 / 3"
+
+
+def _hbm_peak_gbs():
+    peaks = _measured_peaks()
+    if peaks and peaks.get("hbm_gbs"):
+        return float(peaks["hbm_gbs"]), "measured copy bandwidth"
+    return FALLBACK_HBM_GBS, "fallback 6.8 TB/s"
 
 
 def _traffic_record(kernel_key: str):
@@ -262,9 +270,17 @@ def run_ours(args, w, torch, dist):
         bound = "alu"
         kernel_key = "ffma_kernel"
     achieved = w.flops / (ms * 1e-3) / 1e12
+    traffic = _traffic_record(kernel_key)
+    hbm_peak, hbm_src = _hbm_peak_gbs()
+    algo_gbs = w.algorithmic_bytes / (ms * 1e-3) / 1e9
+    hbm = {"algorithmic_gbs": round(algo_gbs, 1),
+           "dram_gbs": round(traffic / (ms * 1e-3) / 1e9, 1) if traffic else None,
+           "peak_gbs": hbm_peak, "peak_source": hbm_src,
+           "frac": round((traffic / (ms * 1e-3) / 1e9 if traffic else algo_gbs) / hbm_peak, 4),
+           "note": "compute-bound: intensity 2MNK / 4(MK+KN+MN) is far above the ridge point"}
     roofline = {
         "bound": bound, "achieved": round(achieved, 3), "peak": round(peak, 3), "unit": "TFLOP/s",
-        "frac": round(achieved / peak, 4), "traffic": _traffic_record(kernel_key), "kernel": kernel_key,
+        "frac": round(achieved / peak, 4), "traffic": traffic, "kernel": kernel_key, "hbm": hbm,
         "peak_source": peak_src,
         "algorithmic_flops_per_launch": w.flops,
         "timing": "CUDA events around each sgemm_f32 call on its stream (includes the small "
