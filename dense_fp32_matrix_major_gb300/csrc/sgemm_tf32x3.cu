@@ -1135,24 +1135,13 @@ int tf32x3_launch(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStre
     if (!tf32x3_supports(p, dev) || dev.device < 0 || dev.device >= kMaxDevices) return SGEMM_ERR_UNSUPPORTED;
     const bool vc = (p.ldc % 4 == 0) && (p.strideC % 4 == 0) && (reinterpret_cast<uintptr_t>(p.C) % 16 == 0);
     const int mode = g_use_tma.load();
-    if (p.transA || p.transB) {
-        // Transposed forms: the tensor-memory kernel (TMA loads needed).
-        if (!tma_ok(p)) return SGEMM_ERR_UNSUPPORTED;
-        g_last_tc_kernel.store(3);
-        if (p.transA && p.transB)
-            return vc ? launch_tma<true, true, true, true>(p, dev, sk_mode, stream, launches)
-                      : launch_tma<true, false, true, true>(p, dev, sk_mode, stream, launches);
-        if (p.transA)
-            return vc ? launch_tma<true, true, true, false>(p, dev, sk_mode, stream, launches)
-                      : launch_tma<true, false, true, false>(p, dev, sk_mode, stream, launches);
-        return vc ? launch_tma<true, true, false, true>(p, dev, sk_mode, stream, launches)
-                  : launch_tma<true, false, false, true>(p, dev, sk_mode, stream, launches);
-    }
-    if (tma_ok(p) && mode != 1) {
+    // The transposed forms always take a TMA kernel (the per-thread-load
+    // kernel serves op(A) = A, op(B) = B only).
+    if (tma_ok(p) && (mode != 1 || p.transA || p.transB)) {
         // Automatic: the SM-pair kernel where its 256 x 256 tiles are filled
         // and the product is large enough for its shorter per-SM operand
         // traffic to pay (measured on GB300: faster from 1024^3 = 2^30
-        // multiply-adds on, even at 512^3).
+        // multiply-adds on, even at 512^3); all four operand forms.
         const double work = static_cast<double>(p.M) * static_cast<double>(p.N) * static_cast<double>(p.K) *
                             static_cast<double>(p.batch);
         const bool pair = mode == 4 || (mode == 0 && p.M >= 256 && p.N >= 256 && work >= 1073741824.0);
@@ -1160,15 +1149,25 @@ int tf32x3_launch(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStre
             g_last_tc_kernel.store(4);
             return tf32x3_pair_launch(p, dev, sk_mode, stream, launches);
         }
-        if (mode == 2) {
-            g_last_tc_kernel.store(2);
+        g_last_tc_kernel.store(mode == 2 && !p.transA && !p.transB ? 2 : 3);
+        if (p.transA && p.transB)
+            return vc ? launch_tma<true, true, true, true>(p, dev, sk_mode, stream, launches)
+                      : launch_tma<true, false, true, true>(p, dev, sk_mode, stream, launches);
+        if (p.transA)
+            return vc ? launch_tma<true, true, true, false>(p, dev, sk_mode, stream, launches)
+                      : launch_tma<true, false, true, false>(p, dev, sk_mode, stream, launches);
+        if (p.transB)
+            return vc ? launch_tma<true, true, false, true>(p, dev, sk_mode, stream, launches)
+                      : launch_tma<true, false, false, true>(p, dev, sk_mode, stream, launches);
+        if (mode == 2)
             return vc ? launch_tma<false, true>(p, dev, sk_mode, stream, launches)
                       : launch_tma<false, false>(p, dev, sk_mode, stream, launches);
-        }
-        g_last_tc_kernel.store(3);
         return vc ? launch_tma<true, true>(p, dev, sk_mode, stream, launches)
                   : launch_tma<true, false>(p, dev, sk_mode, stream, launches);
     }
+    // Transposed forms without 16-byte aligned rows: tf32x3_supports has
+    // rejected them already.
+    if (p.transA || p.transB) return SGEMM_ERR_UNSUPPORTED;
     g_last_tc_kernel.store(1);
     const bool va = (p.lda % 4 == 0) && (p.strideA % 4 == 0) && (reinterpret_cast<uintptr_t>(p.A) % 16 == 0);
     const bool vb = (p.ldb % 4 == 0) && (p.strideB % 4 == 0) && (reinterpret_cast<uintptr_t>(p.B) % 16 == 0);

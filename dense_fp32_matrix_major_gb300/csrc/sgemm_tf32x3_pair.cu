@@ -1,6 +1,6 @@
 // Tensor-core SGEMM on SM pairs: tcgen05.mma.cta_group::2 (kind::tf32) with
-// the three-term TF32 split of sgemm_tf32x3.cu, for op(A) = A, op(B) = B with
-// 16-byte aligned rows.
+// the three-term TF32 split of sgemm_tf32x3.cu, for all four operand forms
+// (op(A) = A or A^T, op(B) = B or B^T) with 16-byte aligned rows.
 //
 // The product is the plain sum of "CUDA算子优化(4)：矩阵乘法", section
 // "矩阵乘法的数学定义"; the pages give no tensor-core design (they name
@@ -188,7 +188,8 @@ __device__ __noinline__ void edge_chunk(const Args &a, uint32_t taddr, float *cr
     });
 }
 
-template <bool VEC_C>
+// TA: A stored K x M (op(A) = A^T); TB: B stored N x K (op(B) = B^T).
+template <bool VEC_C, bool TA, bool TB>
 __global__ void __launch_bounds__(pr::THREADS, 1)
     tf32x3_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                        const __grid_constant__ CUtensorMap tmC, const Args a) {
@@ -316,10 +317,19 @@ __global__ void __launch_bounds__(pr::THREADS, 1)
                     const uint32_t sl = base + pr::RAW0 + static_cast<uint32_t>(slot * pr::SLOT);
                     if (is_a) {
                         mbar_arrive_expect_tx(bar(pr::RAW_FULL + slot), pr::A_RAW);
-                        tma_load_3d(sl, &tmA, kblk * BK, m0, za, bar(pr::RAW_FULL + slot));
+                        if (TA) {  // A stored K x M: four boxes of 32 m x 32 k
+#pragma unroll
+                            for (int b = 0; b < pr::HM / 32; ++b)
+                                tma_load_3d(sl + b * 4096, &tmA, m0 + 32 * b, kblk * BK, za, bar(pr::RAW_FULL + slot));
+                        } else {
+                            tma_load_3d(sl, &tmA, kblk * BK, m0, za, bar(pr::RAW_FULL + slot));
+                        }
                     } else {
                         mbar_arrive_expect_tx(bar(pr::RAW_FULL + slot), pr::B_HALF);
-                        tma_load_3d(sl + pr::A_RAW, &tmB, n0, kblk * BK, zb, bar(pr::RAW_FULL + slot));
+                        if (TB)  // B stored N x K: already K-major, 128 rows of 32 k
+                            tma_load_3d(sl + pr::A_RAW, &tmB, kblk * BK, n0, zb, bar(pr::RAW_FULL + slot));
+                        else
+                            tma_load_3d(sl + pr::A_RAW, &tmB, n0, kblk * BK, zb, bar(pr::RAW_FULL + slot));
                     }
                 }
             });
@@ -346,15 +356,31 @@ __global__ void __launch_bounds__(pr::THREADS, 1)
                     return;
                 }
                 const uint32_t sl = base + pr::RAW0 + static_cast<uint32_t>(slot * pr::SLOT);
-                // A: 16 k-values of row arow (chunks 4*part .. 4*part+3 of the swizzled row).
+                // A: 16 k-values of row arow.
                 float4 av[4];
+                if (TA) {
+                    // Box q holds rows k = 0..31 of columns m = 32q..32q+31 (128-byte
+                    // swizzled): column arow is lane `lane` of each row.
+                    float t[16];
 #pragma unroll
-                for (int j = 0; j < 4; ++j) av[j] = ld_shared_v4(sl + sw128_offset(arow, 4 * part + j));
-                // B: rows 4c..4c+3, columns 4g..4g+3 of the unswizzled 32 x 128 staging tile.
+                    for (int j = 0; j < 16; ++j)
+                        t[j] = ld_shared_f32(sl + static_cast<uint32_t>(q * 4096) + sw128_offset(16 * part + j, lane >> 2) +
+                                             static_cast<uint32_t>((lane & 3) * 4));
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) av[j] = make_float4(t[4 * j], t[4 * j + 1], t[4 * j + 2], t[4 * j + 3]);
+                } else {
+                    // Chunks 4*part .. 4*part+3 of the swizzled K-major row.
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) av[j] = ld_shared_v4(sl + sw128_offset(arow, 4 * part + j));
+                }
+                // B: op(B) = B: rows 4c..4c+3, columns 4g..4g+3 of the unswizzled 32 x 128
+                // staging tile; op(B) = B^T: four 16-byte chunks of the K-major tile.
                 float4 bq[4];
 #pragma unroll
                 for (int qq = 0; qq < 4; ++qq)
-                    bq[qq] = ld_shared_v4(sl + pr::A_RAW + static_cast<uint32_t>((4 * c + qq) * pr::HN * 4 + g * 16));
+                    bq[qq] = TB ? ld_shared_v4(sl + pr::A_RAW + static_cast<uint32_t>((qq * pr::CONV_THREADS + ct) * 16))
+                                : ld_shared_v4(sl + pr::A_RAW +
+                                               static_cast<uint32_t>((4 * c + qq) * pr::HN * 4 + g * 16));
                 fence_proxy_async_smem();  // order these loads before the next TMA into the slot
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(pr::RAW_FREE + slot));
@@ -366,15 +392,24 @@ __global__ void __launch_bounds__(pr::THREADS, 1)
                 }
                 tc_fence_after();
                 const uint32_t st = base + static_cast<uint32_t>(s * pr::OP_STAGE);
-                // Column j of the 4 x 4 block is chunk c of operand row 4g + j.
-                uint32_t off = sw128_offset(4 * g + 0, c);
-                split_store(st + off, st + pr::B_HALF + off, bq[0].x, bq[1].x, bq[2].x, bq[3].x);
-                off = sw128_offset(4 * g + 1, c);
-                split_store(st + off, st + pr::B_HALF + off, bq[0].y, bq[1].y, bq[2].y, bq[3].y);
-                off = sw128_offset(4 * g + 2, c);
-                split_store(st + off, st + pr::B_HALF + off, bq[0].z, bq[1].z, bq[2].z, bq[3].z);
-                off = sw128_offset(4 * g + 3, c);
-                split_store(st + off, st + pr::B_HALF + off, bq[0].w, bq[1].w, bq[2].w, bq[3].w);
+                if (TB) {
+                    // Same swizzled K-major layout: chunk for chunk.
+#pragma unroll
+                    for (int qq = 0; qq < 4; ++qq) {
+                        const uint32_t off = static_cast<uint32_t>((qq * pr::CONV_THREADS + ct) * 16);
+                        split_store(st + off, st + pr::B_HALF + off, bq[qq].x, bq[qq].y, bq[qq].z, bq[qq].w);
+                    }
+                } else {
+                    // Column j of the 4 x 4 block is chunk c of operand row 4g + j.
+                    uint32_t off = sw128_offset(4 * g + 0, c);
+                    split_store(st + off, st + pr::B_HALF + off, bq[0].x, bq[1].x, bq[2].x, bq[3].x);
+                    off = sw128_offset(4 * g + 1, c);
+                    split_store(st + off, st + pr::B_HALF + off, bq[0].y, bq[1].y, bq[2].y, bq[3].y);
+                    off = sw128_offset(4 * g + 2, c);
+                    split_store(st + off, st + pr::B_HALF + off, bq[0].z, bq[1].z, bq[2].z, bq[3].z);
+                    off = sw128_offset(4 * g + 3, c);
+                    split_store(st + off, st + pr::B_HALF + off, bq[0].w, bq[1].w, bq[2].w, bq[3].w);
+                }
                 const uint32_t ta = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + pr::TMEM_A +
                                     static_cast<uint32_t>(64 * s + 16 * part);
 #pragma unroll
@@ -511,14 +546,14 @@ __global__ void __launch_bounds__(pr::THREADS, 1)
 }
 
 constexpr int kMaxDevices = 64;
-std::once_flag g_pair_once[kMaxDevices][2];
-cudaError_t g_pair_err[kMaxDevices][2];
-int g_pair_clusters[kMaxDevices][2];
+std::once_flag g_pair_once[kMaxDevices][8];
+cudaError_t g_pair_err[kMaxDevices][8];
+int g_pair_clusters[kMaxDevices][8];
 
-template <bool VEC_C>
+template <bool VEC_C, bool TA, bool TB>
 int launch_pair(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStream_t stream, int *launches) {
-    auto kernel = tf32x3_pair_kernel<VEC_C>;
-    constexpr int idx = VEC_C ? 1 : 0;
+    auto kernel = tf32x3_pair_kernel<VEC_C, TA, TB>;
+    constexpr int idx = (VEC_C ? 1 : 0) + (TA ? 2 : 0) + (TB ? 4 : 0);
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
@@ -551,9 +586,13 @@ int launch_pair(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStream
     int *flag = watchdog_flag_device_ptr();
     if (!flag) return SGEMM_ERR_LAUNCH;
     alignas(64) CUtensorMap mapA, mapB, mapC;
-    if (!encode_map(&mapA, p.A, p.M, p.K, p.lda, p.batch, p.strideA, BK, pr::HM, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_map(&mapB, p.B, p.K, p.N, p.ldb, p.batch, p.strideB, pr::HN, BK, CU_TENSOR_MAP_SWIZZLE_NONE))
-        return SGEMM_ERR_LAUNCH;
+    const bool ok_a =
+        TA ? encode_map(&mapA, p.A, p.K, p.M, p.lda, p.batch, p.strideA, 32, 32, CU_TENSOR_MAP_SWIZZLE_128B)
+           : encode_map(&mapA, p.A, p.M, p.K, p.lda, p.batch, p.strideA, BK, pr::HM, CU_TENSOR_MAP_SWIZZLE_128B);
+    const bool ok_b =
+        TB ? encode_map(&mapB, p.B, p.N, p.K, p.ldb, p.batch, p.strideB, BK, pr::HN, CU_TENSOR_MAP_SWIZZLE_128B)
+           : encode_map(&mapB, p.B, p.K, p.N, p.ldb, p.batch, p.strideB, pr::HN, BK, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (!ok_a || !ok_b) return SGEMM_ERR_LAUNCH;
     // C through TMA when its rows allow 16-byte aligned boxes and C is not
     // read (beta = 0; split tiles are reduce-added either way).
     const bool c_tma = VEC_C && p.beta == 0.0f &&
@@ -619,8 +658,17 @@ int launch_pair(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStream
 int tf32x3_pair_launch(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStream_t stream, int *launches) {
     if (dev.device < 0 || dev.device >= kMaxDevices) return SGEMM_ERR_DEVICE;
     const bool vc = (p.ldc % 4 == 0) && (p.strideC % 4 == 0) && (reinterpret_cast<uintptr_t>(p.C) % 16 == 0);
-    return vc ? launch_pair<true>(p, dev, sk_mode, stream, launches)
-              : launch_pair<false>(p, dev, sk_mode, stream, launches);
+    const int form = (vc ? 1 : 0) + (p.transA ? 2 : 0) + (p.transB ? 4 : 0);
+    switch (form) {
+        case 0: return launch_pair<false, false, false>(p, dev, sk_mode, stream, launches);
+        case 1: return launch_pair<true, false, false>(p, dev, sk_mode, stream, launches);
+        case 2: return launch_pair<false, true, false>(p, dev, sk_mode, stream, launches);
+        case 3: return launch_pair<true, true, false>(p, dev, sk_mode, stream, launches);
+        case 4: return launch_pair<false, false, true>(p, dev, sk_mode, stream, launches);
+        case 5: return launch_pair<true, false, true>(p, dev, sk_mode, stream, launches);
+        case 6: return launch_pair<false, true, true>(p, dev, sk_mode, stream, launches);
+        default: return launch_pair<true, true, true>(p, dev, sk_mode, stream, launches);
+    }
 }
 
 }  // namespace sgemm

@@ -243,7 +243,7 @@ int sgemm_watchdog_selftest(int64_t wait_ms, sgemm_stream_t stream);
  *   SGEMM_TUNE_WATCHDOG_MS   milliseconds a bounded wait polls before it gives
  *                            up (1 .. 60000; default 2000)
  *   SGEMM_TUNE_TF32X3_KERNEL  tensor-core kernel: 0 = automatic (default):
- *                            the SM-pair kernel for op(A) = A, op(B) = B with
+ *                            the SM-pair kernel for any operand form with
  *                            16-byte aligned bases and row strides, M and N
  *                            >= 256 and at least 2^30 multiply-adds, else the
  *                            TMA kernel with A in tensor memory where the
@@ -252,7 +252,9 @@ int sgemm_watchdog_selftest(int64_t wait_ms, sgemm_stream_t stream);
  *                            operands in tensor memory, 4 = SM pairs (tcgen05
  *                            cta_group::2 on clusters of two CTAs). Kernels
  *                            2-4 need 16-byte aligned rows (else kernel 1
- *                            runs); the transposed forms always take kernel 3.
+ *                            runs); the transposed forms take kernel 4 when
+ *                            it is chosen (automatically or forced) and
+ *                            kernel 3 otherwise.
  * Returns SGEMM_OK or SGEMM_ERR_INVALID_ARG. sgemm_get_tuning returns the
  * value, or -1 for an unknown key.
  */

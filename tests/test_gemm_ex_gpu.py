@@ -73,6 +73,24 @@ def test_forms_and_scales(lib, variant, tile, sk, tA, tB):
             _check(lib, As, Bs, tA, tB, alpha, beta, C0)
 
 
+@pytest.mark.parametrize("tc,sk", [(4, 0), (4, 1), (4, 3), (3, 0)])
+@pytest.mark.parametrize("tA,tB", FORMS)
+def test_forms_on_each_tensor_core_kernel(lib, tc, sk, tA, tB):
+    """Every operand form on the SM-pair kernel (4) and the single-SM
+    tensor-memory kernel (3), under each schedule; 16-byte aligned rows."""
+    lib.set_variant("tf32x3")
+    lib.set_tuning(lib.SGEMM_TUNE_TF32X3_KERNEL, tc)
+    lib.set_tuning(lib.SGEMM_TUNE_STREAM_K, sk)
+    for (M, N, K) in [(129, 257, 48), (300, 200, 516), (64, 300, 1000), (260, 516, 300), (512, 768, 2048)]:
+        As, Bs = _stored(M, N, K, tA, tB, "normal", M + 2 * N + K)
+        C0 = np.random.default_rng(K).standard_normal((M, N)).astype(np.float32)
+        for alpha, beta in [(1.0, 0.0), (-0.5, 2.0)]:
+            _check(lib, As, Bs, tA, tB, alpha, beta, C0)
+    assert lib.get_tuning(lib.SGEMM_TUNE_LAST_TC_KERNEL) == tc
+    lib.set_tuning(lib.SGEMM_TUNE_TF32X3_KERNEL, 0)
+    lib.set_tuning(lib.SGEMM_TUNE_STREAM_K, 0)
+
+
 @pytest.mark.parametrize("variant", ["ffma", "tf32x3"])
 @pytest.mark.parametrize("tA,tB", FORMS)
 def test_integer_forms_bit_exact(lib, variant, tA, tB):
