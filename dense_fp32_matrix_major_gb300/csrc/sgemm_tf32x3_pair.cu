@@ -111,8 +111,17 @@ __device__ __forceinline__ uint32_t cluster_rank() {
     return r;
 }
 
+__device__ __forceinline__ void cluster_arrive() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 __device__ __forceinline__ void cluster_sync() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+    cluster_arrive();
+    cluster_wait();
 }
 
 // Arrive on the mbarrier at this CTA's shared offset `bar` in CTA `cta` of
@@ -206,6 +215,51 @@ __global__ void __launch_bounds__(pr::THREADS, 1)
     const int pair = static_cast<int>(blockIdx.x >> 1), pairs = static_cast<int>(gridDim.x >> 1);
     auto bar = [&](int i) { return smem_u32(bars + i); };
 
+    // TMA of this CTA's A rows (warp 1) or B columns (warp TMA_B_WARP) for
+    // the k-blocks it = from .. to - 1 of its units, into the raw ring.
+    auto tma_pass = [&](uint32_t from, uint32_t to) {
+        const bool is_a = warp == 1;
+        uint32_t it = 0;
+        bool ok = true;
+        for_each_unit_of(a, abort_flag, pair, pairs, [&](int tile, int kb, int ke) {
+            if (!ok || it >= to) return;
+            if (it + static_cast<uint32_t>(ke - kb) <= from) {
+                it += static_cast<uint32_t>(ke - kb);
+                return;
+            }
+            const TileAt at = tile_at<pr::PM, pr::PN>(a, tile);
+            const int m0 = static_cast<int>(at.m0) + pr::HM * static_cast<int>(rank);
+            const int n0 = static_cast<int>(at.n0) + pr::HN * static_cast<int>(rank);
+            const int za = a.a_shared ? 0 : at.item, zb = a.b_shared ? 0 : at.item;
+            for (int kblk = kb; kblk < ke && it < to; ++kblk, ++it) {
+                if (it < from) continue;
+                const int slot = static_cast<int>(it % pr::RAW_SLOTS);
+                const uint32_t ph = (it / pr::RAW_SLOTS) & 1;
+                if (!mbar_wait(bar(pr::RAW_FREE + slot), ph ^ 1, a, abort_flag, WD_PRODUCER)) {
+                    ok = false;
+                    return;
+                }
+                const uint32_t sl = base + pr::RAW0 + static_cast<uint32_t>(slot * pr::SLOT);
+                if (is_a) {
+                    mbar_arrive_expect_tx(bar(pr::RAW_FULL + slot), pr::A_RAW);
+                    if (TA) {  // A stored K x M: four boxes of 32 m x 32 k
+#pragma unroll
+                        for (int b = 0; b < pr::HM / 32; ++b)
+                            tma_load_3d(sl + b * 4096, &tmA, m0 + 32 * b, kblk * BK, za, bar(pr::RAW_FULL + slot));
+                    } else {
+                        tma_load_3d(sl, &tmA, kblk * BK, m0, za, bar(pr::RAW_FULL + slot));
+                    }
+                } else {
+                    mbar_arrive_expect_tx(bar(pr::RAW_FULL + slot), pr::B_HALF);
+                    if (TB)  // B stored N x K: already K-major, 128 rows of 32 k
+                        tma_load_3d(sl + pr::A_RAW, &tmB, kblk * BK, n0, zb, bar(pr::RAW_FULL + slot));
+                    else
+                        tma_load_3d(sl + pr::A_RAW, &tmB, n0, kblk * BK, zb, bar(pr::RAW_FULL + slot));
+                }
+            }
+        });
+    };
+
     if (threadIdx.x == 0) {
         for (int s = 0; s < pr::RAW_SLOTS; ++s) {
             mbar_init(bar(pr::RAW_FULL + s), 2);  // one expect_tx arrival per TMA issuer
@@ -225,6 +279,9 @@ __global__ void __launch_bounds__(pr::THREADS, 1)
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
+    if ((warp == 1 || warp == pr::TMA_B_WARP) && lane == 0)
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(warp == 1 ? &tmA : &tmB)) : "memory");
+    __syncthreads();  // this CTA's mbarriers are initialised
     if (warp == 0) {
         // Both CTAs allocate: the pair's MMAs use the same columns in each.
         asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_holder)),
@@ -233,8 +290,15 @@ __global__ void __launch_bounds__(pr::THREADS, 1)
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
     }
     tc_fence_before();
-    __syncthreads();
-    cluster_sync();  // the peer's mbarriers exist before anyone arrives on them
+    // The cluster barrier publishes the peer's mbarriers before anyone
+    // arrives on them, and the TMEM address to this CTA. The first loads
+    // signal only this CTA's barriers, so the TMA issuers send them while the
+    // pair meets (after their arrival, whose release would otherwise wait for
+    // the loads).
+    cluster_arrive();
+    if ((warp == 1 || warp == pr::TMA_B_WARP) && lane == 0) tma_pass(0, pr::RAW_SLOTS);
+    __syncwarp();
+    cluster_wait();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
     // A pass launched behind this kernel (the activation of split tiles) may
@@ -297,43 +361,7 @@ __global__ void __launch_bounds__(pr::THREADS, 1)
         }
     } else if (warp == 1 || warp == pr::TMA_B_WARP) {
         // ---------------------------------------------------- TMA issuers (A, B)
-        if (lane == 0) {
-            const bool is_a = warp == 1;
-            uint32_t it = 0;
-            bool ok = true;
-            for_each_unit_of(a, abort_flag, pair, pairs, [&](int tile, int kb, int ke) {
-                if (!ok) return;
-                const TileAt at = tile_at<pr::PM, pr::PN>(a, tile);
-                const int m0 = static_cast<int>(at.m0) + pr::HM * static_cast<int>(rank);
-                const int n0 = static_cast<int>(at.n0) + pr::HN * static_cast<int>(rank);
-                const int za = a.a_shared ? 0 : at.item, zb = a.b_shared ? 0 : at.item;
-                for (int kblk = kb; kblk < ke; ++kblk, ++it) {
-                    const int slot = static_cast<int>(it % pr::RAW_SLOTS);
-                    const uint32_t ph = (it / pr::RAW_SLOTS) & 1;
-                    if (!mbar_wait(bar(pr::RAW_FREE + slot), ph ^ 1, a, abort_flag, WD_PRODUCER)) {
-                        ok = false;
-                        return;
-                    }
-                    const uint32_t sl = base + pr::RAW0 + static_cast<uint32_t>(slot * pr::SLOT);
-                    if (is_a) {
-                        mbar_arrive_expect_tx(bar(pr::RAW_FULL + slot), pr::A_RAW);
-                        if (TA) {  // A stored K x M: four boxes of 32 m x 32 k
-#pragma unroll
-                            for (int b = 0; b < pr::HM / 32; ++b)
-                                tma_load_3d(sl + b * 4096, &tmA, m0 + 32 * b, kblk * BK, za, bar(pr::RAW_FULL + slot));
-                        } else {
-                            tma_load_3d(sl, &tmA, kblk * BK, m0, za, bar(pr::RAW_FULL + slot));
-                        }
-                    } else {
-                        mbar_arrive_expect_tx(bar(pr::RAW_FULL + slot), pr::B_HALF);
-                        if (TB)  // B stored N x K: already K-major, 128 rows of 32 k
-                            tma_load_3d(sl + pr::A_RAW, &tmB, kblk * BK, n0, zb, bar(pr::RAW_FULL + slot));
-                        else
-                            tma_load_3d(sl + pr::A_RAW, &tmB, n0, kblk * BK, zb, bar(pr::RAW_FULL + slot));
-                    }
-                }
-            });
-        }
+        if (lane == 0) tma_pass(pr::RAW_SLOTS, 0xffffffffu);
     } else if (warp < pr::EPI_WARP0) {
         // ------------------------------------------------------------ converters
         const int cw = warp - 2;                            // 0 .. 15
