@@ -310,14 +310,18 @@ HostPipe *host_pipe(int device) {
     return hp.status == SGEMM_OK ? &hp : nullptr;
 }
 
-// Width of the column panels of the pipelined host-buffer product, or 0 for
-// one product without panels: panels pay only when the copies are long
-// enough to hide a panel's product behind the next panel's copy.
-int64_t panel_width(int64_t M, int64_t N, int64_t K) {
+// Column panels of the pipelined host-buffer product: their widths in
+// `widths`, their count returned; 0 for one product without panels. Panels
+// pay only when the copies are long enough to hide a panel's product behind
+// the next panel's copy.
+int panel_plan(int64_t M, int64_t N, int64_t K, int64_t (&widths)[kMaxPanels]) {
     const double work = static_cast<double>(M) * static_cast<double>(N) * static_cast<double>(K);
     if (N < 512 || work < 1073741824.0) return 0;
-    const int64_t w = ((N + 7) / 8 + 255) / 256 * 256;  // at most eight panels, 256-column multiples
-    return w < N ? w : 0;
+    const int64_t w = ((N + kMaxPanels - 1) / kMaxPanels + 255) / 256 * 256;  // 256-column multiples
+    if (w >= N) return 0;
+    int n = 0;
+    for (int64_t c0 = 0; c0 < N; c0 += w) widths[n++] = (N - c0 < w) ? N - c0 : w;
+    return n;
 }
 
 }  // namespace
@@ -331,10 +335,11 @@ int sgemm_f32_from_host(int64_t M, int64_t N, int64_t K, const float *A_host, in
     if ((M > 0 && K > 0 && !A_host) || (K > 0 && N > 0 && !B_host) || (M > 0 && N > 0 && !C_host))
         return SGEMM_ERR_INVALID_ARG;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const int64_t w = (M > 0 && K > 0) ? sgemm::panel_width(M, N, K) : 0;
+    int64_t widths[sgemm::kMaxPanels];
+    const int panels = (M > 0 && K > 0) ? sgemm::panel_plan(M, N, K, widths) : 0;
     int device = -1;
     sgemm::HostPipe *hp = nullptr;
-    if (w > 0 && cudaGetDevice(&device) == cudaSuccess && device >= 0 && device < sgemm::kMaxDevices)
+    if (panels > 0 && cudaGetDevice(&device) == cudaSuccess && device >= 0 && device < sgemm::kMaxDevices)
         hp = sgemm::host_pipe(device);
     cudaGetLastError();
     if (!hp) {
@@ -356,14 +361,14 @@ int sgemm_f32_from_host(int64_t M, int64_t N, int64_t K, const float *A_host, in
     // last copy out, so the call keeps the one-stream semantics.
     std::lock_guard<std::mutex> guard(hp->lock);
     const size_t f = sizeof(float);
-    const int64_t panels = (N + w - 1) / w;
     auto fail = [] { return cudaGetLastError(), SGEMM_ERR_LAUNCH; };
     if (cudaEventRecord(hp->fork, s) != cudaSuccess || cudaStreamWaitEvent(hp->compute, hp->fork, 0) != cudaSuccess ||
         cudaStreamWaitEvent(hp->d2h, hp->fork, 0) != cudaSuccess)
         return fail();
     if (copy_rows(dA, A_host, M, K, lda, cudaMemcpyHostToDevice, s) != cudaSuccess) return fail();
-    for (int64_t j = 0; j < panels; ++j) {
-        const int64_t c0 = j * w, wj = (N - c0 < w) ? N - c0 : w;
+    int64_t c0 = 0;
+    for (int j = 0; j < panels; c0 += widths[j], ++j) {
+        const int64_t wj = widths[j];
         if (cudaMemcpy2DAsync(dB + c0, ldb * f, B_host + c0, ldb * f, wj * f, K, cudaMemcpyHostToDevice, s) !=
                 cudaSuccess ||
             cudaEventRecord(hp->b_in[j], s) != cudaSuccess ||
