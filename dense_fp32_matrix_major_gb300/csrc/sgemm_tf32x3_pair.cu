@@ -98,6 +98,11 @@ constexpr uint32_t kIdesc2 = (1u << 4) | (2u << 7) | (2u << 10) | (static_cast<u
 constexpr int RAW_FULL = 0, RAW_FREE = RAW_FULL + RAW_SLOTS, OP_FULL = RAW_FREE + RAW_SLOTS,
               OP_EMPTY = OP_FULL + OP_STAGES, ACC_FULL = OP_EMPTY + OP_STAGES, ACC_EMPTY = ACC_FULL + 1,
               DRAIN = ACC_EMPTY + 1, OP_FWD = DRAIN + 1, NBARS = OP_FWD + OP_STAGES;
+// A pair that moves from one split tile to the next waits ~5 us on GB300
+// for its accumulator to be read out: about 6 k-blocks of MMAs. The split
+// work is shared with that cost counted, so the pairs whose share crosses a
+// tile boundary are not the last to finish.
+constexpr int SWITCH_KB = 6;
 static_assert(NBARS * 8 + 16 <= PBAR_BYTES, "barrier block");
 static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
 static_assert(TMEM_A + OP_STAGES * 64 <= TMEM_COLS, "TMEM columns");
@@ -665,6 +670,7 @@ int launch_pair(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStream
     a.act = p.act;
     a.ep = p.has_epilogue();
     a.kb_cap = long_k ? KB_CAP : 0;
+    a.sk_switch_kb = pr::SWITCH_KB;
     a.signal_dependents = (split > 0 && p.act != SGEMM_ACT_NONE) ? 1 : 0;
     a.c_tma = c_tma ? 1 : 0;
     cfg.gridDim = dim3(2 * sch.grid);

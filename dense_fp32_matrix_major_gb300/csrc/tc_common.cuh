@@ -65,6 +65,12 @@ struct Args {
     // A pass (the activation of split tiles) follows as a programmatic
     // dependent: signal griddepcontrol.launch_dependents.
     int signal_dependents = 0;
+    // Cost, in k-blocks, of a switch from one split tile to the next inside
+    // one worker's share (the next unit's MMAs wait for the accumulator to be
+    // read out). With it the split iterations are shared so that k-blocks
+    // plus switches come out even; 0 shares the k-blocks evenly. Not used
+    // with kb_cap.
+    int sk_switch_kb = 0;
 };
 
 // Item and top-left corner of tile `tile` of the item-major tile order.
@@ -536,8 +542,21 @@ __device__ __forceinline__ void epilogue_chunk(const Args &a, uint32_t taddr, fl
     });
 }
 
+// First split iteration of worker `index` (index = sk_ctas: the end). With
+// a.sk_switch_kb = P the split tiles are laid on a line where each is
+// followed by a gap of P (none after the last), the line is cut evenly, and
+// a cut that falls in a gap moves to the start of the next tile.
+__device__ __forceinline__ int64_t sk_share_start(const Args &a, int index) {
+    if (a.sk_switch_kb <= 0 || a.kb_cap > 0) return a.sk_iters * index / a.sk_ctas;
+    const int64_t seg = a.k_blocks + a.sk_switch_kb;
+    const int64_t line = (a.sk_iters / a.k_blocks) * seg - a.sk_switch_kb;
+    const int64_t v = line * index / a.sk_ctas;
+    const int64_t r = v % seg;
+    return (v / seg) * a.k_blocks + (r < a.k_blocks ? r : a.k_blocks);
+}
+
 // Calls f(tile, kb, ke) for the units of work of worker `index` of `count`
-// (whole tiles round-robin, then its even share of the split iterations), in
+// (whole tiles round-robin, then its share of the split iterations), in
 // order. With a.kb_cap a split unit also ends at every multiple of kb_cap
 // k-blocks, so no unit accumulates more than kb_cap k-blocks in TMEM.
 template <class F>
@@ -547,8 +566,8 @@ __device__ __forceinline__ void for_each_unit_of(const Args &a, volatile int *ab
         f(t, 0, a.k_blocks);
     }
     if (index < a.sk_ctas) {
-        int64_t it = a.sk_iters * index / a.sk_ctas;
-        const int64_t end = a.sk_iters * (index + 1) / a.sk_ctas;
+        int64_t it = sk_share_start(a, index);
+        const int64_t end = sk_share_start(a, index + 1);
         while (it < end) {
             if (*abort_flag) return;
             const int tile = a.dp_tiles + static_cast<int>(it / a.k_blocks);
