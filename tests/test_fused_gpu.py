@@ -202,3 +202,36 @@ def test_headline_shape_fused(lib, kind, act):
                                   shape=(w.M, w.N))
     assert oracle.normalized_error(C[r, c], e64, eS) <= TOL
     assert np.all(np.isfinite(C))
+
+
+@pytest.mark.parametrize("setting", [("ffma", 1, 1, 0), ("tf32x3", 0, 1, 3), ("tf32x3", 0, 1, 4),
+                                     ("tf32x3", 0, 3, 4)], ids=lambda s: "-".join(map(str, s)))
+def test_gelu_pointwise(lib, setting):
+    """GELU of chosen values against x * Phi(x) in double: a K = 4 product
+    whose row i reproduces x_i (A row (x_i, 0, 0, 0), B all ones) feeds the
+    epilogue, in the store of whole tiles and in the pass after split ones.
+    The device evaluates Phi by a rational approximation with error below
+    7.5e-8; the bound allows for it, the fp32 rounding of the evaluation and
+    the 2^-22 relative error with which the three-term product reproduces x."""
+    import math
+
+    import torch
+
+    _configure(lib, *setting)
+    x = np.concatenate([np.linspace(-14.0, 14.0, 2801), [0.0, -0.0, 1e-30, -1e-30, 1e-7, -1e-7, 0.5, -0.5],
+                        [40.0, -40.0, 1e4, -1e4, 1e30, -1e30]]).astype(np.float32)
+    M, N, K = 3072, 256, 4
+    xs = np.resize(x, M)
+    A = np.zeros((M, K), np.float32)
+    A[:, 0] = xs
+    B = np.ones((K, N), np.float32)
+    C = lib.gemm_fused(torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda(), act="gelu")
+    torch.cuda.synchronize()
+    C = C.cpu().numpy()
+    xd = xs.astype(np.float64)
+    exact = np.array([v * 0.5 * (1.0 + math.erf(v / math.sqrt(2.0))) for v in xd])
+    err = np.abs(C - exact[:, None])
+    bound = 1e-6 * np.maximum(1.0, np.abs(xd))[:, None]
+    assert np.all(err <= bound), (setting, float((err / bound).max()), xs[np.argmax((err / bound).max(axis=1))])
+    # Below about -13 the product x * Phi(x) underflows to (minus) zero.
+    assert np.all(C[xs < -14.5] == 0.0)
