@@ -137,7 +137,9 @@ enum sgemm_bias {
 enum sgemm_activation {
     SGEMM_ACT_NONE = 0,
     SGEMM_ACT_RELU = 1, /* x < 0 ? 0 : x (NaN stays NaN) */
-    SGEMM_ACT_GELU = 2, /* x * Phi(x) = x / 2 * (1 + erf(x / sqrt(2))), Phi the standard normal CDF */
+    SGEMM_ACT_GELU = 2, /* x * Phi(x) = x / 2 * (1 + erf(x / sqrt(2))), Phi the standard normal CDF,
+                           Phi evaluated by a rational approximation of error below 7.5e-8
+                           before fp32 rounding (not the tanh form) */
     SGEMM_ACT_SILU = 3  /* x / (1 + exp(-x)) */
 };
 
