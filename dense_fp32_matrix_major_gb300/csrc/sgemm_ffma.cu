@@ -56,8 +56,9 @@ using namespace ffma;
 
 // C = act(beta * C + bias) over `count` tiles starting at `first_tile` of a
 // bm x bn tile grid (C is not read when beta = 0); tiles run item-major over
-// a batch whose items are strideC elements apart. blockIdx.y picks the tile,
-// blockIdx.x a band of 8 rows; a warp handles one row (float4 when aligned).
+// a batch whose items are strideC elements apart. blockIdx.x picks the tile
+// (up to 2^31 - 1 of them), blockIdx.y a band of 8 rows; a warp handles one
+// row (float4 when aligned).
 __global__ void tile_pass_kernel(float *C, int64_t M, int64_t N, int64_t ldc, int64_t strideC, float beta,
                                  const float *bias, int bias_kind, int act, int bm, int bn, int tiles_n,
                                  int tiles_per_item, int first_tile) {
@@ -66,12 +67,12 @@ __global__ void tile_pass_kernel(float *C, int64_t M, int64_t N, int64_t ldc, in
     // main loop at once and waits only before it writes C.
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;");
-    const int tile = first_tile + blockIdx.y;
+    const int tile = first_tile + static_cast<int>(blockIdx.x);
     const int item = tile / tiles_per_item, rest = tile % tiles_per_item;
     C += item * strideC;
     const int64_t m0 = static_cast<int64_t>(rest / tiles_n) * bm;
     const int64_t n0 = static_cast<int64_t>(rest % tiles_n) * bn;
-    const int64_t row = m0 + blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int64_t row = m0 + blockIdx.y * 8 + (threadIdx.x >> 5);
     if (row >= M || row >= m0 + bm) return;
     const int cols = static_cast<int>(min64(bn, N - n0));
     float *p = C + row * ldc + n0;
@@ -141,7 +142,7 @@ int ffma_launch(const Problem &p, const DeviceInfo &dev, int tile, int sk_mode, 
 int split_tiles_prepare(const Problem &p, int bm, int bn, int tiles_n, int tiles_per_item, int first_tile,
                         int count, cudaStream_t stream, int *launches) {
     if (count <= 0) return SGEMM_OK;
-    const dim3 grid(static_cast<unsigned>((bm + 7) / 8), static_cast<unsigned>(count));
+    const dim3 grid(static_cast<unsigned>(count), static_cast<unsigned>((bm + 7) / 8));
     tile_pass_kernel<<<grid, 256, 0, stream>>>(p.C, p.M, p.N, p.ldc, p.strideC, p.beta, p.bias, p.bias_kind,
                                                 SGEMM_ACT_NONE, bm, bn, tiles_n, tiles_per_item, first_tile);
     ++*launches;
@@ -152,7 +153,7 @@ int split_tiles_finish(const Problem &p, int bm, int bn, int tiles_n, int tiles_
                        int count, cudaStream_t stream, int *launches, bool after_signal) {
     if (count <= 0 || p.act == SGEMM_ACT_NONE) return SGEMM_OK;
     cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3(static_cast<unsigned>((bm + 7) / 8), static_cast<unsigned>(count));
+    cfg.gridDim = dim3(static_cast<unsigned>(count), static_cast<unsigned>((bm + 7) / 8));
     cfg.blockDim = dim3(256);
     cfg.stream = stream;
     // Behind a product that signals griddepcontrol.launch_dependents this

@@ -314,3 +314,34 @@ def test_bounded_wait_reports_timeout(lib):
     C, flat, rc = run_sgemm(A, B)
     assert rc == 0 and oracle_error(C, A, B) <= TOL
     assert lib.sgemm_f32_raw(1, 1, 1, 0, 1, 0, 1, 0, 1, 0) == lib.SGEMM_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("setting", [("auto", 0, 0, 0), ("tf32x3", 0, 3, 3), ("ffma", 1, 0, 0)],
+                         ids=["auto-pair", "tmem-sk3", "ffma"])
+def test_output_beyond_2_31_elements(lib, setting):
+    """C with more than 2^31 elements (66000 x 32772, 8.7 GB): element offsets
+    past 32 bits in every index path of the kernels and passes. Checked at
+    sampled outputs (random, the rows around offset 2^31, the last rows and
+    columns) and on a guard row after C that must stay untouched."""
+    import torch
+
+    _apply(lib, setting)
+    M, N, K = 66000, 32772, 68
+    assert M * N > 2**31
+    A, B = wl.make_pair(M, N, K, "normal", 31)
+    flat = torch.full(((M + 1) * N,), float("nan"), dtype=torch.float32, device="cuda")
+    C = flat[: M * N].view(M, N)
+    lib.gemm(torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda(), C)
+    torch.cuda.synchronize()
+    assert bool(torch.isnan(flat[M * N:]).all()), "write past the last row"
+    r0 = 2**31 // N
+    rows = [np.repeat(np.arange(r0 - 2, r0 + 3), 64), np.repeat(np.arange(M - 3, M), 64)]
+    cols = [np.tile(np.linspace(0, N - 1, 64).astype(np.int64), 5), np.tile(np.linspace(0, N - 1, 64).astype(np.int64), 3)]
+    rr, cc = wl.sample_positions(M, N, 4000, seed=13)
+    r = np.concatenate([rr] + rows)
+    c = np.concatenate([cc] + cols)
+    vals = C[torch.from_numpy(r).cuda(), torch.from_numpy(c).cuda()].cpu().numpy()
+    c64, s = oracle.sgemm_f64_at(A, B, r, c)
+    assert oracle.normalized_error(vals, c64, s) <= TOL
+    del flat, C
+    torch.cuda.empty_cache()
