@@ -97,11 +97,10 @@ int check_epilogue(int64_t M, int64_t N, const float *C, int64_t ldc, const floa
     return SGEMM_OK;
 }
 
-// AUTO: the tensor-core path from 2^26 useful multiply-adds up (measured on
-// GB300: it is faster than FFMA from 512^3 on), at any K: its accumulation
-// rounds toward zero, so beyond K = 8192 it splits every tile along K into
-// units of K <= 4096 (2.9e-6 of the 1e-5 bound) added with round-to-nearest
-// fp32 adds. "Useful" discounts the padding of the
+// AUTO: the tensor-core path from 2^14 useful multiply-adds up, at any K:
+// its accumulation rounds toward zero, so beyond K = 8192 it splits every
+// tile along K into units of K <= 4096 (2.9e-6 of the 1e-5 bound) added with
+// round-to-nearest fp32 adds. "Useful" discounts the padding of the
 // tensor-core path's 128 x 256 tiles, which matters for batches of small
 // products (the FFMA path has 64 x 64 tiles for those).
 int auto_variant(const Problem &p, const DeviceInfo &dev) {
@@ -110,7 +109,12 @@ int auto_variant(const Problem &p, const DeviceInfo &dev) {
     const double fill = static_cast<double>(p.M) * static_cast<double>(p.N) / (m_pad * n_pad);
     const double work = static_cast<double>(p.M) * static_cast<double>(p.N) * static_cast<double>(p.K) *
                         static_cast<double>(p.batch) * fill;
-    if (work >= 67108864.0 && tf32x3_supports(p, dev)) return SGEMM_TF32X3;
+    // Measured on GB300 (CUDA events, L2 flushed): the tensor-core kernels
+    // are faster from 64^3 on (64^3: 11.6 vs 16.4 us; 256^3: 19.7 vs 28.7;
+    // 2048 x 128 x 512: 20.0 vs 30.7; 300 x 257 x 513, rows not 16-byte
+    // aligned: 36.3 vs 42.0), FFMA only on the tiniest products (16^3: 8.3
+    // vs 10.5 us), where launch latency is all there is.
+    if (work >= 16384.0 && tf32x3_supports(p, dev)) return SGEMM_TF32X3;
     return SGEMM_FFMA;
 }
 

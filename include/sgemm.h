@@ -54,7 +54,8 @@ enum sgemm_status {
 
 /* Kernel variants. */
 enum sgemm_variant {
-    SGEMM_AUTO = 0,   /* pick per shape and alignment */
+    SGEMM_AUTO = 0,   /* pick per shape and alignment: TF32X3 from 2^14 multiply-adds (tile
+                         padding discounted), FFMA below */
     SGEMM_FFMA = 1,   /* register-blocked fp32 fused multiply-add on the CUDA cores */
     SGEMM_TF32X3 = 2  /* tensor cores (tcgen05) with the three-term TF32 split */
 };

@@ -130,19 +130,26 @@ def test_special_cases(lib):
         C, flat, rc = run_sgemm(A, B, prefill=np.float32(7777.25))
         assert rc == 0
         assert np.all(flat == np.float32(7777.25))
-    # Single nonzero term: one scaled row of B, exactly.
-    A = np.zeros((70, 40), np.float32)
-    A[33, 17] = -0.5
-    B = np.random.default_rng(5).standard_normal((40, 90)).astype(np.float32)
-    C, flat, rc = run_sgemm(A, B)
+    # Single nonzero term and identity: every output is one product plus
+    # exact zeros, so FFMA reproduces B bit for bit. The three-term TF32 split
+    # carries B's bits to 2^-22 of each value (hi + rounded lo), within the bound.
+    A1 = np.zeros((70, 40), np.float32)
+    A1[33, 17] = -0.5
+    B1 = np.random.default_rng(5).standard_normal((40, 90)).astype(np.float32)
     exp = np.zeros((70, 90), np.float32)
-    exp[33] = -0.5 * B[17]
-    assert rc == 0 and np.array_equal(C, exp)
-    # Identity: C == B bit for bit.
+    exp[33] = -0.5 * B1[17]
     I = np.eye(300, dtype=np.float32)
-    B = np.random.default_rng(6).standard_normal((300, 200)).astype(np.float32)
-    C, flat, rc = run_sgemm(I, B)
-    assert rc == 0 and np.array_equal(C, B)
+    B2 = np.random.default_rng(6).standard_normal((300, 200)).astype(np.float32)
+    for variant in ("ffma", "tf32x3", "auto"):
+        _apply(lib, (variant, 0, 0))
+        C1, flat, rc1 = run_sgemm(A1, B1)
+        C2, flat, rc2 = run_sgemm(I, B2)
+        assert rc1 == 0 and rc2 == 0
+        if lib.variant_name(lib.last_variant_used()) == "ffma":
+            assert np.array_equal(C1, exp) and np.array_equal(C2, B2)
+        else:
+            assert oracle_error(C1, A1, B1) <= TOL and oracle_error(C2, I, B2) <= TOL
+            assert np.max(np.abs(C2 - B2) / np.maximum(np.abs(B2), 1e-30)) <= 2.0**-21
 
 
 def test_status_codes_on_device(lib):
