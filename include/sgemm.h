@@ -76,9 +76,10 @@ enum sgemm_variant {
  * arithmetic in an order the library chooses; the acceptance bound is
  * max |C - C_exact| / sum_k |A[i][k]| |B[k][j]| <= 1e-5, and inputs whose
  * products and partial sums are integers below 2^24 give exact results.
- * Non-finite inputs: SGEMM_FFMA follows IEEE arithmetic; SGEMM_TF32X3 gives
- * NaN where IEEE gives +-inf (its split multiplies an infinite high part by
- * a zero low part). NaN inputs give NaN in both.
+ * Non-finite inputs: SGEMM_FFMA follows IEEE arithmetic; SGEMM_TF32X3 (what
+ * SGEMM_AUTO runs from 2^14 multiply-adds on) gives NaN where IEEE gives
+ * +-inf (its split multiplies an infinite high part by a zero low part).
+ * NaN inputs give NaN in both.
  * Returns SGEMM_OK or an sgemm_status code; on error nothing is enqueued.
  */
 int sgemm_f32(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, const float *B,
