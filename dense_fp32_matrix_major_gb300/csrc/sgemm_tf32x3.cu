@@ -1140,11 +1140,14 @@ int tf32x3_launch(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStre
     if (tma_ok(p) && (mode != 1 || p.transA || p.transB)) {
         // Automatic: the SM-pair kernel where its 256 x 256 tiles are filled
         // and the product is large enough for its shorter per-SM operand
-        // traffic to pay (measured on GB300: faster from 1024^3 = 2^30
-        // multiply-adds on, even at 512^3); all four operand forms.
+        // traffic to outweigh its longer start: above 2^29 multiply-adds
+        // (measured on GB300, L2 flushed, pair vs single-SM kernel:
+        // 768 x 768 x 1024 22.9 vs 24.1 us, 1024^3 27.3 vs 31.2; at 2^29,
+        // 512 x 512 x 2048 23.0 vs 21.9 and 512 x 1024 x 1024 22.9 vs 22.0;
+        // 768^3 22.9 vs 22.0); all four operand forms.
         const double work = static_cast<double>(p.M) * static_cast<double>(p.N) * static_cast<double>(p.K) *
                             static_cast<double>(p.batch);
-        const bool pair = mode == 4 || (mode == 0 && p.M >= 256 && p.N >= 256 && work >= 1073741824.0);
+        const bool pair = mode == 4 || (mode == 0 && p.M >= 256 && p.N >= 256 && work > 536870912.0);
         if (pair) {
             g_last_tc_kernel.store(4);
             return tf32x3_pair_launch(p, dev, sk_mode, stream, launches);

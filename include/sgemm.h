@@ -249,7 +249,7 @@ int sgemm_watchdog_selftest(int64_t wait_ms, sgemm_stream_t stream);
  *   SGEMM_TUNE_TF32X3_KERNEL  tensor-core kernel: 0 = automatic (default):
  *                            the SM-pair kernel for any operand form with
  *                            16-byte aligned bases and row strides, M and N
- *                            >= 256 and at least 2^30 multiply-adds, else the
+ *                            >= 256 and more than 2^29 multiply-adds, else the
  *                            TMA kernel with A in tensor memory where the
  *                            rows are 16-byte aligned, else per-thread loads;
  *                            1 = per-thread loads, 2 = TMA, 3 = TMA with A's
