@@ -58,6 +58,26 @@ def _dist_env():
     return ws, rank, local
 
 
+# ------------------------------------------------------- ranks (N > 1)
+
+
+def max_over_ranks(ms: float, dist, device) -> float:
+    """The slowest rank's step time (ms itself when the job has one rank)."""
+    if dist is None:
+        return ms
+    import torch
+
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gflops(ws: int, flops_per_rank: float, ms_max: float) -> float:
+    """Whole-job GFLOP/s: the units every rank processed over the slowest
+    rank's time (each rank runs its own replica of the workload)."""
+    return ws * flops_per_rank / (ms_max * 1e-3) / 1e9
+
+
 # ------------------------------------------------------------------ clocks
 
 
@@ -241,12 +261,8 @@ def run_ours(args, w, torch, dist):
     sampler.stop()
     per_step = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     ms = sum(per_step) / len(per_step)
-    ms_max = ms
-    if dist is not None:
-        t = torch.tensor([ms], dtype=torch.float64, device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_max = float(t.item())
-    value = ws * w.flops / (ms_max * 1e-3) / 1e9
+    ms_max = max_over_ranks(ms, dist, device)
+    value = job_gflops(ws, w.flops, ms_max)
 
     # Parity spot check of the timed output (cheap, sampled; not timed).
     import oracle  # test infrastructure: used here only to spot-check the result
@@ -403,13 +419,9 @@ def run_e2e(args, w, torch, sgemm, A, B, device, dist, ws):
         sgemm.sgemm_f32_from_host(Ah, Bh, Ch, dA, dB, dC, stream)
     ev1.record(stream)
     torch.cuda.synchronize()
-    ms = ev0.elapsed_time(ev1) / steps
-    if dist is not None:
-        t = torch.tensor([ms], dtype=torch.float64, device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ev0.elapsed_time(ev1) / steps, dist, device)
     return {
-        "value": round(ws * w.flops / (ms * 1e-3) / 1e9, 2), "unit": UNIT,
+        "value": round(job_gflops(ws, w.flops, ms), 2), "unit": UNIT,
         "h2d_bytes_per_step": 4 * (w.M * w.K + w.K * w.N), "d2h_bytes_per_step": 4 * w.M * w.N,
         "ms_per_step": round(ms, 4), "steps": steps,
         "path": "sgemm_f32_from_host: pinned host A, B -> device, product, device C -> pinned host",
