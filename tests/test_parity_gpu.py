@@ -352,3 +352,27 @@ def test_output_beyond_2_31_elements(lib, setting):
     assert oracle.normalized_error(vals, c64, s) <= TOL
     del flat, C
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("M,N,K,lda_pad,variant,tc", [
+    (16, 16, 16, 0, "ffma", 0),        # tiniest products stay on the CUDA cores
+    (64, 64, 64, 0, "tf32x3", 3),      # from 2^14 useful multiply-adds: tensor cores
+    (512, 512, 512, 0, "tf32x3", 3),   # single-SM kernel below 2^29
+    (512, 512, 2048, 0, "tf32x3", 3),  # exactly 2^29: still single-SM
+    (768, 768, 1024, 0, "tf32x3", 4),  # above 2^29 with M, N >= 256: SM pairs
+    (2048, 3072, 4096, 0, "tf32x3", 4),
+    (200, 4096, 4096, 0, "tf32x3", 3),  # M < 256: single-SM kernel however large
+    (300, 300, 301, 1, "tf32x3", 1),    # rows not 16-byte aligned: per-thread loads
+])
+def test_auto_dispatch(lib, M, N, K, lda_pad, variant, tc):
+    """AUTO's choice of variant and tensor-core kernel (SGEMM_TUNE_LAST_TC_KERNEL)
+    at the switch points measured on GB300, and a correct result there."""
+    _apply(lib, ("auto", 0, 0, 0))
+    A, B = wl.make_pair(M, N, K, "normal", 61)
+    C, flat, rc = run_sgemm(A, B, lda=K + lda_pad if lda_pad else None)
+    assert rc == 0
+    assert lib.variant_name(lib.last_variant_used()) == variant
+    if variant == "tf32x3":
+        assert lib.get_tuning(lib.SGEMM_TUNE_LAST_TC_KERNEL) == tc
+    r, c = wl.sample_positions(M, N, 500, seed=3)
+    assert sampled_error(C, A, B, r, c) <= TOL
