@@ -670,7 +670,7 @@ int launch_pair(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStream
     a.act = p.act;
     a.ep = p.has_epilogue();
     a.kb_cap = long_k ? KB_CAP : 0;
-    a.sk_switch_kb = pr::SWITCH_KB;
+    count_switches(a, pr::SWITCH_KB);
     a.signal_dependents = (split > 0 && p.act != SGEMM_ACT_NONE) ? 1 : 0;
     a.c_tma = c_tma ? 1 : 0;
     cfg.gridDim = dim3(2 * sch.grid);

@@ -546,8 +546,8 @@ __device__ __forceinline__ void epilogue_chunk(const Args &a, uint32_t taddr, fl
 // a.sk_switch_kb = P the split tiles are laid on a line where each is
 // followed by a gap of P (none after the last), the line is cut evenly, and
 // a cut that falls in a gap moves to the start of the next tile.
-__device__ __forceinline__ int64_t sk_share_start(const Args &a, int index) {
-    if (a.sk_switch_kb <= 0 || a.kb_cap > 0) return a.sk_iters * index / a.sk_ctas;
+__host__ __device__ __forceinline__ int64_t sk_share_start(const Args &a, int index) {
+    if (a.sk_switch_kb <= 0 || a.kb_cap > 0 || a.sk_iters <= 0) return a.sk_iters * index / a.sk_ctas;
     const int64_t seg = a.k_blocks + a.sk_switch_kb;
     const int64_t line = (a.sk_iters / a.k_blocks) * seg - a.sk_switch_kb;
     const int64_t v = line * index / a.sk_ctas;
@@ -555,12 +555,38 @@ __device__ __forceinline__ int64_t sk_share_start(const Args &a, int index) {
     return (v / seg) * a.k_blocks + (r < a.k_blocks ? r : a.k_blocks);
 }
 
+// The slowest share of the split iterations: its k-blocks plus `cost` for
+// each switch from one split tile to the next inside it (every worker that
+// has a share runs the same number of whole tiles).
+__host__ __device__ inline int64_t slowest_share(const Args &a, int64_t cost) {
+    int64_t worst = 0;
+    for (int i = 0; i < a.sk_ctas; ++i) {
+        const int64_t s0 = sk_share_start(a, i), s1 = sk_share_start(a, i + 1);
+        if (s1 <= s0) continue;
+        const int64_t c = (s1 - s0) + cost * ((s1 - 1) / a.k_blocks - s0 / a.k_blocks);
+        worst = c > worst ? c : worst;
+    }
+    return worst;
+}
+
+// Sets a.sk_switch_kb: `cost` where counting the switches makes the slowest
+// share faster than the even split does, else 0 (an even split that already
+// falls on tile boundaries loses to nothing).
+inline void count_switches(Args &a, int cost) {
+    a.sk_switch_kb = 0;
+    if (cost <= 0 || a.sk_ctas <= 0 || a.kb_cap > 0) return;
+    const int64_t even = slowest_share(a, cost);
+    a.sk_switch_kb = cost;
+    if (slowest_share(a, cost) >= even) a.sk_switch_kb = 0;
+}
+
 // Calls f(tile, kb, ke) for the units of work of worker `index` of `count`
 // (whole tiles round-robin, then its share of the split iterations), in
 // order. With a.kb_cap a split unit also ends at every multiple of kb_cap
 // k-blocks, so no unit accumulates more than kb_cap k-blocks in TMEM.
 template <class F>
-__device__ __forceinline__ void for_each_unit_of(const Args &a, volatile int *abort_flag, int index, int count, F &&f) {
+__host__ __device__ __forceinline__ void for_each_unit_of(const Args &a, volatile int *abort_flag, int index, int count,
+                                                          F &&f) {
     for (int t = index; t < a.dp_tiles; t += count) {
         if (*abort_flag) return;
         f(t, 0, a.k_blocks);
