@@ -183,10 +183,11 @@ int sgemm_f32_fused(int transA, int transB, int64_t M, int64_t N, int64_t K, flo
  * asynchronous; the caller synchronises the stream before reading C_host.
  * Same sizes, strides, errors and results as sgemm_f32.
  * Products of at least 2^30 multiply-adds with N >= 512 are pipelined over
- * up to eight column panels of B and C (widths in multiples of 256): A and the B panels are copied in on
- * `stream`, panel j's product runs on a library stream as soon as its B
- * panel is in, and its C panel is copied out on a second library stream, so
- * copies in, products and copies out overlap. `stream` waits for the last
+ * up to eight column panels of B and C (widths in multiples of 256): A and
+ * the B panels are copied in on `stream`, panel j's product runs on a
+ * library stream as soon as its B panel is in, and its C panel is copied
+ * out on a second library stream, so copies in, products and copies out
+ * overlap. `stream` waits for the last
  * copy out, so the call behaves as if everything ran in order on `stream`.
  * The two library streams and their events are created on the first
  * pipelined call on a device and kept for the process (no memory is
@@ -205,11 +206,11 @@ int sgemm_set_variant(int variant);
 int sgemm_get_variant(void);
 /* Name of a variant ("auto", "ffma", "tf32x3"), or "unknown". Static storage. */
 const char *sgemm_variant_name(int variant);
-/* Variant that the most recent successful sgemm_f32 call in this process
- * enqueued (SGEMM_AUTO before any call). For reporting only. */
+/* Variant that the most recent successful product call (any entry point) in
+ * this process enqueued (SGEMM_AUTO before any call). For reporting only. */
 int sgemm_last_variant_used(void);
-/* Number of kernel launches that the most recent successful sgemm_f32 call
- * enqueued (0 for an empty product). For reporting only. */
+/* Number of kernel launches that the most recent successful product call
+ * (any entry point) enqueued (0 for an empty product). For reporting only. */
 int sgemm_last_launch_count(void);
 
 /* Human-readable text of a status code. Static storage. */
