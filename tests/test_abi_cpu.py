@@ -98,3 +98,23 @@ def test_tuning_keys(binding):
 def test_invalid_arguments_rejected_without_device(binding, args):
     # Argument checks run before any CUDA call, so these work on a CPU-only host.
     assert binding.sgemm_f32_raw(*args, 0) == binding.SGEMM_ERR_INVALID_ARG
+
+
+def _header_enums():
+    with open(os.path.join(ROOT, "include", "sgemm.h")) as f:
+        text = re.sub(r"/\*.*?\*/", "", f.read(), flags=re.S)
+    return {name: int(value) for name, value in re.findall(r"\b(SGEMM_[A-Z0-9_]+)\s*=\s*(-?\d+)", text)}
+
+
+def test_binding_constants_match_the_header(binding):
+    """Every enumerator of sgemm.h has the same value in the Python binding,
+    and the binding's name maps use those values."""
+    enums = _header_enums()
+    assert len(enums) >= 20
+    for name, value in enums.items():
+        assert getattr(binding, name) == value, name
+    assert binding.BIAS_KINDS["col"] == enums["SGEMM_BIAS_PER_COL"]
+    assert binding.BIAS_KINDS["row"] == enums["SGEMM_BIAS_PER_ROW"]
+    assert binding.ACTIVATIONS["gelu"] == enums["SGEMM_ACT_GELU"]
+    assert binding.ACTIVATIONS["silu"] == enums["SGEMM_ACT_SILU"]
+    assert binding.ACTIVATIONS["relu"] == enums["SGEMM_ACT_RELU"]
