@@ -891,7 +891,7 @@ int launch(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStream_t st
     const int tiles = static_cast<int>(tiles_m * tiles_n * p.batch);
     // One CTA per SM (the stage ring takes most of shared memory). A stream-K
     // share below 4 k-blocks costs more in fix-up than it saves.
-    const bool long_k = k_blocks > 2 * KB_CAP;  // every tile split, units of <= KB_CAP k-blocks
+    const bool long_k = k_blocks > KB_CAP;  // every tile split, units of <= KB_CAP k-blocks
     const Schedule sch = make_schedule(tiles, k_blocks, dev.sm_count, long_k ? SK_ALL : sk_mode, 4, 0.25);
     const int split = tiles - sch.dp_tiles;
     int rc = split_tiles_prepare(p, BM, BN, static_cast<int>(tiles_n), static_cast<int>(tiles_m * tiles_n),
@@ -997,7 +997,7 @@ int launch_tma(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStream_
     const int64_t k_blocks = (p.K + BK - 1) / BK;
     if (tiles_m * tiles_n * p.batch > INT32_MAX / 2) return SGEMM_ERR_UNSUPPORTED;
     const int tiles = static_cast<int>(tiles_m * tiles_n * p.batch);
-    const bool long_k = k_blocks > 2 * KB_CAP;  // every tile split, units of <= KB_CAP k-blocks
+    const bool long_k = k_blocks > KB_CAP;  // every tile split, units of <= KB_CAP k-blocks
     const Schedule sch = make_schedule(tiles, k_blocks, dev.sm_count, long_k ? SK_ALL : sk_mode, 4, 0.25);
     const int split = tiles - sch.dp_tiles;
     int rc = split_tiles_prepare(p, BM, BN, static_cast<int>(tiles_n), static_cast<int>(tiles_m * tiles_n),

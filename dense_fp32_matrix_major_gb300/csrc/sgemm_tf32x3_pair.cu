@@ -6,37 +6,49 @@
 // "矩阵乘法的数学定义"; the pages give no tensor-core design (they name
 // tensor cores once, "CUDA内存优化入门：从Naive到Tiled矩阵乘法", section 八).
 //
-// Why pairs. On one SM the 128 x 256 kernel moves about 256 KB through
-// shared memory per 32-deep k-block (TMA writes of the raw tiles, the
-// converters' reads and their hi / lo writes of B, and the tensor core's
-// reads of B, 8 KB per 128 x 256 x 8 MMA), which holds the tensor pipe near
-// 83% of its rate. Two CTAs on two SMs of a cluster share one 256 x 256 tile:
-// each holds 128 rows of A (in its TMEM) and 128 columns of B (in its shared
-// memory), and one MMA of 256 x 256 x 8 issued by the even CTA reads both
-// halves. Per SM that halves B's traffic: about 144 KB per k-block for the
-// same flops, under what the shared-memory pipe sustains.
+// Accuracy: short accumulation chains, folded on chip. The tensor core adds
+// each MMA's products into its fp32 accumulator with truncation (measured on
+// GB300: about one unit in the last place of the running value per
+// tcgen05.mma), so one accumulator that chains every MMA of a long K drifts
+// in one direction when the terms share a sign (3.5e-5 of sum |a||b| at
+// K = 16384 on U[0,1] inputs). Here an accumulator never chains more than
+// FOLD_KB k-blocks (12 MMAs each): the pair's MMAs alternate between two
+// accumulators in TMEM, and while the tensor core fills one, the epilogue
+// warps add the other, rounded to nearest, into an fp32 running sum of the
+// tile held in shared memory. The MMAs never wait for a fold.
+//
+// Why pairs. Two CTAs on two SMs of a cluster share one 256 x 128 tile: each
+// holds 128 rows of A (split into hi / lo, in its TMEM) and 64 columns of B
+// (hi / lo in its shared memory), and one MMA of 256 x 128 x 8 issued by the
+// even CTA reads both halves. Each SM's shared memory then serves only half
+// of the B operand the tensor core reads. (Measured on GB300: the 256 x 128
+// x 8 and 256 x 256 x 8 tf32 MMAs run at the same multiply-add rate, 32.7
+// and 65.4 ns each.) TMEM per CTA: two 128-column accumulators and four A
+// stages of 64 columns (hi | lo for 32 values of k), all 512 columns.
 //
 // Roles in each CTA (23 warps):
 //   * warp 0: in the even CTA, one thread issues the pair's MMAs (4 k-slices
-//     x 3 products per k-block, lo*hi + hi*lo + hi*hi) and commits them to
-//     the mbarriers of both CTAs (multicast); in the odd CTA, one thread
-//     forwards "stage filled" to the even CTA (one cluster-scope arrival per
-//     k-block instead of one per converter warp).
+//     x 3 products per k-block, lo*hi + hi*lo + hi*hi) into accumulator
+//     d = (fold interval) mod 2 and commits them to the mbarriers of both
+//     CTAs (multicast).
 //   * warps 1 and 22: TMA of this CTA's A rows (128 x 32, 128-byte swizzled)
-//     and B columns (32 x 128, unswizzled) into a 2-slot raw ring.
-//   * warps 2-17 (converters, two groups of 8 taking alternate k-blocks):
-//     split A into hi / lo and write them to this CTA's TMEM (the A
-//     operand), transpose and split B into K-major, 128-byte-swizzled hi / lo
-//     tiles in a 4-stage shared ring, then one lane per warp arrives on a
-//     local mbarrier (the even CTA's stage-full barrier, or the odd CTA's
-//     forwarding barrier).
-//   * warps 18-21 (epilogue): one per TMEM lane quarter, reading the
-//     accumulator's 256 columns for its 32 rows in 32 x 32 chunks, each
-//     staged in shared memory and written by one TMA bulk store (or bulk
-//     reduce-add for tiles split along K); chunks crossing the last row or
-//     column, C that TMA cannot address, or beta != 0 take per-thread
-//     stores. After the last chunk's TMEM load one lane per warp frees the
-//     accumulator on the even CTA's mbarrier.
+//     and B columns (32 x 64) into a 4-slot raw ring.
+//   * warps 2-17 (converters, four groups of four warps, group g taking the
+//     k-blocks it with it mod 4 = g; each warp of a group serves one TMEM
+//     lane quarter): each thread splits one row of A (32 values) into hi /
+//     lo and writes them to TMEM (tcgen05.st), and transposes and splits one
+//     4 x 4 block of B into the K-major, 128-byte-swizzled hi / lo tiles of a
+//     4-stage shared ring; then one lane per warp signals the even CTA's
+//     stage-full barrier (a local arrival, or from the odd CTA an st.async
+//     that completes transaction bytes on it).
+//   * warps 18-21 (epilogue, one per TMEM lane quarter): for each fold
+//     interval, read the finished accumulator's 128 columns of its 32 rows
+//     (four 32 x 32 chunks), add them into the running sum (or start it) and
+//     free the accumulator; after a unit's last interval, form the output
+//     alpha * sum (+ bias, activation) in the running-sum chunk itself and
+//     write it to C with one TMA bulk store (bulk reduce-add for tiles split
+//     along K) per chunk. Chunks crossing the last row or column, C that TMA
+//     cannot address, or beta != 0 take per-thread stores.
 // Every wait is bounded in time as in the single-SM kernels; the pair meets
 // at cluster barriers only at the start (mbarriers initialised) and at the
 // end (before the TMEM of both is released).
@@ -58,28 +70,28 @@ using namespace tc;
 
 namespace pr {
 
-constexpr int PM = 256, PN = 256;  // C tile of a pair
-constexpr int HM = 128, HN = 128;  // this CTA's rows of A, columns of B
-// Four operand stages: a stage is refilled only after the MMAs that read it
-// have completed, and completions trail issue by the tensor pipe's queue,
-// so three stages left the MMA issuer waiting ~480 cycles per k-block.
-constexpr int OP_STAGES = 4, RAW_SLOTS = 2;
-constexpr int B_HALF = HN * BK * 4;   // 16 KB: one of B hi / B lo, or raw B
+constexpr int PM = 256, PN = 128;  // C tile of a pair
+constexpr int HM = 128, HN = 64;   // this CTA's rows of A, columns of B
+// Longest chain of k-blocks one accumulator sums before it is folded into the
+// running sum: 96 MMAs, ~5e-6 of sum |a||b| on non-negative inputs at any K.
+constexpr int FOLD_KB = 8;
+// Four operand stages (a stage is refilled only after the MMAs that read it
+// have completed, and completions trail issue by the tensor pipe's queue)
+// and four raw slots, one of each per converter group.
+constexpr int OP_STAGES = 4, RAW_SLOTS = 4;
+constexpr int B_HALF = HN * BK * 4;   // 8 KB: one of B hi / B lo, or raw B
 constexpr int A_RAW = HM * BK * 4;    // 16 KB
 constexpr int OP_STAGE = 2 * B_HALF;  // hi | lo
 constexpr int SLOT = A_RAW + B_HALF;  // raw A | raw B
 constexpr int RAW0 = OP_STAGES * OP_STAGE;
-// C staging: per epilogue warp two 32 x 32 fp32 chunks (128-byte swizzled
-// rows) that TMA stores or reduce-adds into C.
+// Running sum: this CTA's 128 x 128 fp32 share of the tile as 16 chunks of
+// 32 x 32 (chunk (q, c): rows 32q.., columns 32c..), rows of 128 bytes in the
+// 128-byte swizzle, so a chunk is also the source of one TMA store of C.
 constexpr int C_CHUNK = 32 * 32 * 4;
-constexpr int C_STAGE0 = RAW0 + RAW_SLOTS * SLOT;
-// Converters: two groups of 8 warps taking alternate k-blocks (one group's
-// chain of waits, loads, stores and arrivals takes longer than one k-block
-// of MMA, so one group alone would hold the tensor pipe back).
-constexpr int GROUP_WARPS = 8, CONV_GROUPS = 2, CONV_WARPS = GROUP_WARPS * CONV_GROUPS, EPI_WARPS = 4;
-// Epilogue: EPI_WARPS / 4 warps per TMEM lane quarter, each reading an equal
-// share of the accumulator's 32-column chunks; C_BUFS staging chunks each.
-constexpr int EPI_PER_QUAD = EPI_WARPS / 4, CHUNKS_PER_WARP = (PN / 32) / EPI_PER_QUAD, C_BUFS = 2;
+constexpr int R0 = RAW0 + RAW_SLOTS * SLOT;
+constexpr int R_BYTES = (HM / 32) * (PN / 32) * C_CHUNK;
+constexpr int CHUNKS = PN / 32;  // chunks per lane quarter
+constexpr int GROUP_WARPS = 4, CONV_GROUPS = 4, CONV_WARPS = GROUP_WARPS * CONV_GROUPS, EPI_WARPS = 4;
 constexpr int CONV_THREADS = 32 * GROUP_WARPS;  // threads converting one k-block
 constexpr int EPI_WARP0 = 2 + CONV_WARPS;
 // A second TMA issuer: a warp keeps only about one box in processing at a
@@ -87,26 +99,29 @@ constexpr int EPI_WARP0 = 2 + CONV_WARPS;
 // depth), so A and B come from separate warps.
 constexpr int TMA_B_WARP = EPI_WARP0 + EPI_WARPS;
 constexpr int THREADS = 32 * (TMA_B_WARP + 1);
-constexpr int BAR_OFFSET = C_STAGE0 + EPI_WARPS * C_BUFS * C_CHUNK;
+constexpr int BAR_OFFSET = R0 + R_BYTES;
 constexpr int PBAR_BYTES = 256;
 constexpr int SMEM_BYTES = BAR_OFFSET + PBAR_BYTES + 1024;
-constexpr uint32_t TMEM_A = PN;  // A stages after the 256-column accumulator
-// Instruction descriptor: D fp32, A and B tf32, both K-major, N = 256, M = 256.
+constexpr uint32_t TMEM_A = 2 * PN;  // A stages after the two 128-column accumulators
+// Instruction descriptor: D fp32, A and B tf32, both K-major, N = 128, M = 256.
 constexpr uint32_t kIdesc2 = (1u << 4) | (2u << 7) | (2u << 10) | (static_cast<uint32_t>(PN >> 3) << 17) |
                              (static_cast<uint32_t>(PM >> 4) << 24);
 // mbarrier indices
 constexpr int RAW_FULL = 0, RAW_FREE = RAW_FULL + RAW_SLOTS, OP_FULL = RAW_FREE + RAW_SLOTS,
-              OP_EMPTY = OP_FULL + OP_STAGES, ACC_FULL = OP_EMPTY + OP_STAGES, ACC_EMPTY = ACC_FULL + 1,
-              DRAIN = ACC_EMPTY + 1, OP_FWD = DRAIN + 1, NBARS = OP_FWD + OP_STAGES;
-// A pair that moves from one split tile to the next waits ~5 us on GB300
-// for its accumulator to be read out: about 6 k-blocks of MMAs. The split
-// work is shared with that cost counted, so the pairs whose share crosses a
-// tile boundary are not the last to finish.
-constexpr int SWITCH_KB = 6;
-static_assert(NBARS * 8 + 16 <= PBAR_BYTES, "barrier block");
+              OP_EMPTY = OP_FULL + OP_STAGES, ACC_FULL = OP_EMPTY + OP_STAGES, ACC_EMPTY = ACC_FULL + 2,
+              DRAIN = ACC_EMPTY + 2, NBARS = DRAIN + 1;
+// The odd CTA's converter warps report a filled stage with st.async: a 4-byte
+// store into the even CTA's shared memory that completes 4 bytes of
+// transactions on its stage-full barrier with release semantics at cluster
+// scope, without stalling the warp (a remote mbarrier.arrive.release.cluster
+// held the arriving thread ~0.8 us per k-block on GB300, measured).
+constexpr uint32_t SIGNAL_BYTES = 4 * GROUP_WARPS;
+static_assert(NBARS * 8 + 24 <= PBAR_BYTES, "barrier block");
 static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
 static_assert(TMEM_A + OP_STAGES * 64 <= TMEM_COLS, "TMEM columns");
 static_assert((HN / 4) * (BK / 4) == CONV_THREADS, "one 4 x 4 B block per converter thread");
+static_assert(CONV_GROUPS == OP_STAGES && RAW_SLOTS == OP_STAGES, "group g owns raw slot g and stage g");
+static_assert(SLOT % 1024 == 0 && RAW0 % 1024 == 0 && R0 % 1024 == 0, "1024-byte aligned swizzled buffers");
 
 }  // namespace pr
 
@@ -137,8 +152,22 @@ __device__ __forceinline__ void mbar_arrive_at(uint32_t bar, uint32_t cta) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote) : "memory");
 }
 
-// One 256 x 256 x 8 product of the pair: A (128 rows per CTA) from TMEM, B
-// (128 columns per CTA) from shared memory.
+// st.async of a 4-byte word into CTA `cta`'s shared memory at this CTA's
+// offset `word`, completing 4 bytes of transactions on the mbarrier at offset
+// `bar` there. The completion has release semantics at cluster scope (this
+// thread's prior writes, and those it has observed, are visible to a thread
+// that sees the phase complete) and the issuing thread does not wait for it.
+__device__ __forceinline__ void st_async_signal(uint32_t word, uint32_t bar, uint32_t cta) {
+    uint32_t rw, rb;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rw) : "r"(word), "r"(cta));
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rb) : "r"(bar), "r"(cta));
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(rw), "r"(0u),
+                 "r"(rb)
+                 : "memory");
+}
+
+// One 256 x 128 x 8 product of the pair: A (128 rows per CTA) from TMEM, B
+// (64 columns per CTA) from shared memory.
 __device__ __forceinline__ void tc_mma2_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t accumulate) {
     asm volatile(
         "{\n"
@@ -160,12 +189,12 @@ __device__ __forceinline__ void tc_commit2(uint32_t bar) {
         : "memory");
 }
 
-// Fused-epilogue values of 16 accumulator columns (chunk columns base ..
-// base + 15) written to the staging row of this lane: ACT(alpha * v + bias),
-// the bias per row (bl) or per column (lane (base + j)'s bl, by shuffle).
+// Fused-epilogue values of 16 columns (chunk columns base .. base + 15)
+// written to the swizzled chunk row of this lane: ACT(alpha * v + bias), the
+// bias per row (bl) or per column (lane (base + j)'s bl, by shuffle).
 template <int ACT>
 __device__ __forceinline__ void stage16_ep(uint32_t buf, int lane, int base, float alpha, bool col_bias, float bl,
-                                           const float (&v)[16]) {
+                                           const float *v) {
 #pragma unroll
     for (int j = 0; j < 16; j += 4) {
         float b[4];
@@ -177,29 +206,74 @@ __device__ __forceinline__ void stage16_ep(uint32_t buf, int lane, int base, flo
     }
 }
 
-__device__ __forceinline__ void stage16_fused(int act, uint32_t buf, int lane, int base, float alpha, bool col_bias,
-                                              float bl, const float (&v)[16]) {
+__device__ __forceinline__ void stage32_fused(int act, uint32_t buf, int lane, float alpha, bool col_bias, float bl,
+                                              const float (&v)[32]) {
     switch (act) {
-        case SGEMM_ACT_RELU: stage16_ep<SGEMM_ACT_RELU>(buf, lane, base, alpha, col_bias, bl, v); break;
-        case SGEMM_ACT_GELU: stage16_ep<SGEMM_ACT_GELU>(buf, lane, base, alpha, col_bias, bl, v); break;
-        case SGEMM_ACT_SILU: stage16_ep<SGEMM_ACT_SILU>(buf, lane, base, alpha, col_bias, bl, v); break;
-        default: stage16_ep<SGEMM_ACT_NONE>(buf, lane, base, alpha, col_bias, bl, v); break;
+        case SGEMM_ACT_RELU:
+            stage16_ep<SGEMM_ACT_RELU>(buf, lane, 0, alpha, col_bias, bl, v);
+            stage16_ep<SGEMM_ACT_RELU>(buf, lane, 16, alpha, col_bias, bl, v + 16);
+            break;
+        case SGEMM_ACT_GELU:
+            stage16_ep<SGEMM_ACT_GELU>(buf, lane, 0, alpha, col_bias, bl, v);
+            stage16_ep<SGEMM_ACT_GELU>(buf, lane, 16, alpha, col_bias, bl, v + 16);
+            break;
+        case SGEMM_ACT_SILU:
+            stage16_ep<SGEMM_ACT_SILU>(buf, lane, 0, alpha, col_bias, bl, v);
+            stage16_ep<SGEMM_ACT_SILU>(buf, lane, 16, alpha, col_bias, bl, v + 16);
+            break;
+        default:
+            stage16_ep<SGEMM_ACT_NONE>(buf, lane, 0, alpha, col_bias, bl, v);
+            stage16_ep<SGEMM_ACT_NONE>(buf, lane, 16, alpha, col_bias, bl, v + 16);
+            break;
     }
 }
 
-// A chunk that crosses the last row or column of C: per-thread stores, and
-// on the tile's last chunk the accumulator release (one lane per warp, on
-// the even CTA's barrier acc_empty). Out of line: it is rare, and inlined it
-// would compete for registers with the interior path.
+// The last fold of a unit for a chunk written with per-thread stores: the
+// chunk's accumulator columns (TMEM address taddr) plus, unless `first`, the
+// running sum (chunk rc), then C = alpha * v + beta * C (+ bias, activation)
+// for a whole tile or C += alpha * v with atomics for a tile split along K.
+// `release`: the chunk is the accumulator's last; free it on the even CTA's
+// barrier acc_empty once read. Used for chunks that cross the last row or
+// column of C and for C that TMA cannot write; called by all 32 lanes (the
+// bias shuffles). Out of line: it is rare, and inlined it would compete for
+// registers with the interior path.
 template <bool VEC_C>
-__device__ __noinline__ void edge_chunk(const Args &a, uint32_t taddr, float *crow, int64_t row, int64_t col0,
-                                        bool atomic, bool last, uint32_t acc_empty) {
+__device__ __noinline__ void edge_final_chunk(const Args &a, uint32_t taddr, uint32_t rc, bool first, float *crow,
+                                              int64_t row, int64_t col0, bool atomic, bool release,
+                                              uint32_t acc_empty) {
     const int lane = static_cast<int>(threadIdx.x & 31);
-    epilogue_chunk_then<VEC_C>(a, taddr, crow, row, col0, atomic, last, [&] {
+    float v[32];
+    tmem_load32(taddr, v);
+    if (release) {
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_at(acc_empty, 0);
-    });
+    }
+    if (!first) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const float4 r = ld_shared_v4(rc + sw128_offset(lane, j));
+            v[4 * j] += r.x;
+            v[4 * j + 1] += r.y;
+            v[4 * j + 2] += r.z;
+            v[4 * j + 3] += r.w;
+        }
+    }
+    if (col0 >= a.N) return;  // uniform over the warp
+    if (a.ep && !atomic) {
+        float bl = 0.0f;
+        if (a.bias_kind == SGEMM_BIAS_PER_COL && col0 + lane < a.N) bl = __ldg(a.bias + col0 + lane);
+        if (a.bias_kind == SGEMM_BIAS_PER_ROW && row < a.M) bl = __ldg(a.bias + row);
+        float h[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) h[j] = v[j];
+        store16_fused<VEC_C>(a, crow, row, col0, 0, bl, h);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) h[j] = v[16 + j];
+        store16_fused<VEC_C>(a, crow, row, col0 + 16, 16, bl, h);
+    } else {
+        store_chunk<VEC_C>(a, crow, row, col0, v, atomic);
+    }
 }
 
 // TA: A stored K x M (op(A) = A^T); TB: B stored N x K (op(B) = B^T).
@@ -214,6 +288,8 @@ __global__ void __launch_bounds__(pr::THREADS, 1)
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + pr::BAR_OFFSET);
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + pr::NBARS);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + pr::NBARS + 1);
+    // Target word of the odd CTA's st.async signals (its value is not used).
+    const uint32_t signal_word = smem_u32(bars + pr::NBARS + 2);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_rank();
@@ -222,6 +298,7 @@ __global__ void __launch_bounds__(pr::THREADS, 1)
 
     // TMA of this CTA's A rows (warp 1) or B columns (warp TMA_B_WARP) for
     // the k-blocks it = from .. to - 1 of its units, into the raw ring.
+    const bool tma_warp = warp == 1 || warp == pr::TMA_B_WARP;
     auto tma_pass = [&](uint32_t from, uint32_t to) {
         const bool is_a = warp == 1;
         uint32_t it = 0;
@@ -256,7 +333,7 @@ __global__ void __launch_bounds__(pr::THREADS, 1)
                     }
                 } else {
                     mbar_arrive_expect_tx(bar(pr::RAW_FULL + slot), pr::B_HALF);
-                    if (TB)  // B stored N x K: already K-major, 128 rows of 32 k
+                    if (TB)  // B stored N x K: already K-major, 64 rows of 32 k
                         tma_load_3d(sl + pr::A_RAW, &tmB, kblk * BK, n0, zb, bar(pr::RAW_FULL + slot));
                     else
                         tma_load_3d(sl + pr::A_RAW, &tmB, n0, kblk * BK, zb, bar(pr::RAW_FULL + slot));
@@ -267,25 +344,28 @@ __global__ void __launch_bounds__(pr::THREADS, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < pr::RAW_SLOTS; ++s) {
-            mbar_init(bar(pr::RAW_FULL + s), 2);  // one expect_tx arrival per TMA issuer
+            mbar_init(bar(pr::RAW_FULL + s), 2);                   // one expect_tx arrival per TMA issuer
             mbar_init(bar(pr::RAW_FREE + s), pr::GROUP_WARPS);  // one lane per converter warp
         }
         for (int s = 0; s < pr::OP_STAGES; ++s) {
-            // Even CTA: its own converter warps plus one forwarded arrival for
-            // the odd CTA's warps (OP_FWD there), so the converters never pay
-            // a cluster-scope release.
-            mbar_init(bar(pr::OP_FULL + s), pr::GROUP_WARPS + 1);
-            mbar_init(bar(pr::OP_FWD + s), pr::GROUP_WARPS);
+            // Even CTA: one arrival per own converter warp (the first also
+            // expects SIGNAL_BYTES), and SIGNAL_BYTES of transactions from the
+            // odd CTA's converter warps (st.async, see below).
+            mbar_init(bar(pr::OP_FULL + s), pr::GROUP_WARPS);
             mbar_init(bar(pr::OP_EMPTY + s), 1);
         }
-        mbar_init(bar(pr::ACC_FULL), 1);
-        mbar_init(bar(pr::ACC_EMPTY), 2 * pr::EPI_WARPS);
+        for (int d = 0; d < 2; ++d) {
+            mbar_init(bar(pr::ACC_FULL + d), 1);
+            mbar_init(bar(pr::ACC_EMPTY + d), 2 * pr::EPI_WARPS);
+        }
         mbar_init(bar(pr::DRAIN), 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if ((warp == 1 || warp == pr::TMA_B_WARP) && lane == 0)
-        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(warp == 1 ? &tmA : &tmB)) : "memory");
+    if (tma_warp && lane == 0) {
+        const bool is_a = warp == 1;
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(is_a ? &tmA : &tmB)) : "memory");
+    }
     __syncthreads();  // this CTA's mbarriers are initialised
     if (warp == 0) {
         // Both CTAs allocate: the pair's MMAs use the same columns in each.
@@ -301,7 +381,7 @@ __global__ void __launch_bounds__(pr::THREADS, 1)
     // pair meets (after their arrival, whose release would otherwise wait for
     // the loads).
     cluster_arrive();
-    if ((warp == 1 || warp == pr::TMA_B_WARP) && lane == 0) tma_pass(0, pr::RAW_SLOTS);
+    if (tma_warp && lane == 0) tma_pass(0, pr::RAW_SLOTS);
     __syncwarp();
     cluster_wait();
     tc_fence_after();
@@ -312,70 +392,90 @@ __global__ void __launch_bounds__(pr::THREADS, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------------ MMA issuer
-        if (rank == 0 && lane == 0) {
-            uint32_t it = 0, unit = 0;
+        // A 256 x 128 x 8 MMA takes ~33 ns and the tensor core queues only a
+        // few, so the issuer's own work between MMAs shows as idle tensor
+        // time. The whole warp runs the loop (its values stay warp-uniform)
+        // and one elected lane issues; the stage addresses are one add from
+        // precomputed bases, and the next stage's barrier is tested while this
+        // k-block's last k-slice is still queued.
+        if (rank == 0) {
+            const bool leader = elect_one();
+            uint32_t it = 0, iv = 0;  // k-blocks and fold intervals issued so far
+            const uint64_t desc0 = sw128_desc(base);
+            const uint32_t a0 = tmem_base + pr::TMEM_A;
+            bool ready = false;  // the stage of k-block `it` was seen full (and fenced) early
             for_each_unit_of(a, abort_flag, pair, pairs, [&](int, int kb, int ke) {
-                if (!mbar_wait<true>(bar(pr::ACC_EMPTY), (unit & 1) ^ 1, a, abort_flag, WD_MMA_ACC)) return;
-                tc_fence_after();
-                for (int kblk = kb; kblk < ke; ++kblk, ++it) {
-                    const int s = static_cast<int>(it % pr::OP_STAGES);
-                    const uint32_t ph = (it / pr::OP_STAGES) & 1;
-                    if (!mbar_wait<true>(bar(pr::OP_FULL + s), ph, a, abort_flag, WD_MMA_FULL)) return;
+                for (int k0 = kb; k0 < ke; k0 += pr::FOLD_KB) {
+                    const int k1 = ke - k0 > pr::FOLD_KB ? k0 + pr::FOLD_KB : ke;
+                    const uint32_t d = iv & 1;
+                    // Accumulator d is free once the epilogue has folded the
+                    // interval that used it two intervals back.
+                    const bool ok = mbar_wait<true>(bar(pr::ACC_EMPTY + d), ((iv >> 1) & 1) ^ 1, a, abort_flag,
+                                                    WD_MMA_ACC);
+                    if (!__all_sync(0xffffffffu, ok)) return;
                     tc_fence_after();
-                    const uint32_t st = base + static_cast<uint32_t>(s * pr::OP_STAGE);
-                    const uint64_t b_hi = sw128_desc(st), b_lo = sw128_desc(st + pr::B_HALF);
-                    const uint32_t a_hi = tmem_base + pr::TMEM_A + static_cast<uint32_t>(64 * s);
-                    const uint32_t a_lo = a_hi + 32;
+                    const uint32_t dt = tmem_base + d * pr::PN;
+                    for (int kblk = k0; kblk < k1; ++kblk, ++it) {
+                        const uint32_t s = it % pr::OP_STAGES;
+                        if (!ready) {
+                            const bool full = mbar_wait<true>(bar(pr::OP_FULL + s), (it / pr::OP_STAGES) & 1, a,
+                                                              abort_flag, WD_MMA_FULL);
+                            if (!__all_sync(0xffffffffu, full)) return;
+                            tc_fence_after();
+                        }
+                        const uint64_t b_hi = desc0 + static_cast<uint64_t>(s * (pr::OP_STAGE >> 4));
+                        const uint64_t b_lo = b_hi + (pr::B_HALF >> 4);
+                        const uint32_t a_hi = a0 + 64 * s, a_lo = a_hi + 32;
+                        const uint32_t acc0 = kblk == k0 ? 0u : 1u;  // each interval starts its accumulator
 #pragma unroll
-                    for (int ks = 0; ks < BK / 8; ++ks) {
-                        const uint64_t adv = static_cast<uint64_t>(ks * 2);
-                        const uint32_t ac = static_cast<uint32_t>(ks * 8);
-                        const uint32_t first = (kblk == kb && ks == 0) ? 0u : 1u;
-                        tc_mma2_ts(tmem_base, a_lo + ac, b_hi + adv, first);
-                        tc_mma2_ts(tmem_base, a_hi + ac, b_lo + adv, 1u);
-                        tc_mma2_ts(tmem_base, a_hi + ac, b_hi + adv, 1u);
+                        for (int ks = 0; ks < BK / 8; ++ks) {
+                            const uint64_t adv = static_cast<uint64_t>(ks * 2);
+                            const uint32_t ac = static_cast<uint32_t>(ks * 8);
+                            if (ks == BK / 8 - 1) {
+                                // The next k-block's stage, tested without blocking.
+                                const uint32_t nx = it + 1;
+                                ready = __all_sync(0xffffffffu, mbar_test_wait<true>(bar(pr::OP_FULL + nx % pr::OP_STAGES),
+                                                                                     (nx / pr::OP_STAGES) & 1));
+                                if (ready) tc_fence_after();
+                            }
+                            if (leader) {
+                                tc_mma2_ts(dt, a_lo + ac, b_hi + adv, ks == 0 ? acc0 : 1u);
+                                tc_mma2_ts(dt, a_hi + ac, b_lo + adv, 1u);
+                                tc_mma2_ts(dt, a_hi + ac, b_hi + adv, 1u);
+                            }
+                            __syncwarp();
+                        }
+                        if (leader) tc_commit2(bar(pr::OP_EMPTY + s));
+                        __syncwarp();
                     }
-                    tc_commit2(bar(pr::OP_EMPTY + s));
+                    if (leader) tc_commit2(bar(pr::ACC_FULL + d));
+                    __syncwarp();
+                    ++iv;
                 }
-                tc_commit2(bar(pr::ACC_FULL));
-                ++unit;
             });
-            tc_commit2(bar(pr::DRAIN));
-            const bool was_aborted = *abort_flag != 0;
-            if (!mbar_wait(bar(pr::DRAIN), 0, a, abort_flag, WD_DRAIN) && was_aborted) {
-                const uint64_t t0 = global_timer();
-                while (!mbar_try_wait(bar(pr::DRAIN), 0) && global_timer() - t0 < a.timeout_ns) {
+            if (leader) tc_commit2(bar(pr::DRAIN));
+            __syncwarp();
+            if (lane == 0) {
+                const bool was_aborted = *abort_flag != 0;
+                if (!mbar_wait(bar(pr::DRAIN), 0, a, abort_flag, WD_DRAIN) && was_aborted) {
+                    const uint64_t t0 = global_timer();
+                    while (!mbar_try_wait(bar(pr::DRAIN), 0) && global_timer() - t0 < a.timeout_ns) {
+                    }
                 }
             }
         }
-        if (rank != 0 && lane == 0) {
-            // Forwarder: once this CTA's converters have filled stage s, one
-            // cluster-scope arrival tells the even CTA's MMA issuer.
-            uint32_t it = 0;
-            bool ok = true;
-            for_each_unit_of(a, abort_flag, pair, pairs, [&](int, int kb, int ke) {
-                for (int kblk = kb; kblk < ke && ok; ++kblk, ++it) {
-                    const int s = static_cast<int>(it % pr::OP_STAGES);
-                    if (!mbar_wait(bar(pr::OP_FWD + s), (it / pr::OP_STAGES) & 1, a, abort_flag, WD_PRODUCER)) {
-                        ok = false;
-                        return;
-                    }
-                    mbar_arrive_at(bar(pr::OP_FULL + s), 0);
-                }
-            });
-        }
-    } else if (warp == 1 || warp == pr::TMA_B_WARP) {
+    } else if (tma_warp) {
         // ---------------------------------------------------- TMA issuers (A, B)
         if (lane == 0) tma_pass(pr::RAW_SLOTS, 0xffffffffu);
     } else if (warp < pr::EPI_WARP0) {
         // ------------------------------------------------------------ converters
-        const int cw = warp - 2;                            // 0 .. 15
-        const uint32_t group = static_cast<uint32_t>(cw >> 3);  // k-blocks with it % 2 == group
-        const int ct = threadIdx.x - 64 - 256 * static_cast<int>(group);
-        const int l = ct & 7, tb = ct >> 3;                 // 32 groups of eight lanes
-        const int g = (tb >> 3) * 8 + l, c = (l + tb) & 7;  // this thread's 4 x 4 B block
-        const int q = warp & 3, part = (cw >> 2) & 1;       // TMEM lane quarter, k-columns 16*part..+15
-        const int arow = 32 * q + lane;                     // A row this thread converts
+        const int cw = warp - 2;                                 // 0 .. 15
+        const uint32_t group = static_cast<uint32_t>(cw >> 2);  // k-blocks with it % 4 == group
+        const int ct = ((cw & 3) << 5) + lane;                   // 0 .. 127 within the group
+        const int l = ct & 7, tb = ct >> 3;                      // 16 groups of eight lanes
+        const int g = (tb >> 3) * 8 + l, c = (l + tb) & 7;       // this thread's 4 x 4 B block
+        const int q = warp & 3;                                  // TMEM lane quarter
+        const int arow = 32 * q + lane;                          // A row this thread converts
         uint32_t it = 0;
         bool ok = true;
         for_each_unit_of(a, abort_flag, pair, pairs, [&](int, int kb, int ke) {
@@ -389,24 +489,26 @@ __global__ void __launch_bounds__(pr::THREADS, 1)
                     return;
                 }
                 const uint32_t sl = base + pr::RAW0 + static_cast<uint32_t>(slot * pr::SLOT);
-                // A: 16 k-values of row arow.
-                float4 av[4];
+                // A: the 32 k-values of row arow.
+                float av[32];
                 if (TA) {
                     // Box q holds rows k = 0..31 of columns m = 32q..32q+31 (128-byte
                     // swizzled): column arow is lane `lane` of each row.
-                    float t[16];
 #pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        t[j] = ld_shared_f32(sl + static_cast<uint32_t>(q * 4096) + sw128_offset(16 * part + j, lane >> 2) +
-                                             static_cast<uint32_t>((lane & 3) * 4));
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) av[j] = make_float4(t[4 * j], t[4 * j + 1], t[4 * j + 2], t[4 * j + 3]);
+                    for (int j = 0; j < 32; ++j)
+                        av[j] = ld_shared_f32(sl + static_cast<uint32_t>(q * 4096) + sw128_offset(j, lane >> 2) +
+                                              static_cast<uint32_t>((lane & 3) * 4));
                 } else {
-                    // Chunks 4*part .. 4*part+3 of the swizzled K-major row.
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) av[j] = ld_shared_v4(sl + sw128_offset(arow, 4 * part + j));
+                    for (int j = 0; j < 8; ++j) {
+                        const float4 t = ld_shared_v4(sl + sw128_offset(arow, j));
+                        av[4 * j] = t.x;
+                        av[4 * j + 1] = t.y;
+                        av[4 * j + 2] = t.z;
+                        av[4 * j + 3] = t.w;
+                    }
                 }
-                // B: op(B) = B: rows 4c..4c+3, columns 4g..4g+3 of the unswizzled 32 x 128
+                // B: op(B) = B: rows 4c..4c+3, columns 4g..4g+3 of the unswizzled 32 x 64
                 // staging tile; op(B) = B^T: four 16-byte chunks of the K-major tile.
                 float4 bq[4];
 #pragma unroll
@@ -443,19 +545,13 @@ __global__ void __launch_bounds__(pr::THREADS, 1)
                     off = sw128_offset(4 * g + 3, c);
                     split_store(st + off, st + pr::B_HALF + off, bq[0].w, bq[1].w, bq[2].w, bq[3].w);
                 }
-                const uint32_t ta = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + pr::TMEM_A +
-                                    static_cast<uint32_t>(64 * s + 16 * part);
+                const uint32_t ta =
+                    tmem_base + (static_cast<uint32_t>(32 * q) << 16) + pr::TMEM_A + static_cast<uint32_t>(64 * s);
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {  // 8 values at a time: fewer live registers
+                for (int h = 0; h < 4; ++h) {  // 8 values at a time: fewer live registers
                     float hi[8], lo[8];
-                    split_tf32(av[2 * h].x, hi[0], lo[0]);
-                    split_tf32(av[2 * h].y, hi[1], lo[1]);
-                    split_tf32(av[2 * h].z, hi[2], lo[2]);
-                    split_tf32(av[2 * h].w, hi[3], lo[3]);
-                    split_tf32(av[2 * h + 1].x, hi[4], lo[4]);
-                    split_tf32(av[2 * h + 1].y, hi[5], lo[5]);
-                    split_tf32(av[2 * h + 1].z, hi[6], lo[6]);
-                    split_tf32(av[2 * h + 1].w, hi[7], lo[7]);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) split_tf32(av[8 * h + j], hi[j], lo[j]);
                     tmem_store8(ta + 8 * h, hi);
                     tmem_store8(ta + 32 + 8 * h, lo);
                 }
@@ -463,97 +559,105 @@ __global__ void __launch_bounds__(pr::THREADS, 1)
                 fence_proxy_async_smem();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar((rank == 0 ? pr::OP_FULL : pr::OP_FWD) + s));
+                if (lane == 0) {
+                    if (rank != 0)
+                        st_async_signal(signal_word, bar(pr::OP_FULL + s), 0);  // the even CTA issues the MMAs
+                    else if ((cw & 3) == 0)
+                        mbar_arrive_expect_tx(bar(pr::OP_FULL + s), pr::SIGNAL_BYTES);
+                    else
+                        mbar_arrive(bar(pr::OP_FULL + s));
+                }
             }
         });
     } else {
         // -------------------------------------------------------------- epilogue
         const int q = warp & 3;  // TMEM lane quarter this warp may access
-        const uint32_t stage0 =
-            base + pr::C_STAGE0 + static_cast<uint32_t>((warp - pr::EPI_WARP0) * pr::C_BUFS * pr::C_CHUNK);
-        const int ch0 = ((warp - pr::EPI_WARP0) >> 2) * pr::CHUNKS_PER_WARP;  // this warp's chunks
-        const int ch_end = ch0 + pr::CHUNKS_PER_WARP;
+        const uint32_t rq = base + pr::R0 + static_cast<uint32_t>(q * pr::CHUNKS * pr::C_CHUNK);  // its chunks
         // C may still be in the beta pre-pass launched just before this
         // kernel (programmatic dependent launch): only the epilogue waits.
         asm volatile("griddepcontrol.wait;" ::: "memory");
-        uint32_t unit = 0, nchunk = 0;
-        auto release = [&] {
-            // The accumulator is out of TMEM: one lane per warp frees it on the
+        uint32_t iv = 0;  // fold intervals consumed so far
+        auto release = [&](uint32_t d) {
+            // Accumulator d is out of TMEM: one lane per warp frees it on the
             // even CTA's barrier.
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive_at(bar(pr::ACC_EMPTY), 0);
+            if (lane == 0) mbar_arrive_at(bar(pr::ACC_EMPTY + d), 0);
         };
         for_each_unit_of(a, abort_flag, pair, pairs, [&](int tile, int kb, int ke) {
-            if (!mbar_wait<true>(bar(pr::ACC_FULL), unit & 1, a, abort_flag, WD_EPILOGUE)) return;
-            tc_fence_after();
             const TileAt at = tile_at<pr::PM, pr::PN>(a, tile);
             const int64_t row0 = at.m0 + pr::HM * static_cast<int64_t>(rank) + q * 32;
             const int64_t row = row0 + lane;
             // Stream-K tiles hold beta * C + bias already: every unit adds.
             const bool atomic = tile >= a.dp_tiles;
-            if (a.c_tma) {
-                // Each 32 x 32 chunk inside the matrix: TMEM -> registers ->
-                // (epilogue) -> swizzled staging rows -> one TMA store (or
-                // reduce-add) of the chunk. Chunks that cross the last row or
-                // column use the per-thread stores.
-                const bool fused = a.ep && !atomic;
-                const bool col_bias = a.bias_kind == SGEMM_BIAS_PER_COL;
-                const float alpha = a.alpha;
-                const float rb = (a.bias_kind == SGEMM_BIAS_PER_ROW && row < a.M) ? __ldg(a.bias + row) : 0.0f;
-                float *crow = a.C + at.item * a.strideC + row * a.ldc;
+            const bool fused = a.ep && !atomic;
+            const bool col_bias = a.bias_kind == SGEMM_BIAS_PER_COL;
+            const float rb = (a.bias_kind == SGEMM_BIAS_PER_ROW && row < a.M) ? __ldg(a.bias + row) : 0.0f;
+            float *crow = a.C + at.item * a.strideC + row * a.ldc;
+            // The previous unit's TMA stores read the running sum: wait until
+            // they have, before this unit overwrites it.
+            if (lane == 0) bulk_wait_read<0>();
+            __syncwarp();
+            for (int k0 = kb; k0 < ke; k0 += pr::FOLD_KB) {
+                const bool first = k0 == kb, last = ke - k0 <= pr::FOLD_KB;
+                const uint32_t d = iv & 1;
+                if (!mbar_wait<true>(bar(pr::ACC_FULL + d), (iv >> 1) & 1, a, abort_flag, WD_EPILOGUE)) return;
+                tc_fence_after();
+                ++iv;
+                const uint32_t dt = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + d * pr::PN;
 #pragma unroll 1
-                for (int ch = ch0; ch < ch_end; ++ch) {
-                    const uint32_t taddr =
-                        tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(ch * 32);
+                for (int ch = 0; ch < pr::CHUNKS; ++ch) {
+                    const uint32_t rc = rq + static_cast<uint32_t>(ch * pr::C_CHUNK);
                     const int64_t col0 = at.n0 + ch * 32;
-                    const bool last = ch == ch_end - 1;
-                    if (col0 + 32 > a.N || row0 + 32 > a.M) {
-                        edge_chunk<VEC_C>(a, taddr, crow, row, col0, atomic, last, bar(pr::ACC_EMPTY));
+                    if (last && (!a.c_tma || col0 + 32 > a.N || row0 + 32 > a.M)) {
+                        edge_final_chunk<VEC_C>(a, dt + static_cast<uint32_t>(ch * 32), rc, first, crow, row, col0,
+                                                atomic, ch == pr::CHUNKS - 1, bar(pr::ACC_EMPTY + d));
                         continue;
                     }
-                    const uint32_t buf = stage0 + (nchunk % pr::C_BUFS) * pr::C_CHUNK;
-                    ++nchunk;
-                    // Per-column bias of this chunk: lane l holds column col0 + l.
-                    const float bl = (fused && col_bias) ? __ldg(a.bias + col0 + lane) : rb;
-                    if (lane == 0) bulk_wait_read<pr::C_BUFS - 1>();  // the store C_BUFS chunks back has read this buffer
-                    __syncwarp();
-                    if (fused) {
-                        float v[16];
-                        tmem_load16(taddr, v);
-                        stage16_fused(a.act, buf, lane, 0, alpha, col_bias, bl, v);
-                        tmem_load16(taddr + 16, v);
-                        if (last) release();
-                        stage16_fused(a.act, buf, lane, 16, alpha, col_bias, bl, v);
-                    } else {
-                        float v[32];
-                        tmem_load32(taddr, v);
-                        if (last) release();
+                    float v[32];
+                    tmem_load32(dt + static_cast<uint32_t>(ch * 32), v);
+                    if (ch == pr::CHUNKS - 1) release(d);
+                    if (!first) {
 #pragma unroll
-                        for (int j = 0; j < 32; j += 4)
-                            st_shared_v4(buf + sw128_offset(lane, j >> 2), alpha * v[j], alpha * v[j + 1],
-                                         alpha * v[j + 2], alpha * v[j + 3]);
+                        for (int j = 0; j < 8; ++j) {
+                            const float4 r = ld_shared_v4(rc + sw128_offset(lane, j));
+                            v[4 * j] += r.x;
+                            v[4 * j + 1] += r.y;
+                            v[4 * j + 2] += r.z;
+                            v[4 * j + 3] += r.w;
+                        }
                     }
-                    fence_proxy_async_smem();  // staging writes -> visible to the TMA engine
+                    if (!last) {
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            st_shared_v4(rc + sw128_offset(lane, j), v[4 * j], v[4 * j + 1], v[4 * j + 2],
+                                         v[4 * j + 3]);
+                        continue;
+                    }
+                    // The unit's sum is complete: write this chunk of C.
+                    if (fused) {
+                        // Per-column bias of this chunk: lane l holds column col0 + l.
+                        const float bl = col_bias ? __ldg(a.bias + col0 + lane) : rb;
+                        stage32_fused(a.act, rc, lane, a.alpha, col_bias, bl, v);
+                    } else {
+                        const float alpha = a.alpha;
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            st_shared_v4(rc + sw128_offset(lane, j), alpha * v[4 * j], alpha * v[4 * j + 1],
+                                         alpha * v[4 * j + 2], alpha * v[4 * j + 3]);
+                    }
+                    fence_proxy_async_smem();  // chunk writes -> visible to the TMA engine
                     __syncwarp();
                     if (lane == 0) {
                         const int x = static_cast<int>(col0), y = static_cast<int>(row0);
                         if (atomic)
-                            tma_reduce_add_3d(&tmC, x, y, at.item, buf);
+                            tma_reduce_add_3d(&tmC, x, y, at.item, rc);
                         else
-                            tma_store_3d(&tmC, x, y, at.item, buf);
+                            tma_store_3d(&tmC, x, y, at.item, rc);
                         bulk_commit();
                     }
                 }
-            } else {
-                float *crow = a.C + at.item * a.strideC + row * a.ldc;
-#pragma unroll 1
-                for (int ch = ch0; ch < ch_end; ++ch)
-                    epilogue_chunk_then<VEC_C>(
-                        a, tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(ch * 32), crow,
-                        row, at.n0 + ch * 32, atomic, ch == ch_end - 1, release);
             }
-            ++unit;
         });
         if (lane == 0) bulk_wait<0>();  // every store of this warp has landed
     }
@@ -637,9 +741,10 @@ int launch_pair(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStream
     if (tiles_m * tiles_n * p.batch > INT32_MAX / 2 || k_blocks > INT32_MAX / 2) return SGEMM_ERR_UNSUPPORTED;
     const int tiles = static_cast<int>(tiles_m * tiles_n * p.batch);
     // One pair per two SMs, as many pairs as fit at once. A stream-K share
-    // below 4 k-blocks costs more in fix-up than it saves.
-    const bool long_k = k_blocks > 2 * KB_CAP;  // every tile split, units of <= KB_CAP k-blocks
-    const Schedule sch = make_schedule(tiles, k_blocks, clusters, long_k ? SK_ALL : sk_mode, 4, 0.25);
+    // below 4 k-blocks costs more in fix-up than it saves. Accumulation
+    // chains are bounded by the folds inside the kernel, so units may span
+    // any number of k-blocks.
+    const Schedule sch = make_schedule(tiles, k_blocks, clusters, sk_mode, 4, 0.25);
     const int split = tiles - sch.dp_tiles;
     int rc = split_tiles_prepare(p, pr::PM, pr::PN, static_cast<int>(tiles_n), static_cast<int>(tiles_m * tiles_n),
                                  sch.dp_tiles, split, stream, launches);
@@ -669,8 +774,8 @@ int launch_pair(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStream
     a.bias_kind = p.bias_kind;
     a.act = p.act;
     a.ep = p.has_epilogue();
-    a.kb_cap = long_k ? KB_CAP : 0;
-    count_switches(a, pr::SWITCH_KB);
+    a.kb_cap = 0;
+    a.sk_switch_kb = 0;  // a unit switch costs no MMA time: the accumulators alternate
     a.signal_dependents = (split > 0 && p.act != SGEMM_ACT_NONE) ? 1 : 0;
     a.c_tma = c_tma ? 1 : 0;
     cfg.gridDim = dim3(2 * sch.grid);

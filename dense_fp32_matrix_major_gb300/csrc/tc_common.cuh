@@ -22,12 +22,16 @@ constexpr int B_TILE = BN * BK * 4;         // bytes of one B tile (hi or lo)
 constexpr int EPILOGUE_WARPS = 4;
 constexpr int TMEM_COLS = 512;
 constexpr int BAR_BYTES = 128;
-// The tensor core's fp32 accumulation in TMEM rounds toward zero, so its
-// error grows with the number of k-blocks one accumulator sums. Products
-// with more than 2 * KB_CAP k-blocks (K > 8192) are split along K into
-// units of at most KB_CAP k-blocks (K = 4096, normalised error ~3e-6), whose
-// partial sums are added into C with round-to-nearest fp32 adds.
-constexpr int KB_CAP = 128;
+// The tensor core adds each MMA's products into the fp32 accumulator in TMEM
+// with truncation (measured on GB300: about one unit in the last place of
+// the running sum lost per tcgen05.mma, all in the same direction when the
+// terms share a sign). The error therefore grows with the number of MMAs
+// that one accumulator chains, whatever K is: ~6.7e-7 of sum |a||b| per
+// 32-deep k-block (12 MMAs) on non-negative inputs. Products with more than
+// KB_CAP k-blocks are split along K into units of at most KB_CAP k-blocks
+// (~5.4e-6 on non-negative inputs), whose partial sums are added into C
+// with round-to-nearest fp32 adds.
+constexpr int KB_CAP = 8;
 
 // Watchdog codes (which wait gave up).
 enum : int { WD_PRODUCER = 1, WD_MMA_FULL = 2, WD_MMA_ACC = 3, WD_EPILOGUE = 4, WD_DRAIN = 5, WD_SELFTEST = 6 };
@@ -150,6 +154,35 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Whether the phase with the given parity has completed, without waiting
+// (test_wait never suspends the thread).
+template <bool CLUSTER = false>
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    if (CLUSTER) {
+        asm volatile(
+            "{\n"
+            " .reg .pred p;\n"
+            " mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+            " selp.u32 %0, 1, 0, p;\n"
+            "}\n"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity)
+            : "memory");
+    } else {
+        asm volatile(
+            "{\n"
+            " .reg .pred p;\n"
+            " mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+            " selp.u32 %0, 1, 0, p;\n"
+            "}\n"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity)
+            : "memory");
+    }
+    return ok != 0;
+}
+
 // Wait for the phase with the given parity to complete, within the time
 // limit; false if the limit passed or another role already aborted.
 template <bool CLUSTER = false>
@@ -168,6 +201,19 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const A
             }
         }
     }
+}
+
+// True in exactly one lane of the (converged, full) warp.
+__device__ __forceinline__ bool elect_one() {
+    uint32_t e;
+    asm volatile(
+        "{\n"
+        " .reg .pred p;\n"
+        " elect.sync _|p, 0xffffffff;\n"
+        " selp.u32 %0, 1, 0, p;\n"
+        "}\n"
+        : "=r"(e));
+    return e != 0;
 }
 
 __device__ __forceinline__ void fence_proxy_async_smem() {

@@ -13,7 +13,11 @@ The shapes follow the workloads that the source pages time:
 * M = 2048, K = 4096, N = 3072 with N(0, 1) entries, the benchmark shape of
   "CUDA算子优化(4)：矩阵乘法" (host driver of the V1 and V2 kernels);
 * a ragged 1023 x 1537 x 2049 case whose row lengths are not multiples of
-  four floats, so no 16-byte vector path applies.
+  four floats, so no 16-byte vector path applies;
+* non-negative entries, U[0, 1) as the complete program of "CUDA内存优化入门：
+  从Naive到Tiled矩阵乘法" section 八 initialises its matrices (rand() /
+  RAND_MAX), and |N(0, 1)|: every product then has the same sign, so
+  rounding errors that lean one way add up instead of cancelling.
 
 Random entries come from numpy's PCG64 generator (``np.random.default_rng``),
 which gives the same stream on every platform, drawn in float64 and rounded
@@ -33,7 +37,7 @@ class Workload:
     M: int
     N: int
     K: int
-    dist: str  # "normal", "uniform", "ones", "int4" (integers in [-4, 4])
+    dist: str  # "normal", "uniform", "uniform01", "absnormal", "ones", "int4" (integers in [-4, 4])
     seed: int = 0
     lda: int | None = None  # row strides in elements; None = dense rows
     ldb: int | None = None
@@ -66,6 +70,11 @@ def _draw(rng: np.random.Generator, shape, dist: str) -> np.ndarray:
         return rng.standard_normal(shape).astype(np.float32)
     if dist == "uniform":
         return (rng.random(shape) * 2.0 - 1.0).astype(np.float32)
+    if dist == "uniform01":
+        # U[0, 1): the pages' rand() / RAND_MAX initialisation, non-negative
+        return rng.random(shape).astype(np.float32)
+    if dist == "absnormal":
+        return np.abs(rng.standard_normal(shape)).astype(np.float32)
     if dist == "ones":
         return np.ones(shape, dtype=np.float32)
     if dist == "int4":
@@ -96,6 +105,12 @@ def make_inputs(w: Workload):
 def make_pair(M: int, N: int, K: int, dist: str = "normal", seed: int = 0):
     """(A, B) for an ad-hoc shape with dense rows."""
     return make_inputs(Workload(f"adhoc_{M}x{N}x{K}", M, N, K, dist, seed))
+
+
+def make_mixed(M: int, N: int, K: int, dist_a: str, dist_b: str, seed: int = 0):
+    """(A, B) with A drawn from ``dist_a`` and B from ``dist_b`` (dense rows)."""
+    rng = np.random.default_rng(seed)
+    return _draw(rng, (M, K), dist_a), _draw(rng, (K, N), dist_b)
 
 
 def sample_positions(M: int, N: int, count: int, seed: int = 0):

@@ -164,39 +164,42 @@ def test_status_codes_on_device(lib):
 # ------------------------------------------------------------- benchmark configs
 
 
-def _config_error(C, A, B, w):
-    if w.M * w.N * w.K <= 1024 ** 3:
-        return oracle_error(C, A, B)
-    # Full sizes beyond the oracle's budget: a band of full rows (every column
-    # tile and the last, ragged one) plus seeded samples over the whole box.
-    band = 32
-    C64, S = oracle.sgemm_f64_rows(A, B, w.M - band, w.M)
-    err_band = oracle.normalized_error(C[w.M - band:], C64, S)
-    r, c = wl.sample_positions(w.M, w.N, 4000, seed=w.seed)
-    return max(err_band, sampled_error(C, A, B, r, c))
+_config_oracle = {}
+
+
+def _config_reference(w):
+    """(A, B, C64, S) of a benchmark workload: the full double product from the
+    threaded oracle, computed once per workload and shared by every variant."""
+    if w.name not in _config_oracle:
+        A, B = wl.make_inputs(w)
+        C64, S = oracle.sgemm_f64_rows(A, B)
+        _config_oracle[w.name] = (A, B, C64, S)
+    return _config_oracle[w.name]
 
 
 @pytest.mark.parametrize("w", wl.ALL, ids=lambda w: w.name)
 @pytest.mark.parametrize("variant,tc", [("auto", 0), ("ffma", 0), ("tf32x3", 3), ("tf32x3", 2), ("tf32x3", 1),
                                         ("tf32x3", 4)])
 def test_benchmark_configs(lib, w, variant, tc):
+    """Every output of every benchmark configuration against the oracle (the
+    headline is the shape of "CUDA算子优化(4)：矩阵乘法", host code of the V1
+    kernel: M = 2048, K = 4096, N = 3072)."""
     _apply(lib, (variant, 0, 0, tc))
-    A, B = wl.make_inputs(w)
+    A, B, C64, S = _config_reference(w)
     C, flat, rc = run_sgemm(A, B, lda=w.lda, ldb=w.ldb, ldc=w.ldc)
     assert rc == 0
     assert outside_box_intact(flat, w.M, w.N, w.ldc or w.N, 0)
     if w.dist == "ones":
         assert np.all(C == np.float32(w.K))  # the page's closed form: every output is K
-    else:
-        err = _config_error(C, A, B, w)
-        assert err <= TOL, err
+    err = oracle.normalized_error(C, C64, S)
+    assert err <= TOL, err
 
 
 def test_from_host_entry_point(lib):
     import torch
 
     w = wl.C3_RAGGED
-    A, B = wl.make_inputs(w)
+    A, B, _, _ = _config_reference(w)
     Ah = torch.from_numpy(A).pin_memory()
     Bh = torch.from_numpy(B).pin_memory()
     Ch = torch.full((w.M, w.N), float("nan")).pin_memory()
@@ -204,8 +207,8 @@ def test_from_host_entry_point(lib):
     lib.set_variant(0)
     lib.sgemm_f32_from_host(Ah, Bh, Ch, dA, dB, dC)
     torch.cuda.synchronize()
-    r, c = wl.sample_positions(w.M, w.N, 2000, seed=1)
-    assert sampled_error(Ch.numpy(), A, B, r, c) <= TOL
+    _, _, C64, S = _config_reference(w)
+    assert oracle.normalized_error(Ch.numpy(), C64, S) <= TOL
 
 
 @pytest.mark.parametrize("w", [wl.C5_HEAD, wl.C4_2048], ids=lambda w: w.name)
@@ -215,7 +218,7 @@ def test_from_host_pipelined_on_side_stream(lib, w):
     stream's later work, and every panel, the last one included, is right."""
     import torch
 
-    A, B = wl.make_inputs(w)
+    A, B, _, _ = _config_reference(w)
     Ah = torch.from_numpy(A).pin_memory()
     Bh = torch.from_numpy(B).pin_memory()
     Ch = torch.full((w.M, w.N), float("nan")).pin_memory()
@@ -227,12 +230,8 @@ def test_from_host_pipelined_on_side_stream(lib, w):
         lib.sgemm_f32_from_host(Ah, Bh, Ch, dA, dB, dC, stream=side)
         side.synchronize()
         C = Ch.numpy()
-        assert np.all(np.isfinite(C))
-        r, c = wl.sample_positions(w.M, w.N, 1500, seed=2)
-        assert sampled_error(C, A, B, r, c) <= TOL
-        # Every column (all panels), densely, on a band of rows.
-        C64, S = oracle.sgemm_f64_rows(A, B, 0, 16)
-        assert oracle.normalized_error(C[:16], C64, S) <= TOL
+        _, _, C64, S = _config_reference(w)
+        assert oracle.normalized_error(C, C64, S) <= TOL  # every panel, every output
 
 
 def test_repeat_calls_are_stable(lib):
@@ -247,8 +246,9 @@ def test_repeat_calls_are_stable(lib):
 
 
 def test_tf32x3_long_k_margin(lib):
-    """The tensor-core path rounds each accumulation toward zero, so its error
-    grows with K; at K = 8192 it must still meet the bound."""
+    """The tensor core truncates each accumulation, so a long chain of MMAs
+    into one accumulator would drift; at K = 8192 the result must still meet
+    the bound."""
     _apply(lib, ("tf32x3", 0, 0))
     A, B = wl.make_pair(256, 512, 8192, "normal", 88)
     C, flat, rc = run_sgemm(A, B)
@@ -260,9 +260,10 @@ def test_tf32x3_long_k_margin(lib):
 @pytest.mark.parametrize("variant,tc", [("auto", 0), ("tf32x3", 1), ("tf32x3", 3), ("tf32x3", 4)])
 @pytest.mark.parametrize("K", [8193, 20000, 40000])
 def test_tf32x3_beyond_k_8192(lib, variant, tc, K):
-    """Past K = 8192 the tensor-core kernels split every tile along K into
-    units of at most 4096, so the error stays at the K = 4096 level however
-    long K gets (without the split it grows about linearly with K)."""
+    """However long K gets, no tensor-core accumulator chains more than a
+    few k-blocks of MMAs before its value is added, rounded to nearest, into
+    an fp32 sum, so the error stays at the short-K level (one accumulator
+    over all of K would drift about linearly with K)."""
     _apply(lib, (variant, 0, 0, tc))
     M, N = 256, 512
     A, B = wl.make_pair(M, N, K, "normal", K)
