@@ -9,13 +9,22 @@ written between timed steps to flush L2; only the product is inside the
 CUDA events.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--variant auto|ffma|tf32x3] [--workload NAME] [--all-configs]
+                    [--variant auto|ffma|tf32x3] [--workload NAME] [--no-extras]
+                    [--batched] [--fused]
 
-Prints one JSON line (rank 0). With N > 1 (torchrun, one process per GPU)
-every rank runs its own replica of the workload: the product does not shard
-with a data-path exchange, so there is no collective beyond the timing
-barrier and the max-over-ranks reduction. ``--impl reference`` times the CPU
-oracle (the pages' float triple loop) on a bounded row sample instead.
+Prints the headline JSON line first (rank 0): every output of the timed
+product is compared with the CPU oracle, ``cpu_baseline`` is the oracle's
+float loop (i-k-j order, bit-identical to the pages' i-j-k loop) on all host
+cores over a bounded row sample, and ``e2e`` goes through host buffers. With
+one GPU further lines follow (unless --no-extras): one per other benchmark
+configuration (every output checked), the pages' single-thread CPU loop at
+512^3 and 1024^3 and the 1024^2 all-ones product end to end, each beside the
+figure the pages print for their own hardware. With N > 1 (torchrun, one
+process per GPU) every rank runs its own replica of the workload: the product
+does not shard with a data-path exchange, so there is no collective beyond
+the timing barrier and the max-over-ranks reduction. ``--impl reference``
+times the CPU oracle (the pages' float loop, threaded) on a bounded row
+sample instead.
 """
 
 from __future__ import annotations
@@ -49,6 +58,18 @@ GB300_MAX_SM_MHZ = 2070.0
 FALLBACK_BF16_TFLOPS = 1900.0
 FALLBACK_HBM_GBS = 6800.0
 TF32_OVER_BF16 = 1.1 / 2.25
+# Tensor-pipe rate of kind::tf32 MMAs on GB300 read from the ncu pipe counters
+# (and matched by a microbenchmark of back-to-back 256 x 256 x 8 and 256 x 128
+# x 8 tcgen05.mma: 1936 multiply-adds per cycle per SM at the nominal 2.07 GHz,
+# i.e. 2048 at the clock the events saw): the ceiling at the sampled clock.
+TF32_MACS_PER_CLK_PER_SM = 2048
+# The pages' own numbers, quoted beside ours (other hardware, context only):
+# "CUDA内存优化入门：从Naive到Tiled矩阵乘法" section 四, the CPU triple loop on an
+# i7: ~450 ms at 512^3 and ~3600 ms at 1024^3; "CUDA 性能优化实战笔记 + C++示例
+# 代码（第七章重点）" section 一, the 1024^2 all-ones program timed end to end
+# (copies included) on an RTX 2060: 47.33 ms Debug, 33.37 ms Release.
+PAGE_CPU_MS = {512: 450.0, 1024: 3600.0}
+PAGE_E2E_MS_1024 = 33.37
 
 
 def _dist_env():
@@ -167,6 +188,13 @@ def _tf32x3_peak_tflops():
     return FALLBACK_BF16_TFLOPS * TF32_OVER_BF16 / 3.0, "fallback bf16 1.9 PF x 1.1/2.25 / 3"
 
 
+def _tf32x3_pipe_ceiling(sm_count: int, sm_mhz: float):
+    """fp32-equivalent ceiling from the measured tensor-pipe rate at the sampled clock."""
+    tflops = sm_count * TF32_MACS_PER_CLK_PER_SM * 2 * sm_mhz * 1e6 / 1e12 / 3.0
+    return tflops, (f"{sm_count} SMs x {TF32_MACS_PER_CLK_PER_SM} tf32 MAC/clk (ncu pipe counters) x 2 x "
+                    f"{sm_mhz:.0f} MHz sampled / 3 products")
+
+
 def _hbm_peak_gbs():
     peaks = _measured_peaks()
     if peaks and peaks.get("hbm_gbs"):
@@ -210,7 +238,10 @@ def _device_inputs(w, torch, device):
     return A, B, dA, dB, dC
 
 
-def run_ours(args, w, torch, dist):
+def run_ours(args, w, torch, dist, full_parity: bool = False, with_e2e: bool = True):
+    """Time sgemm_f32 on workload w (inputs resident in HBM, L2 flushed
+    between steps) and check its output against the oracle: every output
+    when full_parity, else seeded samples."""
     from dense_fp32_matrix_major_gb300 import sgemm
 
     ws, rank, local = _dist_env()
@@ -264,28 +295,44 @@ def run_ours(args, w, torch, dist):
     ms_max = max_over_ranks(ms, dist, device)
     value = job_gflops(ws, w.flops, ms_max)
 
-    # Parity spot check of the timed output (cheap, sampled; not timed).
-    import oracle  # test infrastructure: used here only to spot-check the result
-    r, c = wl.sample_positions(w.M, w.N, 64, seed=99)
-    c64, s = oracle.sgemm_f64_at(A, B, r, c)
-    err = oracle.normalized_error(dC.cpu().numpy()[r, c], c64, s)
+    # Parity check of the timed output (not timed): every output against the
+    # threaded double oracle, or seeded samples.
+    import oracle  # test infrastructure: used here only to check the result
+    Cgot = dC.cpu().numpy()
+    if full_parity:
+        C64, S = oracle.sgemm_f64_rows(np.ascontiguousarray(A), np.ascontiguousarray(B))
+        err = oracle.normalized_error(Cgot, C64, S)
+        parity = {"err": err, "compared": "every output", "bound": 1e-5}
+        if w.dist == "ones":
+            parity["all_equal_K"] = bool(np.all(Cgot == np.float32(w.K)))
+    else:
+        r, c = wl.sample_positions(w.M, w.N, 64, seed=99)
+        c64, s = oracle.sgemm_f64_at(A, B, r, c)
+        err = oracle.normalized_error(Cgot[r, c], c64, s)
+        parity = {"err": err, "compared": f"{len(r)} sampled outputs", "bound": 1e-5}
 
     # End to end: host buffers through the C ABI, copies inside the timed region.
-    e2e = run_e2e(args, w, torch, sgemm, A, B, device, dist, ws)
+    e2e = run_e2e(args, w, torch, sgemm, A, B, device, dist, ws) if with_e2e else None
 
     clocks = sampler.summary(wall0, wall1 + 0.12)
     sm_max = clocks["sm_max_mhz"] or GB300_MAX_SM_MHZ
     sm_count = torch.cuda.get_device_properties(device).multi_processor_count
+    pipe = None
     if variant_used == "tf32x3":
         peak, peak_src = _tf32x3_peak_tflops()
         bound = "tensor"
         kernel_key = tc_kernel
+        clk = clocks["sm_mhz"] or GB300_MAX_SM_MHZ
+        pipe_peak, pipe_src = _tf32x3_pipe_ceiling(sm_count, clk)
     else:
         peak = sm_count * FP32_LANES_PER_SM * 2 * sm_max * 1e6 / 1e12
         peak_src = f"{sm_count} SMs x 128 FP32 lanes x 2 x {sm_max:.0f} MHz (recipe unit counts)"
         bound = "alu"
         kernel_key = "ffma_kernel"
     achieved = w.flops / (ms * 1e-3) / 1e12
+    if variant_used == "tf32x3":
+        pipe = {"peak": round(pipe_peak, 3), "frac": round(achieved / pipe_peak, 4), "unit": "TFLOP/s",
+                "peak_source": pipe_src}
     traffic = _traffic_record(kernel_key)
     hbm_peak, hbm_src = _hbm_peak_gbs()
     algo_gbs = w.algorithmic_bytes / (ms * 1e-3) / 1e9
@@ -303,6 +350,7 @@ def run_ours(args, w, torch, dist):
         "bound": bound, "achieved": round(achieved, 3), "peak": round(peak, 3), "unit": "TFLOP/s",
         "frac": round(achieved / peak, 4), "traffic": traffic, "kernel": kernel_key, "hbm": hbm,
         "fp32_ffma_peak": fp32_ffma,
+        "tensor_pipe_ceiling": pipe,
         "peak_source": peak_src,
         "algorithmic_flops_per_launch": w.flops,
         "timing": "CUDA events around each sgemm_f32 call on its stream (includes the small "
@@ -312,7 +360,7 @@ def run_ours(args, w, torch, dist):
         "value": value, "ms_per_step": ms_max, "wall_s": wall, "variant": variant_used,
         "launches_per_step": launches_per_step, "per_step_ms_min": min(per_step),
         "per_step_ms_median": statistics.median(per_step), "roofline": roofline, "e2e": e2e,
-        "clocks": clocks, "parity_sampled_err": err,
+        "clocks": clocks, "parity": parity, "kernel": kernel_key,
     }
 
 
@@ -441,25 +489,46 @@ def _host_inputs(w):
 
 
 def cpu_oracle_sample(w, budget_s: float):
-    """Time the oracle's float loop (one thread) on the first rows of the workload."""
+    """Time the oracle's float twin (the pages' loop arithmetic in i-k-j order,
+    threaded by rows, bit-identical to their i-j-k loop) on all host cores,
+    on the first rows of the workload, about budget_s seconds of work."""
     import oracle  # test infrastructure: timed here as the CPU baseline
 
     A, B = _host_inputs(w)
-    rows = 1
+    A = np.ascontiguousarray(A)
+    B = np.ascontiguousarray(B)
+    cores = os.cpu_count() or 1
+    rows = min(w.M, cores)
     t0 = time.perf_counter()
-    oracle.sgemm_f32(np.ascontiguousarray(A[:rows]), B)
+    oracle.sgemm_f32_rows(A, B, 0, rows, nthreads=cores)
     t1 = time.perf_counter() - t0
-    rows = int(max(1, min(w.M, budget_s / max(t1, 1e-6))))
+    rows = int(max(1, min(w.M, rows * budget_s / max(t1, 1e-6))))
     t0 = time.perf_counter()
-    oracle.sgemm_f32(np.ascontiguousarray(A[:rows]), B)
+    oracle.sgemm_f32_rows(A, B, 0, rows, nthreads=cores)
     secs = time.perf_counter() - t0
     flops = 2 * rows * w.N * w.K
     return {
-        "value": round(flops / secs / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
-        "sample": f"rows 0..{rows - 1} of A ({rows} x {w.K}) times all of B ({w.K} x {w.N}): "
-                  f"the float i-j-k loop, one thread, {secs:.1f} s",
+        "value": round(flops / secs / 1e9, 4), "unit": UNIT, "cores": min(cores, rows), "kind": "oracle",
+        "sample": f"rows 0..{rows - 1} of A ({rows} x {w.K}) times all of B ({w.K} x {w.N}): the float "
+                  f"loop in i-k-j order (bit-identical to the i-j-k loop), {min(cores, rows)} threads, "
+                  f"{secs:.1f} s",
         "seconds": round(secs, 2),
     }
+
+
+def cpu_pages_loop(n: int):
+    """The pages' single-thread i-j-k float loop over a whole n^3 product (as
+    their section 四 times it on an i7), for comparison with their figure."""
+    import oracle  # test infrastructure: timed here as the pages' CPU loop
+
+    A, B = wl.make_pair(n, n, n, "uniform01", 0)
+    t0 = time.perf_counter()
+    oracle.sgemm_f32(A, B)
+    ms = (time.perf_counter() - t0) * 1e3
+    return {"line": "pages_cpu_loop", "workload": f"sq{n}_uniform01", "ms": round(ms, 1),
+            "value": round(2.0 * n ** 3 / (ms * 1e-3) / 1e9, 4), "unit": UNIT, "cores": 1,
+            "kind": "oracle (float i-j-k loop, one thread)",
+            "page_ms": PAGE_CPU_MS[n], "page_hardware": "Intel i7 (\"CUDA内存优化入门\" section 四)"}
 
 
 def run_reference(args, w):
@@ -481,11 +550,12 @@ def run_reference(args, w):
         "ms_per_step": round(2 * w.M * w.N * w.K / (value * 1e9) * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic", "config": _config(w, "oracle"),
-        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": r["cores"], "kind": "oracle",
                          "sample": r["sample"]},
         "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
-        "note": "the CPU oracle (float triple loop of the source pages), timed on a bounded row "
-                "sample each step; ms_per_step is the full workload extrapolated from the rate",
+        "note": "the CPU oracle (the source pages' float loop, in i-k-j order and threaded by rows, "
+                "bit-identical to their i-j-k loop), timed on a bounded row sample each step on all host "
+                "cores; ms_per_step is the full workload extrapolated from the rate",
     }
 
 
@@ -494,6 +564,45 @@ def _config(w, variant):
             "layout": "row-major fp32, lda=K, ldb=N, ldc=N", "variant": variant,
             "l2": "flushed between timed steps (256 MiB write); inputs+output 109 MB < 129 MB L2",
             "parallelism": "replicas (one independent product per GPU)"}
+
+
+def print_extras(args, headline, torch):
+    """One line per other benchmark configuration (every output checked), the
+    pages' single-thread CPU loop at 512^3 and 1024^3, and the 1024^2 all-ones
+    product end to end beside the pages' figure."""
+    from dense_fp32_matrix_major_gb300 import sgemm
+
+    for other in wl.ALL:
+        if other is headline:
+            continue
+        sub = argparse.Namespace(**vars(args))
+        sub.steps = min(args.steps, 200)
+        r = run_ours(sub, other, torch, None, full_parity=True, with_e2e=False)
+        roof = r["roofline"]
+        print(json.dumps({
+            "line": "config", "workload": other.name, "config": _config(other, r["variant"]),
+            "value": round(r["value"], 2), "unit": UNIT, "ms_per_step": round(r["ms_per_step"], 5),
+            "variant": r["variant"], "kernel": r["kernel"], "launches_per_step": r["launches_per_step"],
+            "roofline_frac": roof["frac"], "roofline_peak": roof["peak"],
+            "tensor_pipe_frac": roof["tensor_pipe_ceiling"]["frac"] if roof["tensor_pipe_ceiling"] else None,
+            "fp32_ffma_frac": roof["fp32_ffma_peak"]["frac"], "parity": r["parity"],
+            "clocks": r["clocks"]}), flush=True)
+    for n in (512, 1024):
+        print(json.dumps(cpu_pages_loop(n)), flush=True)
+    # The all-ones 1024^2 product through host buffers, copies included, as the
+    # pages time their program end to end.
+    ones = wl.C2_ONES
+    A, B = _host_inputs(ones)
+    device = torch.device("cuda", torch.cuda.current_device())
+    sub = argparse.Namespace(**vars(args))
+    sgemm.set_variant(args.variant)
+    e = run_e2e(sub, ones, torch, sgemm, A, B, device, None, 1)
+    print(json.dumps({"line": "pages_e2e", "workload": ones.name, "ms": e["ms_per_step"], "value": e["value"],
+                      "unit": UNIT, "h2d_bytes_per_step": e["h2d_bytes_per_step"],
+                      "d2h_bytes_per_step": e["d2h_bytes_per_step"], "path": e["path"],
+                      "page_ms": PAGE_E2E_MS_1024,
+                      "page_hardware": "RTX 2060 (\"CUDA 性能优化实战笔记\" section 一, Release build)"}),
+          flush=True)
 
 
 def main():
@@ -509,8 +618,11 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-step-seconds", type=float, default=4.0)
-    ap.add_argument("--all-configs", action="store_true",
-                    help="also print one extra line per workload (not the headline line)")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="print only the headline line (by default, with one GPU, one more line per "
+                         "benchmark configuration, the pages' CPU loop at 512^3 and 1024^3, and the "
+                         "1024^2 all-ones product end to end follow it)")
+    ap.add_argument("--all-configs", action="store_true", help=argparse.SUPPRESS)  # the default now
     ap.add_argument("--batched", action="store_true",
                     help="also print one extra line per strided-batched workload")
     ap.add_argument("--fused", action="store_true",
@@ -535,7 +647,7 @@ def main():
         torch.cuda.set_device(local)
         tdist.init_process_group("nccl")
         dist = tdist
-    res = run_ours(args, w, torch, dist)
+    res = run_ours(args, w, torch, dist, full_parity=(ws == 1))
     if rank == 0:
         line = {
             "metric": METRIC, "value": round(res["value"], 2), "unit": UNIT, "n_gpus": ws,
@@ -549,21 +661,12 @@ def main():
             "clocks": res["clocks"],
             "per_step_ms": {"mean": round(res["ms_per_step"], 5), "min": round(res["per_step_ms_min"], 5),
                             "median": round(res["per_step_ms_median"], 5)},
-            "parity_sampled_err": res["parity_sampled_err"],
+            "parity": res["parity"],
         }
         line["cpu_baseline"] = cpu_oracle_sample(w, args.cpu_seconds) if ws == 1 else None
         print(json.dumps(line), flush=True)
-        if args.all_configs:
-            for other in wl.ALL:
-                if other is w:
-                    continue
-                sub = argparse.Namespace(**vars(args))
-                sub.steps = min(args.steps, 200)
-                r = run_ours(sub, other, torch, None)
-                print(json.dumps({"workload": other.name, "value": round(r["value"], 2), "unit": UNIT,
-                                  "ms_per_step": round(r["ms_per_step"], 5), "variant": r["variant"],
-                                  "roofline_frac": r["roofline"]["frac"],
-                                  "parity_sampled_err": r["parity_sampled_err"]}), flush=True)
+        if ws == 1 and not args.no_extras:
+            print_extras(args, w, torch)
         if args.batched:
             for bw in wl.BATCHED:
                 print(json.dumps(run_batched_bench(args, bw, torch)), flush=True)

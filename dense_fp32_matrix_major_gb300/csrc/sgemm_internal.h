@@ -123,8 +123,10 @@ int scale_launch(const Problem &p, const DeviceInfo &dev, cudaStream_t stream, i
 // cannot run the request.
 bool tf32x3_supports(const Problem &p, const DeviceInfo &dev);
 int tf32x3_launch(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStream_t stream, int *launches);
-// The SM-pair kernel (op(A) = A, op(B) = B, TMA-compatible operands only).
-int tf32x3_pair_launch(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStream_t stream, int *launches);
+// The SM-pair kernel (every operand form; cpa: A and B rows not 16-byte
+// aligned, loaded with cp.async instead of TMA).
+int tf32x3_pair_launch(const Problem &p, const DeviceInfo &dev, int sk_mode, bool cpa, cudaStream_t stream,
+                       int *launches);
 
 // Watchdog flag shared by kernels with bounded waits (one per device, in the
 // tf32x3 translation unit). Read-and-clear; returns 0 or the first recorded code.

@@ -19,8 +19,11 @@
 //
 // Layout and roles (one persistent CTA per SM, 13 warps):
 //   * Block tile 128 x 256 of C, k-block 32. The 128 x 256 fp32 accumulator
-//     lives in TMEM (256 of the 512 columns; two buffers, so the epilogue of
-//     one tile overlaps the main loop of the next).
+//     lives in TMEM (columns 0-255) and is restarted every FOLD_KB k-blocks:
+//     the epilogue warps add it, rounded to nearest, into a running sum of
+//     the tile in columns 256-511 (the tensor core truncates as it
+//     accumulates, so no accumulator may chain many MMAs), and the MMAs of
+//     the next interval wait for that fold.
 //   * Warps 1-8 (producers) read a k-block of A (128 x 32) and B (32 x 256)
 //     from global memory (any alignment; 16-byte loads where the rows allow,
 //     unguarded loads for k-blocks inside the matrices), split
@@ -87,7 +90,7 @@ __global__ void __launch_bounds__(THREADS, 1) tf32x3_kernel(const Args a) {
     const uint32_t base = (raw + 1023u) & ~1023u;  // 1024-aligned: the swizzle uses address bits 4-9
     uint8_t *smem = smem_raw + (base - raw);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_BYTES);
-    // bars[0..1] full, [2..3] empty, [4..5] acc_full, [6..7] acc_empty, [8] drain
+    // bars[0..1] full, [2..3] empty, [4] acc_full, [6] acc_empty, [8] drain
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + 9);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 10);
 
@@ -99,10 +102,8 @@ __global__ void __launch_bounds__(THREADS, 1) tf32x3_kernel(const Args a) {
             mbar_init(bar(s), PRODUCER_THREADS);
             mbar_init(bar(2 + s), 1);
         }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(bar(4 + b), 1);
-            mbar_init(bar(6 + b), 32 * EPILOGUE_WARPS);
-        }
+        mbar_init(bar(4), 1);
+        mbar_init(bar(6), 32 * EPILOGUE_WARPS);
         mbar_init(bar(8), 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -122,32 +123,34 @@ __global__ void __launch_bounds__(THREADS, 1) tf32x3_kernel(const Args a) {
     if (warp == 0) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            uint32_t it = 0, unit = 0;
+            uint32_t it = 0, iv = 0;  // k-blocks and fold intervals issued so far
             for_each_unit(a, abort_flag, [&](int, int kb, int ke) {
-                const int buf = unit & 1;
-                if (!mbar_wait(bar(6 + buf), ((unit >> 1) & 1) ^ 1, a, abort_flag, WD_MMA_ACC)) return;
-                tc_fence_after();
-                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
-                for (int kblk = kb; kblk < ke; ++kblk, ++it) {
-                    const int s = it & 1;
-                    if (!mbar_wait(bar(s), (it >> 1) & 1, a, abort_flag, WD_MMA_FULL)) return;
+                for (int k0 = kb; k0 < ke; k0 += FOLD_KB) {
+                    const int k1 = ke - k0 > FOLD_KB ? k0 + FOLD_KB : ke;
+                    // The accumulator is free once the previous interval is folded.
+                    if (!mbar_wait(bar(6), (iv & 1) ^ 1, a, abort_flag, WD_MMA_ACC)) return;
                     tc_fence_after();
-                    const uint32_t st = base + static_cast<uint32_t>(s * STAGE_BYTES);
-                    const uint64_t a_hi = sw128_desc(st), a_lo = sw128_desc(st + A_TILE);
-                    const uint64_t b_hi = sw128_desc(st + 2 * A_TILE), b_lo = sw128_desc(st + 2 * A_TILE + B_TILE);
+                    for (int kblk = k0; kblk < k1; ++kblk, ++it) {
+                        const int s = it & 1;
+                        if (!mbar_wait(bar(s), (it >> 1) & 1, a, abort_flag, WD_MMA_FULL)) return;
+                        tc_fence_after();
+                        const uint32_t st = base + static_cast<uint32_t>(s * STAGE_BYTES);
+                        const uint64_t a_hi = sw128_desc(st), a_lo = sw128_desc(st + A_TILE);
+                        const uint64_t b_hi = sw128_desc(st + 2 * A_TILE), b_lo = sw128_desc(st + 2 * A_TILE + B_TILE);
 #pragma unroll
-                    for (int ks = 0; ks < BK / 8; ++ks) {
-                        // 8 tf32 = 32 bytes along K: advance the start address (field units of 16 B).
-                        const uint64_t adv = static_cast<uint64_t>(ks * 2);
-                        const uint32_t first = (kblk == kb && ks == 0) ? 0u : 1u;
-                        tc_mma(d_tmem, a_lo + adv, b_hi + adv, first);
-                        tc_mma(d_tmem, a_hi + adv, b_lo + adv, 1u);
-                        tc_mma(d_tmem, a_hi + adv, b_hi + adv, 1u);
+                        for (int ks = 0; ks < BK / 8; ++ks) {
+                            // 8 tf32 = 32 bytes along K: advance the start address (field units of 16 B).
+                            const uint64_t adv = static_cast<uint64_t>(ks * 2);
+                            const uint32_t first = (kblk == k0 && ks == 0) ? 0u : 1u;
+                            tc_mma(tmem_base, a_lo + adv, b_hi + adv, first);
+                            tc_mma(tmem_base, a_hi + adv, b_lo + adv, 1u);
+                            tc_mma(tmem_base, a_hi + adv, b_hi + adv, 1u);
+                        }
+                        tc_commit(bar(2 + s));  // the stage is free once these MMAs finish
                     }
-                    tc_commit(bar(2 + s));  // the stage is free once these MMAs finish
+                    tc_commit(bar(4));  // interval done: the epilogue folds or stores it
+                    ++iv;
                 }
-                tc_commit(bar(4 + buf));  // accumulator ready for the epilogue
-                ++unit;
             });
             // Drain: every MMA this thread issued has finished before TMEM is freed.
             tc_commit(bar(8));
@@ -303,25 +306,51 @@ __global__ void __launch_bounds__(THREADS, 1) tf32x3_kernel(const Args a) {
     } else {
         // -------------------------------------------------------------- epilogue
         const int q = warp & 3;  // TMEM lane quarter this warp may access
-        uint32_t unit = 0;
+        const uint32_t tq = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+        uint32_t iv = 0;
         for_each_unit(a, abort_flag, [&](int tile, int kb, int ke) {
-            const int buf = unit & 1;
-            if (!mbar_wait(bar(4 + buf), (unit >> 1) & 1, a, abort_flag, WD_EPILOGUE)) return;
-            tc_fence_after();
             const TileAt at = tile_at(a, tile);
             const int64_t m0 = at.m0, n0 = at.n0;
             const int64_t row = m0 + q * 32 + lane;
             // Stream-K tiles hold beta * C + bias already: every unit adds.
             const bool atomic = tile >= a.dp_tiles;
             float *crow = a.C + at.item * a.strideC + row * a.ldc;
+            for (int k0 = kb; k0 < ke; k0 += FOLD_KB) {
+                const bool first = k0 == kb, last = ke - k0 <= FOLD_KB;
+                if (!mbar_wait(bar(4), iv & 1, a, abort_flag, WD_EPILOGUE)) return;
+                tc_fence_after();
+                ++iv;
 #pragma unroll 1
-            for (int ch = 0; ch < BN / 32; ++ch)
-                epilogue_chunk<VEC_C>(
-                    a, tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * BN + ch * 32),
-                    crow, row, n0 + ch * 32, atomic, false, 0);
-            tc_fence_before();
-            mbar_arrive(bar(6 + buf));
-            ++unit;
+                for (int ch = 0; ch < BN / 32; ++ch) {
+                    const uint32_t td = tq + static_cast<uint32_t>(ch * 32), tr = td + BN;
+                    float v[32];
+                    tmem_load32(td, v);
+                    if (!first) {
+                        float r[32];
+                        tmem_load32(tr, r);
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) v[j] += r[j];
+                    }
+                    if (ch == BN / 32 - 1) {
+                        // The accumulator is out: the next interval's MMAs may start.
+                        tmem_wait_st();
+                        tc_fence_before();
+                        mbar_arrive(bar(6));
+                    }
+                    if (last) {
+                        store_chunk_regs<VEC_C>(a, crow, row, n0 + ch * 32, v, atomic);
+                    } else {
+                        float h[16];
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) h[j] = v[j];
+                        tmem_store16(tr, h);
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) h[j] = v[16 + j];
+                        tmem_store16(tr + 16, h);
+                    }
+                }
+                if (!last) tmem_wait_st();  // the running sum is written before it is read again
+            }
         });
     }
 
@@ -891,8 +920,9 @@ int launch(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStream_t st
     const int tiles = static_cast<int>(tiles_m * tiles_n * p.batch);
     // One CTA per SM (the stage ring takes most of shared memory). A stream-K
     // share below 4 k-blocks costs more in fix-up than it saves.
-    const bool long_k = k_blocks > KB_CAP;  // every tile split, units of <= KB_CAP k-blocks
-    const Schedule sch = make_schedule(tiles, k_blocks, dev.sm_count, long_k ? SK_ALL : sk_mode, 4, 0.25);
+    // Accumulation chains are bounded by the folds inside the kernel, so
+    // units may span any number of k-blocks.
+    const Schedule sch = make_schedule(tiles, k_blocks, dev.sm_count, sk_mode, 4, 0.25);
     const int split = tiles - sch.dp_tiles;
     int rc = split_tiles_prepare(p, BM, BN, static_cast<int>(tiles_n), static_cast<int>(tiles_m * tiles_n),
                                  sch.dp_tiles, split, stream, launches);
@@ -926,7 +956,7 @@ int launch(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStream_t st
     a.bias_kind = p.bias_kind;
     a.act = p.act;
     a.ep = p.has_epilogue();
-    a.kb_cap = long_k ? KB_CAP : 0;
+    a.kb_cap = 0;
     kernel<<<sch.grid, THREADS, SMEM_BYTES, stream>>>(a);
     ++*launches;
     if (cudaGetLastError() != cudaSuccess) return SGEMM_ERR_LAUNCH;
@@ -1125,8 +1155,8 @@ int watchdog_set_ms(int64_t ms) {
 }
 
 bool tf32x3_supports(const Problem &p, const DeviceInfo &dev) {
-    // Transposed forms need the TMA path (16-byte aligned bases and strides).
-    if ((p.transA || p.transB) && !tma_ok(p)) return false;
+    // Every operand form at any alignment (the SM-pair kernel loads rows that
+    // TMA cannot address with cp.async).
     return p.M > 0 && p.N > 0 && p.K > 0 && dev.cc_major == 10 && dev.cc_minor == 3 &&
            dev.smem_optin >= static_cast<size_t>(tma::SMEM_BYTES);
 }
@@ -1138,19 +1168,17 @@ int tf32x3_launch(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStre
     // The transposed forms always take a TMA kernel (the per-thread-load
     // kernel serves op(A) = A, op(B) = B only).
     if (tma_ok(p) && (mode != 1 || p.transA || p.transB)) {
-        // Automatic: the SM-pair kernel where its 256 x 256 tiles are filled
-        // and the product is large enough for its shorter per-SM operand
-        // traffic to outweigh its longer start: above 2^29 multiply-adds
-        // (measured on GB300, L2 flushed, pair vs single-SM kernel:
-        // 768 x 768 x 1024 22.9 vs 24.1 us, 1024^3 27.3 vs 31.2; at 2^29,
-        // 512 x 512 x 2048 23.0 vs 21.9 and 512 x 1024 x 1024 22.9 vs 22.0;
-        // 768^3 22.9 vs 22.0); all four operand forms.
+        // Automatic: the SM-pair kernel from 2^20 multiply-adds on, any
+        // shape (measured on GB300, L2 flushed, pair vs single-SM kernel:
+        // 64^3 11.3 vs 10.4 us, 128^3 12.3 vs 14.5, 512^3 16.4 vs 19.7,
+        // 2048 x 128 x 512 17.4 vs 20.2, 200 x 4096 x 4096 49.2 vs 67.6,
+        // 1024^3 25.6 vs 31.3); all four operand forms.
         const double work = static_cast<double>(p.M) * static_cast<double>(p.N) * static_cast<double>(p.K) *
                             static_cast<double>(p.batch);
-        const bool pair = mode == 4 || (mode == 0 && p.M >= 256 && p.N >= 256 && work > 536870912.0);
+        const bool pair = mode == 4 || (mode == 0 && work >= 1048576.0);
         if (pair) {
             g_last_tc_kernel.store(4);
-            return tf32x3_pair_launch(p, dev, sk_mode, stream, launches);
+            return tf32x3_pair_launch(p, dev, sk_mode, false, stream, launches);
         }
         g_last_tc_kernel.store(mode == 2 && !p.transA && !p.transB ? 2 : 3);
         if (p.transA && p.transB)
@@ -1168,9 +1196,17 @@ int tf32x3_launch(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStre
         return vc ? launch_tma<true, true>(p, dev, sk_mode, stream, launches)
                   : launch_tma<true, false>(p, dev, sk_mode, stream, launches);
     }
-    // Transposed forms without 16-byte aligned rows: tf32x3_supports has
-    // rejected them already.
-    if (p.transA || p.transB) return SGEMM_ERR_UNSUPPORTED;
+    // Rows that TMA cannot address (or per-thread loads forced): the
+    // per-thread-load kernel for op(A) = A, op(B) = B; the SM-pair kernel with
+    // cp.async loaders for the transposed forms (which the per-thread-load
+    // kernel does not serve) or when forced (4). Its 4-byte copies are slow
+    // to issue (measured on GB300: ~5.5 us for one warp's half of a k-block,
+    // so 1023 x 2049 x 1537 with rows of 1537 and 2049 floats takes 309 us
+    // there against 131 us on the per-thread-load kernel).
+    if (p.transA || p.transB || mode == 4) {
+        g_last_tc_kernel.store(4);
+        return tf32x3_pair_launch(p, dev, sk_mode, true, stream, launches);
+    }
     g_last_tc_kernel.store(1);
     const bool va = (p.lda % 4 == 0) && (p.strideA % 4 == 0) && (reinterpret_cast<uintptr_t>(p.A) % 16 == 0);
     const bool vb = (p.ldb % 4 == 0) && (p.strideB % 4 == 0) && (reinterpret_cast<uintptr_t>(p.B) % 16 == 0);

@@ -1,6 +1,7 @@
 // Tensor-core SGEMM on SM pairs: tcgen05.mma.cta_group::2 (kind::tf32) with
 // the three-term TF32 split of sgemm_tf32x3.cu, for all four operand forms
-// (op(A) = A or A^T, op(B) = B or B^T) with 16-byte aligned rows.
+// (op(A) = A or A^T, op(B) = B or B^T) at any alignment: TMA loads the raw
+// tiles where the rows are 16-byte aligned, 4-byte cp.async copies elsewhere.
 //
 // The product is the plain sum of "CUDA算子优化(4)：矩阵乘法", section
 // "矩阵乘法的数学定义"; the pages give no tensor-core design (they name
@@ -32,7 +33,9 @@
 //     d = (fold interval) mod 2 and commits them to the mbarriers of both
 //     CTAs (multicast).
 //   * warps 1 and 22: TMA of this CTA's A rows (128 x 32, 128-byte swizzled)
-//     and B columns (32 x 64) into a 4-slot raw ring.
+//     and B columns (32 x 64) into a 4-slot raw ring (one lane each), or,
+//     for rows TMA cannot address, all lanes of both copying half of each
+//     tile with 4-byte cp.async.
 //   * warps 2-17 (converters, four groups of four warps, group g taking the
 //     k-blocks it with it mod 4 = g; each warp of a group serves one TMEM
 //     lane quarter): each thread splits one row of A (32 values) into hi /
@@ -73,8 +76,9 @@ namespace pr {
 constexpr int PM = 256, PN = 128;  // C tile of a pair
 constexpr int HM = 128, HN = 64;   // this CTA's rows of A, columns of B
 // Longest chain of k-blocks one accumulator sums before it is folded into the
-// running sum: 96 MMAs, ~5e-6 of sum |a||b| on non-negative inputs at any K.
-constexpr int FOLD_KB = 8;
+// running sum (tc::FOLD_KB = 8): 96 MMAs, ~5e-6 of sum |a||b| on non-negative
+// inputs at any K.
+constexpr int FOLD_KB = tc::FOLD_KB;
 // Four operand stages (a stage is refilled only after the MMAs that read it
 // have completed, and completions trail issue by the tensor pipe's queue)
 // and four raw slots, one of each per converter group.
@@ -342,9 +346,91 @@ __global__ void __launch_bounds__(pr::THREADS, 1)
         });
     };
 
+    // The same ring filled with 4-byte cp.async copies (a.cpa: rows that TMA
+    // cannot address), by all lanes of warps 1 and TMA_B_WARP, each copying
+    // half of this CTA's A tile and half of its B tile in the layouts the TMA
+    // boxes have (A, and B stored N x K, in the 128-byte swizzle; B stored
+    // K x N plain), zero outside the matrices. Every lane's copies for a slot
+    // are tracked by one cp.async arrival on the slot's full barrier.
+    auto load_pass = [&](uint32_t from, uint32_t to) {
+        const int half = warp == 1 ? 0 : 1;
+        uint32_t it = 0;
+        bool ok = true;
+        for_each_unit_of(a, abort_flag, pair, pairs, [&](int tile, int kb, int ke) {
+            if (!ok || it >= to) return;
+            if (it + static_cast<uint32_t>(ke - kb) <= from) {
+                it += static_cast<uint32_t>(ke - kb);
+                return;
+            }
+            const TileAt at = tile_at<pr::PM, pr::PN>(a, tile);
+            const int64_t m0 = at.m0 + pr::HM * static_cast<int64_t>(rank);
+            const int64_t n0 = at.n0 + pr::HN * static_cast<int64_t>(rank);
+            const float *Ai = a.A + (a.a_shared ? 0 : at.item * a.strideA);
+            const float *Bi = a.B + (a.b_shared ? 0 : at.item * a.strideB);
+            for (int kblk = kb; kblk < ke && it < to; ++kblk, ++it) {
+                if (it < from) continue;
+                const int slot = static_cast<int>(it % pr::RAW_SLOTS);
+                const bool free = mbar_wait(bar(pr::RAW_FREE + slot), ((it / pr::RAW_SLOTS) & 1) ^ 1, a, abort_flag,
+                                            WD_PRODUCER);
+                if (!__all_sync(0xffffffffu, free)) {
+                    ok = false;
+                    return;
+                }
+                const uint32_t sl = base + pr::RAW0 + static_cast<uint32_t>(slot * pr::SLOT);
+                const int64_t k0 = static_cast<int64_t>(kblk) * BK;
+                const uint32_t lo4 = static_cast<uint32_t>((lane & 3) * 4);
+                if (TA) {
+                    // A stored K x M: boxes 2 half, 2 half + 1 of 32 k-rows x 32 m; lane = m.
+                    for (int bx = 2 * half; bx < 2 * half + 2; ++bx) {
+                        const int64_t m = m0 + 32 * bx + lane;
+                        for (int r = 0; r < 32; ++r) {
+                            const int64_t k = k0 + r;
+                            const bool v = k < a.K && m < a.M;
+                            cp_async4(sl + static_cast<uint32_t>(bx * 4096) + sw128_offset(r, lane >> 2) + lo4,
+                                      v ? Ai + k * a.lda + m : Ai, v);
+                        }
+                    }
+                } else {
+                    // A rows 64 half .. 64 half + 63 of the tile; lane = k.
+                    const int64_t k = k0 + lane;
+                    for (int r = 64 * half; r < 64 * half + 64; ++r) {
+                        const int64_t m = m0 + r;
+                        const bool v = k < a.K && m < a.M;
+                        cp_async4(sl + sw128_offset(r, lane >> 2) + lo4, v ? Ai + m * a.lda + k : Ai, v);
+                    }
+                }
+                const uint32_t sb = sl + pr::A_RAW;
+                if (TB) {
+                    // B stored N x K: n-rows 32 half .. 32 half + 31 of 32 k; lane = k.
+                    const int64_t k = k0 + lane;
+                    for (int r = 32 * half; r < 32 * half + 32; ++r) {
+                        const int64_t n = n0 + r;
+                        const bool v = k < a.K && n < a.N;
+                        cp_async4(sb + sw128_offset(r, lane >> 2) + lo4, v ? Bi + n * a.ldb + k : Bi, v);
+                    }
+                } else {
+                    // B stored K x N: k-rows 16 half .. 16 half + 15 of 64 n (plain rows of 256 bytes).
+                    for (int r = 16 * half; r < 16 * half + 16; ++r) {
+                        const int64_t k = k0 + r;
+#pragma unroll
+                        for (int c2 = 0; c2 < 2; ++c2) {
+                            const int64_t n = n0 + 32 * c2 + lane;
+                            const bool v = k < a.K && n < a.N;
+                            cp_async4(sb + static_cast<uint32_t>(r * pr::HN * 4 + (32 * c2 + lane) * 4),
+                                      v ? Bi + k * a.ldb + n : Bi, v);
+                        }
+                    }
+                }
+                cp_async_arrive(bar(pr::RAW_FULL + slot));
+            }
+        });
+    };
+
     if (threadIdx.x == 0) {
         for (int s = 0; s < pr::RAW_SLOTS; ++s) {
-            mbar_init(bar(pr::RAW_FULL + s), 2);                   // one expect_tx arrival per TMA issuer
+            // One expect_tx arrival per TMA issuer, or one cp.async arrival
+            // per lane of the two loader warps.
+            mbar_init(bar(pr::RAW_FULL + s), a.cpa ? 64 : 2);
             mbar_init(bar(pr::RAW_FREE + s), pr::GROUP_WARPS);  // one lane per converter warp
         }
         for (int s = 0; s < pr::OP_STAGES; ++s) {
@@ -362,7 +448,7 @@ __global__ void __launch_bounds__(pr::THREADS, 1)
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (tma_warp && lane == 0) {
+    if (tma_warp && lane == 0 && !a.cpa) {
         const bool is_a = warp == 1;
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(is_a ? &tmA : &tmB)) : "memory");
     }
@@ -381,7 +467,12 @@ __global__ void __launch_bounds__(pr::THREADS, 1)
     // pair meets (after their arrival, whose release would otherwise wait for
     // the loads).
     cluster_arrive();
-    if (tma_warp && lane == 0) tma_pass(0, pr::RAW_SLOTS);
+    if (tma_warp) {
+        if (a.cpa)
+            load_pass(0, pr::RAW_SLOTS);
+        else if (lane == 0)
+            tma_pass(0, pr::RAW_SLOTS);
+    }
     __syncwarp();
     cluster_wait();
     tc_fence_after();
@@ -466,7 +557,10 @@ __global__ void __launch_bounds__(pr::THREADS, 1)
         }
     } else if (tma_warp) {
         // ---------------------------------------------------- TMA issuers (A, B)
-        if (lane == 0) tma_pass(pr::RAW_SLOTS, 0xffffffffu);
+        if (a.cpa)
+            load_pass(pr::RAW_SLOTS, 0xffffffffu);
+        else if (lane == 0)
+            tma_pass(pr::RAW_SLOTS, 0xffffffffu);
     } else if (warp < pr::EPI_WARP0) {
         // ------------------------------------------------------------ converters
         const int cw = warp - 2;                                 // 0 .. 15
@@ -688,7 +782,7 @@ cudaError_t g_pair_err[kMaxDevices][8];
 int g_pair_clusters[kMaxDevices][8];
 
 template <bool VEC_C, bool TA, bool TB>
-int launch_pair(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStream_t stream, int *launches) {
+int launch_pair(const Problem &p, const DeviceInfo &dev, int sk_mode, bool cpa, cudaStream_t stream, int *launches) {
     auto kernel = tf32x3_pair_kernel<VEC_C, TA, TB>;
     constexpr int idx = (VEC_C ? 1 : 0) + (TA ? 2 : 0) + (TB ? 4 : 0);
     cudaLaunchAttribute attr[2];
@@ -722,14 +816,16 @@ int launch_pair(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStream
     }
     int *flag = watchdog_flag_device_ptr();
     if (!flag) return SGEMM_ERR_LAUNCH;
-    alignas(64) CUtensorMap mapA, mapB, mapC;
-    const bool ok_a =
-        TA ? encode_map(&mapA, p.A, p.K, p.M, p.lda, p.batch, p.strideA, 32, 32, CU_TENSOR_MAP_SWIZZLE_128B)
-           : encode_map(&mapA, p.A, p.M, p.K, p.lda, p.batch, p.strideA, BK, pr::HM, CU_TENSOR_MAP_SWIZZLE_128B);
-    const bool ok_b =
-        TB ? encode_map(&mapB, p.B, p.N, p.K, p.ldb, p.batch, p.strideB, BK, pr::HN, CU_TENSOR_MAP_SWIZZLE_128B)
-           : encode_map(&mapB, p.B, p.K, p.N, p.ldb, p.batch, p.strideB, pr::HN, BK, CU_TENSOR_MAP_SWIZZLE_NONE);
-    if (!ok_a || !ok_b) return SGEMM_ERR_LAUNCH;
+    alignas(64) CUtensorMap mapA{}, mapB{}, mapC{};
+    if (!cpa) {  // operands through TMA; otherwise the kernel's cp.async loaders read A and B
+        const bool ok_a =
+            TA ? encode_map(&mapA, p.A, p.K, p.M, p.lda, p.batch, p.strideA, 32, 32, CU_TENSOR_MAP_SWIZZLE_128B)
+               : encode_map(&mapA, p.A, p.M, p.K, p.lda, p.batch, p.strideA, BK, pr::HM, CU_TENSOR_MAP_SWIZZLE_128B);
+        const bool ok_b =
+            TB ? encode_map(&mapB, p.B, p.N, p.K, p.ldb, p.batch, p.strideB, BK, pr::HN, CU_TENSOR_MAP_SWIZZLE_128B)
+               : encode_map(&mapB, p.B, p.K, p.N, p.ldb, p.batch, p.strideB, pr::HN, BK, CU_TENSOR_MAP_SWIZZLE_NONE);
+        if (!ok_a || !ok_b) return SGEMM_ERR_LAUNCH;
+    }
     // C through TMA when its rows allow 16-byte aligned boxes and C is not
     // read (beta = 0; split tiles are reduce-added either way).
     const bool c_tma = VEC_C && p.beta == 0.0f &&
@@ -753,6 +849,11 @@ int launch_pair(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStream
     a.M = p.M;
     a.N = p.N;
     a.K = p.K;
+    a.A = p.A;
+    a.lda = p.lda;
+    a.B = p.B;
+    a.ldb = p.ldb;
+    a.cpa = cpa ? 1 : 0;
     a.C = p.C;
     a.ldc = p.ldc;
     a.tiles_n = static_cast<int>(tiles_n);
@@ -794,19 +895,20 @@ int launch_pair(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStream
 
 }  // namespace
 
-int tf32x3_pair_launch(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStream_t stream, int *launches) {
+int tf32x3_pair_launch(const Problem &p, const DeviceInfo &dev, int sk_mode, bool cpa, cudaStream_t stream,
+                       int *launches) {
     if (dev.device < 0 || dev.device >= kMaxDevices) return SGEMM_ERR_DEVICE;
     const bool vc = (p.ldc % 4 == 0) && (p.strideC % 4 == 0) && (reinterpret_cast<uintptr_t>(p.C) % 16 == 0);
     const int form = (vc ? 1 : 0) + (p.transA ? 2 : 0) + (p.transB ? 4 : 0);
     switch (form) {
-        case 0: return launch_pair<false, false, false>(p, dev, sk_mode, stream, launches);
-        case 1: return launch_pair<true, false, false>(p, dev, sk_mode, stream, launches);
-        case 2: return launch_pair<false, true, false>(p, dev, sk_mode, stream, launches);
-        case 3: return launch_pair<true, true, false>(p, dev, sk_mode, stream, launches);
-        case 4: return launch_pair<false, false, true>(p, dev, sk_mode, stream, launches);
-        case 5: return launch_pair<true, false, true>(p, dev, sk_mode, stream, launches);
-        case 6: return launch_pair<false, true, true>(p, dev, sk_mode, stream, launches);
-        default: return launch_pair<true, true, true>(p, dev, sk_mode, stream, launches);
+        case 0: return launch_pair<false, false, false>(p, dev, sk_mode, cpa, stream, launches);
+        case 1: return launch_pair<true, false, false>(p, dev, sk_mode, cpa, stream, launches);
+        case 2: return launch_pair<false, true, false>(p, dev, sk_mode, cpa, stream, launches);
+        case 3: return launch_pair<true, true, false>(p, dev, sk_mode, cpa, stream, launches);
+        case 4: return launch_pair<false, false, true>(p, dev, sk_mode, cpa, stream, launches);
+        case 5: return launch_pair<true, false, true>(p, dev, sk_mode, cpa, stream, launches);
+        case 6: return launch_pair<false, true, true>(p, dev, sk_mode, cpa, stream, launches);
+        default: return launch_pair<true, true, true>(p, dev, sk_mode, cpa, stream, launches);
     }
 }
 

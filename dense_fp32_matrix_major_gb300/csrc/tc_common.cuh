@@ -30,8 +30,12 @@ constexpr int BAR_BYTES = 128;
 // 32-deep k-block (12 MMAs) on non-negative inputs. Products with more than
 // KB_CAP k-blocks are split along K into units of at most KB_CAP k-blocks
 // (~5.4e-6 on non-negative inputs), whose partial sums are added into C
-// with round-to-nearest fp32 adds.
+// with round-to-nearest fp32 adds (the TMA kernels of sgemm_tf32x3.cu).
 constexpr int KB_CAP = 8;
+// Kernels that fold on chip restart their accumulator every FOLD_KB
+// k-blocks and add it, rounded to nearest, into an fp32 running sum of the
+// tile (TMEM or shared memory), so units of any length keep that error.
+constexpr int FOLD_KB = 8;
 
 // Watchdog codes (which wait gave up).
 enum : int { WD_PRODUCER = 1, WD_MMA_FULL = 2, WD_MMA_ACC = 3, WD_EPILOGUE = 4, WD_DRAIN = 5, WD_SELFTEST = 6 };
@@ -63,6 +67,9 @@ struct Args {
     // Kernels with a C tensor map: write C through shared memory with TMA
     // bulk stores (and bulk reduce-adds for split tiles).
     int c_tma = 0;
+    // Operands whose rows TMA cannot address (not 16-byte aligned): the raw
+    // ring is filled with 4-byte cp.async copies instead (pair kernel).
+    int cpa = 0;
     // Longest run of k-blocks one unit may accumulate in TMEM (0: no limit);
     // split units start at multiples of it (see for_each_unit_of).
     int kb_cap = 0;
@@ -302,6 +309,20 @@ __device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap *map, int x,
                      reinterpret_cast<uint64_t>(map)),
                  "r"(x), "r"(y), "r"(z), "r"(src)
                  : "memory");
+}
+
+// 4-byte asynchronous copy global -> shared; valid == false writes zero and
+// reads nothing (src must still be a valid address).
+__device__ __forceinline__ void cp_async4(uint32_t dst, const float *src, bool valid) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst),
+                 "l"(__cvta_generic_to_global(src)), "r"(valid ? 4 : 0)
+                 : "memory");
+}
+
+// The mbarrier gets one arrival once every cp.async this thread issued so far
+// has completed (its expected count must include that arrival).
+__device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
@@ -544,6 +565,31 @@ __device__ __forceinline__ void store_chunk(const Args &a, float *crow, int64_t 
 #pragma unroll
         for (int j = 0; j < 32; ++j)
             if (col0 + j < N) crow[col0 + j] = beta != 0.0f ? fmaf(beta, crow[col0 + j], alpha * v[j]) : alpha * v[j];
+    }
+}
+
+// Writes 32 finished values of one row held in registers (columns col0 ..
+// col0 + 31): C = act(alpha * v + beta * C + bias) for a whole tile (the bias
+// and activation with a fused epilogue), C += alpha * v with atomics for a
+// tile split along K. Called by all 32 lanes of the warp (the bias shuffles).
+template <bool VEC_C>
+__device__ __forceinline__ void store_chunk_regs(const Args &a, float *crow, int64_t row, int64_t col0,
+                                                 const float (&v)[32], bool atomic) {
+    if (col0 >= a.N) return;  // uniform over the warp
+    if (a.ep && !atomic) {
+        const int lane = static_cast<int>(threadIdx.x & 31);
+        float bl = 0.0f;
+        if (a.bias_kind == SGEMM_BIAS_PER_COL && col0 + lane < a.N) bl = __ldg(a.bias + col0 + lane);
+        if (a.bias_kind == SGEMM_BIAS_PER_ROW && row < a.M) bl = __ldg(a.bias + row);
+        float h[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) h[j] = v[j];
+        store16_fused<VEC_C>(a, crow, row, col0, 0, bl, h);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) h[j] = v[16 + j];
+        store16_fused<VEC_C>(a, crow, row, col0 + 16, 16, bl, h);
+    } else {
+        store_chunk<VEC_C>(a, crow, row, col0, v, atomic);
     }
 }
 

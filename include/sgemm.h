@@ -105,9 +105,7 @@ enum sgemm_op {
  *             B are not read.
  * Same conventions, errors and accuracy bound as sgemm_f32, with the error
  * scale |alpha| sum_k |op(A)[i][k]| |op(B)[k][j]| + |beta| |C[i][j]|.
- * SGEMM_TF32X3 serves op(A) = A, op(B) = B at any alignment and the
- * transposed forms when A and B have 16-byte aligned bases and row strides;
- * SGEMM_AUTO picks a variant that serves the request.
+ * Both variants serve every operand form at any alignment.
  */
 int sgemm_f32_ex(int transA, int transB, int64_t M, int64_t N, int64_t K, float alpha, const float *A,
                  int64_t lda, const float *B, int64_t ldb, float beta, float *C, int64_t ldc,
@@ -248,18 +246,20 @@ int sgemm_watchdog_selftest(int64_t wait_ms, sgemm_stream_t stream);
  *   SGEMM_TUNE_WATCHDOG_MS   milliseconds a bounded wait polls before it gives
  *                            up (1 .. 60000; default 2000)
  *   SGEMM_TUNE_TF32X3_KERNEL  tensor-core kernel: 0 = automatic (default):
- *                            the SM-pair kernel for any operand form with
- *                            16-byte aligned bases and row strides, M and N
- *                            >= 256 and more than 2^29 multiply-adds, else the
- *                            TMA kernel with A in tensor memory where the
- *                            rows are 16-byte aligned, else per-thread loads;
+ *                            where A and B have 16-byte aligned bases and
+ *                            row strides, the SM-pair kernel from 2^20
+ *                            multiply-adds on and the TMA kernel with A in
+ *                            tensor memory below; otherwise per-thread loads
+ *                            (the SM-pair kernel for the transposed forms);
  *                            1 = per-thread loads, 2 = TMA, 3 = TMA with A's
  *                            operands in tensor memory, 4 = SM pairs (tcgen05
- *                            cta_group::2 on clusters of two CTAs). Kernels
- *                            2-4 need 16-byte aligned rows (else kernel 1
- *                            runs); the transposed forms take kernel 4 when
- *                            it is chosen (automatically or forced) and
- *                            kernel 3 otherwise.
+ *                            cta_group::2 on clusters of two CTAs; TMA loads
+ *                            for 16-byte aligned rows, cp.async otherwise).
+ *                            Kernels 2 and 3 need 16-byte aligned rows (else
+ *                            kernel 1 runs, or kernel 4 for the transposed
+ *                            forms); kernel 1 serves op(A) = A, op(B) = B
+ *                            only (the transposed forms take kernel 3 when
+ *                            the rows are aligned, else kernel 4).
  * Returns SGEMM_OK or SGEMM_ERR_INVALID_ARG. sgemm_get_tuning returns the
  * value, or -1 for an unknown key.
  */

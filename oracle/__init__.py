@@ -72,6 +72,8 @@ def _load():
             lib.oracle_sgemm_f64.argtypes = [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _vp, _i64]
             lib.oracle_sgemm_f64_rows.argtypes = [
                 _i64, _i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _vp, _i64, ctypes.c_int]
+            lib.oracle_sgemm_f32_rows.argtypes = [
+                _i64, _i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, ctypes.c_int]
             lib.oracle_sgemm_f64_at.argtypes = [
                 _i64, _i64, _i64, _vp, _i64, _vp, _i64, _i64, _vp, _vp, _vp, _vp]
             _d = ctypes.c_double
@@ -81,7 +83,7 @@ def _load():
                                                _i64, _vp, _i64, _d, _vp, _i64, _i64, _vp, _vp, _vp, _vp]
             lib.oracle_epilogue_f64.argtypes = [_i64, _vp, _vp, _i64, _i64, _vp, ctypes.c_int, ctypes.c_int,
                                                 _vp, _vp]
-            for fn in (lib.oracle_sgemm_f32, lib.oracle_sgemm_f64, lib.oracle_sgemm_f64_rows,
+            for fn in (lib.oracle_sgemm_f32, lib.oracle_sgemm_f32_rows, lib.oracle_sgemm_f64, lib.oracle_sgemm_f64_rows,
                        lib.oracle_sgemm_f64_at, lib.oracle_gemm_f64, lib.oracle_gemm_f64_at,
                        lib.oracle_epilogue_f64):
                 fn.restype = ctypes.c_int
@@ -118,6 +120,26 @@ def sgemm_f32(A: np.ndarray, B: np.ndarray) -> np.ndarray:
     C = np.empty((M, N), dtype=np.float32)
     _check(_load().oracle_sgemm_f32(M, N, K, pa, lda, pb, ldb, C.ctypes.data, max(N, 1)),
            "oracle_sgemm_f32")
+    return C
+
+
+def sgemm_f32_rows(A: np.ndarray, B: np.ndarray, row_begin: int = 0, row_end=None,
+                   nthreads: int | None = None) -> np.ndarray:
+    """Rows [row_begin, row_end) of the pages' float product, i-k-j order,
+    threaded by rows; bit-identical to :func:`sgemm_f32` on those rows."""
+    (M, K), (K2, N) = A.shape, B.shape
+    if K != K2:
+        raise ValueError("inner dimensions differ")
+    row_end = M if row_end is None else row_end
+    if not 0 <= row_begin <= row_end <= M:
+        raise ValueError("row band out of range")
+    if nthreads is None:
+        nthreads = os.cpu_count() or 1
+    pa, lda = _rowmajor(A, "A")
+    pb, ldb = _rowmajor(B, "B")
+    C = np.empty((row_end - row_begin, N), dtype=np.float32)
+    _check(_load().oracle_sgemm_f32_rows(row_begin, row_end, N, K, pa, lda, pb, ldb, C.ctypes.data,
+                                         max(N, 1), int(nthreads)), "oracle_sgemm_f32_rows")
     return C
 
 

@@ -38,6 +38,14 @@
  *                        across threads by rows; output row 0 is row_begin.
  *                        Each element still adds its terms in k-ascending
  *                        order, so it equals oracle_sgemm_f64 bit for bit.
+ *   oracle_sgemm_f32_rows  the pages' float arithmetic with i, k, j loop order
+ *                        over a band of rows, split across threads by rows
+ *                        (the timed CPU baseline): every element still adds
+ *                        its rounded products in k-ascending order into one
+ *                        float, so it equals oracle_sgemm_f32 bit for bit;
+ *                        the inner loop runs along a row of B, which the
+ *                        compiler may vectorise across j without changing
+ *                        any element's order of operations.
  *   oracle_sgemm_f64_at  C64 and S at a list of (row, col) samples, for
  *                        checks at sizes where the full product is too slow.
  *   oracle_gemm_f64      the general form C = alpha * op(A) * op(B) + beta * C
@@ -199,6 +207,77 @@ int oracle_sgemm_f64_rows(int64_t row_begin, int64_t row_end, int64_t N, int64_t
             rows_worker(&jobs[t]);
     }
     rows_worker(&jobs[0]);
+    for (int t = 1; t < nthreads; ++t)
+        if (created[t]) pthread_join(tid[t], NULL);
+    free(tid);
+    free(created);
+    free(jobs);
+    return 0;
+}
+
+struct f32_rows_job {
+    int64_t band0, row_begin, row_end, N, K, lda, ldb, ldc;
+    const float *A, *B;
+    float *C;
+};
+
+static void *f32_rows_worker(void *arg)
+{
+    const struct f32_rows_job *job = (const struct f32_rows_job *)arg;
+    for (int64_t i = job->row_begin; i < job->row_end; ++i) {
+        float *c = job->C + (i - job->band0) * job->ldc;
+        for (int64_t j = 0; j < job->N; ++j) c[j] = 0.0f;
+        for (int64_t k = 0; k < job->K; ++k) {
+            const float a = job->A[i * job->lda + k];
+            const float *brow = job->B + k * job->ldb;
+            for (int64_t j = 0; j < job->N; ++j) {
+                float prod = a * brow[j];
+                c[j] = c[j] + prod;
+            }
+        }
+    }
+    return NULL;
+}
+
+int oracle_sgemm_f32_rows(int64_t row_begin, int64_t row_end, int64_t N, int64_t K,
+                          const float *A, int64_t lda, const float *B, int64_t ldb,
+                          float *C, int64_t ldc, int nthreads)
+{
+    if (row_begin < 0 || row_end < row_begin) return 1;
+    if (!oracle_args_ok(row_end, N, K, A, lda, B, ldb, C, ldc)) return 1;
+    int64_t rows = row_end - row_begin;
+    if (rows == 0 || N == 0) return 0;
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > rows) nthreads = (int)rows;
+    pthread_t *tid = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
+    char *created = (char *)calloc((size_t)nthreads, 1);
+    struct f32_rows_job *jobs = (struct f32_rows_job *)calloc((size_t)nthreads, sizeof(struct f32_rows_job));
+    if (!tid || !created || !jobs) {
+        free(tid);
+        free(created);
+        free(jobs);
+        return 2;
+    }
+    for (int t = 0; t < nthreads; ++t) {
+        jobs[t].band0 = row_begin;
+        jobs[t].row_begin = row_begin + rows * t / nthreads;
+        jobs[t].row_end = row_begin + rows * (t + 1) / nthreads;
+        jobs[t].N = N;
+        jobs[t].K = K;
+        jobs[t].lda = lda;
+        jobs[t].ldb = ldb;
+        jobs[t].ldc = ldc;
+        jobs[t].A = A;
+        jobs[t].B = B;
+        jobs[t].C = C;
+    }
+    for (int t = 1; t < nthreads; ++t) {
+        if (pthread_create(&tid[t], NULL, f32_rows_worker, &jobs[t]) == 0)
+            created[t] = 1;
+        else
+            f32_rows_worker(&jobs[t]);
+    }
+    f32_rows_worker(&jobs[0]);
     for (int t = 1; t < nthreads; ++t)
         if (created[t]) pthread_join(tid[t], NULL);
     free(tid);

@@ -27,6 +27,13 @@ int oracle_sgemm_f64_rows(int64_t row_begin, int64_t row_end, int64_t N, int64_t
                           const float *A, int64_t lda, const float *B, int64_t ldb,
                           double *C64, double *S, int64_t ldc, int nthreads);
 
+/* Rows [row_begin, row_end) of the float product (the pages' loop arithmetic)
+ * in i-k-j order, threaded by rows: bit-identical to oracle_sgemm_f32 on
+ * those rows. Output row r of C is product row row_begin + r. */
+int oracle_sgemm_f32_rows(int64_t row_begin, int64_t row_end, int64_t N, int64_t K,
+                          const float *A, int64_t lda, const float *B, int64_t ldb,
+                          float *C, int64_t ldc, int nthreads);
+
 /* Double product and S at n_samples (rows[t], cols[t]) positions. */
 int oracle_sgemm_f64_at(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda,
                         const float *B, int64_t ldb, int64_t n_samples, const int64_t *rows,

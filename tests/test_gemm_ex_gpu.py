@@ -34,21 +34,10 @@ def _stored(M, N, K, transA, transB, dist, seed):
     return As, Bs
 
 
-def _tma_aligned(As, Bs, **kw):
-    lda = kw.get("lda") or As.shape[1]
-    ldb = kw.get("ldb") or Bs.shape[1]
-    offs = kw.get("offsets", (0, 0, 0))
-    return lda % 4 == 0 and ldb % 4 == 0 and offs[0] % 4 == 0 and offs[1] % 4 == 0
-
-
 def _check(lib, As, Bs, tA, tB, alpha, beta, C0, **kw):
     C, flat, rc = run_gemm_ex(As, Bs, transA=tA, transB=tB, alpha=alpha, beta=beta,
                               C_init=C0 if beta else None, **kw)
-    if lib.get_variant() == lib.SGEMM_TF32X3 and (tA or tB) and not _tma_aligned(As, Bs, **kw):
-        # Forced tensor cores serve transposed forms only with 16-byte aligned rows.
-        assert rc == lib.SGEMM_ERR_UNSUPPORTED
-        return
-    assert rc == 0
+    assert rc == 0  # every form at any alignment, on either variant
     M, N = C.shape
     ldc = kw.get("ldc") or max(N, 1)
     assert outside_box_intact(flat, M, N, ldc, kw.get("offsets", (0, 0, 0))[2])
@@ -130,12 +119,20 @@ def test_beta_zero_ignores_nan_c_and_alpha_zero(lib):
         assert rc == 0 and np.all(C == 0)
 
 
-def test_forced_tensor_cores_on_unaligned_transposes(lib):
-    """TF32X3 serves transposed forms only through TMA (16-byte aligned rows)."""
+@pytest.mark.parametrize("tA,tB", FORMS)
+def test_forced_tensor_cores_on_unaligned_transposes(lib, tA, tB):
+    """Forced tensor cores serve every form with rows that are not 16-byte
+    aligned (the transposed forms on the SM-pair kernel's cp.async loaders),
+    at a size that spans several pair tiles and a ragged edge, with alpha and
+    beta."""
     lib.set_variant("tf32x3")
-    As, Bs = _stored(100, 100, 101, 1, 0, "normal", 5)  # A stored 101 x 100: lda = 100 is aligned
-    _, _, rc = run_gemm_ex(As, Bs, transA=True, lda=101)
-    assert rc in (0, lib.SGEMM_ERR_UNSUPPORTED)
+    M, N, K = 300, 270, 301
+    As, Bs = _stored(M, N, K, tA, tB, "uniform", 5)
+    C0 = np.random.default_rng(6).standard_normal((M, N)).astype(np.float32)
+    _check(lib, As, Bs, tA, tB, 0.75, -1.5, C0, lda=As.shape[1] + 1, ldb=Bs.shape[1] + 3, ldc=N + 1,
+           offsets=(1, 2, 3))
+    if tA or tB:  # the per-thread-load kernel serves op(A) = A, op(B) = B only
+        assert lib.get_tuning(lib.SGEMM_TUNE_LAST_TC_KERNEL) == 4
 
 
 @pytest.mark.parametrize("tA,tB", FORMS)

@@ -246,6 +246,27 @@ def test_rows_twin_bit_identical():
     assert np.array_equal(R64, C64[10:20]) and np.array_equal(RS, S[10:20])
 
 
+@pytest.mark.parametrize("dist", ["normal", "uniform01"])
+def test_float_rows_twin_bit_identical(dist):
+    """The timed float twin (i-k-j, threaded by rows) adds the same rounded
+    products in the same k order as the pages' i-j-k loop: every bit equal,
+    for any band of rows, thread count and padded stride."""
+    A, B = wl.make_pair(41, 67, 203, dist, 11)
+    C = oracle.sgemm_f32(A, B)
+    for nthreads in (1, 3, 16):
+        R = oracle.sgemm_f32_rows(A, B, nthreads=nthreads)
+        assert np.array_equal(R.view(np.uint32), C.view(np.uint32))
+    R = oracle.sgemm_f32_rows(A, B, 7, 30, nthreads=4)
+    assert np.array_equal(R.view(np.uint32), C[7:30].view(np.uint32))
+    Rp = oracle.sgemm_f32_rows(wl.strided(A, 211), wl.strided(B, 70), nthreads=2)
+    assert np.array_equal(Rp.view(np.uint32), C.view(np.uint32))
+    # And it is the float loop, not a double one: a long same-sign sum
+    # differs from the double product rounded once.
+    A1, B1 = wl.make_pair(3, 5, 4096, "uniform01", 2)
+    C64, _ = oracle.sgemm_f64(A1, B1)
+    assert not np.array_equal(oracle.sgemm_f32_rows(A1, B1), C64.astype(np.float32))
+
+
 def test_sampled_twin_matches():
     A, B = wl.make_pair(29, 31, 47, "uniform", 4)
     C64, S = oracle.sgemm_f64(A, B)

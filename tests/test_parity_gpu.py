@@ -357,12 +357,12 @@ def test_output_beyond_2_31_elements(lib, setting):
 
 @pytest.mark.parametrize("M,N,K,lda_pad,variant,tc", [
     (16, 16, 16, 0, "ffma", 0),        # tiniest products stay on the CUDA cores
-    (64, 64, 64, 0, "tf32x3", 3),      # from 2^14 useful multiply-adds: tensor cores
-    (512, 512, 512, 0, "tf32x3", 3),   # single-SM kernel below 2^29
-    (512, 512, 2048, 0, "tf32x3", 3),  # exactly 2^29: still single-SM
-    (768, 768, 1024, 0, "tf32x3", 4),  # above 2^29 with M, N >= 256: SM pairs
+    (64, 64, 64, 0, "tf32x3", 3),      # from 2^14 useful multiply-adds: tensor cores, single SM
+    (128, 128, 64, 0, "tf32x3", 4),    # from 2^20: SM pairs
+    (512, 512, 512, 0, "tf32x3", 4),
+    (768, 768, 1024, 0, "tf32x3", 4),
     (2048, 3072, 4096, 0, "tf32x3", 4),
-    (200, 4096, 4096, 0, "tf32x3", 3),  # M < 256: single-SM kernel however large
+    (200, 4096, 4096, 0, "tf32x3", 4),  # thin products too
     (300, 300, 301, 1, "tf32x3", 1),    # rows not 16-byte aligned: per-thread loads
 ])
 def test_auto_dispatch(lib, M, N, K, lda_pad, variant, tc):
