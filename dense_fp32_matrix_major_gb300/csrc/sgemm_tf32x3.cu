@@ -338,6 +338,8 @@ __global__ void __launch_bounds__(THREADS, 1) tf32x3_kernel(const Args a) {
                         mbar_arrive(bar(6));
                     }
                     if (last) {
+                        fix_nonfinite(a, at.item, row, n0 + ch * 32, static_cast<int64_t>(kb) * BK,
+                                      static_cast<int64_t>(ke) * BK, v);
                         store_chunk_regs<VEC_C>(a, crow, row, n0 + ch * 32, v, atomic);
                     } else {
                         float h[16];
@@ -597,7 +599,8 @@ __global__ void __launch_bounds__(tma::THREADS, 1)
             for (int ch = 0; ch < BN / 32; ++ch)
                 epilogue_chunk<VEC_C>(
                     a, tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * BN + ch * 32),
-                    crow, row, n0 + ch * 32, atomic, false, 0);
+                    crow, row, n0 + ch * 32, atomic, false, 0, at.item, static_cast<int64_t>(kb) * BK,
+                    static_cast<int64_t>(ke) * BK);
             tc_fence_before();
             mbar_arrive(bar(6 + buf));
             ++unit;
@@ -861,7 +864,8 @@ __global__ void __launch_bounds__(tm3::THREADS, 1)
 #pragma unroll 1
             for (int ch = 0; ch < BN / 32; ++ch)  // the last chunk frees the accumulator for the next unit
                 epilogue_chunk<VEC_C>(a, tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(ch * 32),
-                                      crow, row, n0 + ch * 32, atomic, ch == BN / 32 - 1, bar(9));
+                                      crow, row, n0 + ch * 32, atomic, ch == BN / 32 - 1, bar(9), at.item,
+                                      static_cast<int64_t>(kb) * BK, static_cast<int64_t>(ke) * BK);
             ++unit;
         });
     }
@@ -1037,6 +1041,12 @@ int launch_tma(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStream_
     a.M = p.M;
     a.N = p.N;
     a.K = p.K;
+    a.A = p.A;
+    a.lda = p.lda;
+    a.B = p.B;
+    a.ldb = p.ldb;
+    a.ta = TA ? 1 : 0;
+    a.tb = TB ? 1 : 0;
     a.C = p.C;
     a.ldc = p.ldc;
     a.tiles_n = static_cast<int>(tiles_n);

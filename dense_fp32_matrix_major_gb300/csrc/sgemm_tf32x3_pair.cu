@@ -233,37 +233,48 @@ __device__ __forceinline__ void stage32_fused(int act, uint32_t buf, int lane, f
 }
 
 // The last fold of a unit for a chunk written with per-thread stores: the
-// chunk's accumulator columns (TMEM address taddr) plus, unless `first`, the
-// running sum (chunk rc), then C = alpha * v + beta * C (+ bias, activation)
-// for a whole tile or C += alpha * v with atomics for a tile split along K.
-// `release`: the chunk is the accumulator's last; free it on the even CTA's
-// barrier acc_empty once read. Used for chunks that cross the last row or
-// column of C and for C that TMA cannot write; called by all 32 lanes (the
-// bias shuffles). Out of line: it is rare, and inlined it would compete for
-// registers with the interior path.
+// unit's finished sum for this lane's row, columns col0 .. col0 + 31 (chunk
+// rc of shared memory, swizzled), repaired where it is NaN (fix_nonfinite,
+// over the unit's k-range [k_begin, k_end) of batch item `item`), then C =
+// alpha * v + beta * C (+ bias, activation) for a whole tile or C += alpha *
+// v with atomics for a tile split along K. Used for chunks that cross the
+// last row or column of C, for C that TMA cannot write and for chunks holding
+// a NaN; called by all 32 lanes (the bias shuffles and the NaN vote). Out of
+// line: it is rare, and inlined it would compete for registers with the
+// interior path.
 template <bool VEC_C>
-__device__ __noinline__ void edge_final_chunk(const Args &a, uint32_t taddr, uint32_t rc, bool first, float *crow,
-                                              int64_t row, int64_t col0, bool atomic, bool release,
-                                              uint32_t acc_empty) {
+__device__ __noinline__ void edge_final_chunk(const Args &a, uint32_t rc, float *crow, int64_t row, int64_t col0,
+                                              bool atomic, int item, int64_t k_begin, int64_t k_end) {
     const int lane = static_cast<int>(threadIdx.x & 31);
+    if (col0 >= a.N) return;  // uniform over the warp
     float v[32];
-    tmem_load32(taddr, v);
-    if (release) {
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive_at(acc_empty, 0);
-    }
-    if (!first) {
+    auto load = [&] {
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             const float4 r = ld_shared_v4(rc + sw128_offset(lane, j));
-            v[4 * j] += r.x;
-            v[4 * j + 1] += r.y;
-            v[4 * j + 2] += r.z;
-            v[4 * j + 3] += r.w;
+            v[4 * j] = r.x;
+            v[4 * j + 1] = r.y;
+            v[4 * j + 2] = r.z;
+            v[4 * j + 3] = r.w;
+        }
+    };
+    load();
+    bool nan = false;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) nan |= v[j] != v[j];
+    if (nan && row < a.M) {
+        // Repair in shared memory, one column at a time (few registers).
+        const float *A = a.A + (a.a_shared ? 0 : item * a.strideA);
+        const float *B = a.B + (a.b_shared ? 0 : item * a.strideB);
+        if (k_end > a.K) k_end = a.K;
+#pragma unroll 1
+        for (int j = 0; j < 32 && col0 + j < a.N; ++j) {
+            const uint32_t addr = rc + sw128_offset(lane, j >> 2) + static_cast<uint32_t>((j & 3) * 4);
+            const float x = ld_shared_f32(addr);
+            if (x != x) st_shared_f32(addr, dot_ieee(A, a.lda, a.ta, B, a.ldb, a.tb, row, col0 + j, k_begin, k_end));
         }
     }
-    if (col0 >= a.N) return;  // uniform over the warp
+    if (nan) load();
     if (a.ep && !atomic) {
         float bl = 0.0f;
         if (a.bias_kind == SGEMM_BIAS_PER_COL && col0 + lane < a.N) bl = __ldg(a.bias + col0 + lane);
@@ -284,7 +295,7 @@ __device__ __noinline__ void edge_final_chunk(const Args &a, uint32_t taddr, uin
 template <bool VEC_C, bool TA, bool TB>
 __global__ void __launch_bounds__(pr::THREADS, 1)
     tf32x3_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                       const __grid_constant__ CUtensorMap tmC, const Args a) {
+                       const __grid_constant__ CUtensorMap tmC, const __grid_constant__ Args a) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -703,11 +714,6 @@ __global__ void __launch_bounds__(pr::THREADS, 1)
                 for (int ch = 0; ch < pr::CHUNKS; ++ch) {
                     const uint32_t rc = rq + static_cast<uint32_t>(ch * pr::C_CHUNK);
                     const int64_t col0 = at.n0 + ch * 32;
-                    if (last && (!a.c_tma || col0 + 32 > a.N || row0 + 32 > a.M)) {
-                        edge_final_chunk<VEC_C>(a, dt + static_cast<uint32_t>(ch * 32), rc, first, crow, row, col0,
-                                                atomic, ch == pr::CHUNKS - 1, bar(pr::ACC_EMPTY + d));
-                        continue;
-                    }
                     float v[32];
                     tmem_load32(dt + static_cast<uint32_t>(ch * 32), v);
                     if (ch == pr::CHUNKS - 1) release(d);
@@ -729,6 +735,18 @@ __global__ void __launch_bounds__(pr::THREADS, 1)
                         continue;
                     }
                     // The unit's sum is complete: write this chunk of C.
+                    bool nan = false;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) nan |= v[j] != v[j];
+                    if (__any_sync(0xffffffffu, nan) || !a.c_tma || col0 + 32 > a.N || row0 + 32 > a.M) {
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            st_shared_v4(rc + sw128_offset(lane, j), v[4 * j], v[4 * j + 1], v[4 * j + 2],
+                                         v[4 * j + 3]);
+                        edge_final_chunk<VEC_C>(a, rc, crow, row, col0, atomic, at.item,
+                                                static_cast<int64_t>(kb) * BK, static_cast<int64_t>(ke) * BK);
+                        continue;
+                    }
                     if (fused) {
                         // Per-column bias of this chunk: lane l holds column col0 + l.
                         const float bl = col_bias ? __ldg(a.bias + col0 + lane) : rb;
@@ -854,6 +872,8 @@ int launch_pair(const Problem &p, const DeviceInfo &dev, int sk_mode, bool cpa, 
     a.B = p.B;
     a.ldb = p.ldb;
     a.cpa = cpa ? 1 : 0;
+    a.ta = TA ? 1 : 0;
+    a.tb = TB ? 1 : 0;
     a.C = p.C;
     a.ldc = p.ldc;
     a.tiles_n = static_cast<int>(tiles_n);

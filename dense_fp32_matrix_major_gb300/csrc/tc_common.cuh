@@ -70,6 +70,9 @@ struct Args {
     // Operands whose rows TMA cannot address (not 16-byte aligned): the raw
     // ring is filled with 4-byte cp.async copies instead (pair kernel).
     int cpa = 0;
+    // Operand forms (A stored K x M, B stored N x K), for the recomputation of
+    // non-finite outputs (fix_nonfinite).
+    int ta = 0, tb = 0;
     // Longest run of k-blocks one unit may accumulate in TMEM (0: no limit);
     // split units start at multiples of it (see for_each_unit_of).
     int kb_cap = 0;
@@ -345,6 +348,10 @@ __device__ __forceinline__ float ld_shared_f32(uint32_t addr) {
     return v;
 }
 
+__device__ __forceinline__ void st_shared_f32(uint32_t addr, float v) {
+    asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
 __device__ __forceinline__ float4 ld_shared_v4(uint32_t addr) {
     float4 v;
     asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
@@ -568,6 +575,57 @@ __device__ __forceinline__ void store_chunk(const Args &a, float *crow, int64_t 
     }
 }
 
+// op(A)[row][k] * op(B)[k][col] summed over k in [k_begin, k_end) with fp32
+// fused multiply-adds in k order: IEEE arithmetic, infinities and NaN
+// propagating as they do on the CUDA cores. A and B point at the batch
+// item's operands; ta: A stored K x M, tb: B stored N x K.
+__device__ __forceinline__ float dot_ieee(const float *A, int64_t lda, int ta, const float *B, int64_t ldb, int tb,
+                                          int64_t row, int64_t col, int64_t k_begin, int64_t k_end) {
+    float s = 0.0f;
+#pragma unroll 1
+    for (int64_t k = k_begin; k < k_end; ++k) {
+        const float x = ta ? A[k * lda + row] : A[row * lda + k];
+        const float y = tb ? B[col * ldb + k] : B[k * ldb + col];
+        s = fmaf(x, y, s);
+    }
+    return s;
+}
+
+// Non-finite inputs: the three-term split multiplies an infinite high part
+// by the NaN low part (inf - inf) of its own value, so an output that summed
+// an infinity comes out NaN where IEEE arithmetic gives +-inf. Finite inputs
+// never give NaN, so every NaN among v (columns col0 .. col0 + N - 1 of one
+// row of batch item `item`, the sum over the k-range [k_begin, k_end)) is
+// recomputed there with IEEE arithmetic (dot_ieee); NaN inputs give NaN
+// again. Adding such per-range results keeps IEEE's rules (inf + finite =
+// inf, inf - inf = NaN). Called by all 32 lanes: one comparison per value
+// and a warp vote when nothing is NaN. The repair walks the columns in a
+// rolled loop (one copy of the dot product, v kept in registers by selects).
+template <int N>
+__device__ __forceinline__ void fix_nonfinite(const Args &a, int item, int64_t row, int64_t col0, int64_t k_begin,
+                                              int64_t k_end, float (&v)[N]) {
+    bool bad = false;
+#pragma unroll
+    for (int j = 0; j < N; ++j) bad |= v[j] != v[j];
+    if (!__any_sync(0xffffffffu, bad)) return;
+    const float *A = a.A + (a.a_shared ? 0 : item * a.strideA);
+    const float *B = a.B + (a.b_shared ? 0 : item * a.strideB);
+    if (k_end > a.K) k_end = a.K;
+    const bool in_rows = row < a.M;
+#pragma unroll 1
+    for (int j = 0; j < N; ++j) {
+        float x = 0.0f;
+#pragma unroll
+        for (int i = 0; i < N; ++i)
+            if (i == j) x = v[i];
+        if (x == x || !in_rows || col0 + j >= a.N) continue;
+        x = dot_ieee(A, a.lda, a.ta, B, a.ldb, a.tb, row, col0 + j, k_begin, k_end);
+#pragma unroll
+        for (int i = 0; i < N; ++i)
+            if (i == j) v[i] = x;
+    }
+}
+
 // Writes 32 finished values of one row held in registers (columns col0 ..
 // col0 + 31): C = act(alpha * v + beta * C + bias) for a whole tile (the bias
 // and activation with a fused epilogue), C += alpha * v with atomics for a
@@ -594,44 +652,34 @@ __device__ __forceinline__ void store_chunk_regs(const Args &a, float *crow, int
 }
 
 // Epilogue of one 32-column chunk of the accumulator at TMEM address taddr
-// (this thread's lane): loads it and writes C. release: call on_release()
-// once the chunk is out of TMEM (the accumulator may be reused). With a
-// fused bias / activation on a whole tile the chunk goes in two 16-column
-// halves, which leaves the activation the registers it needs.
+// (this thread's lane, the sum over the unit's k-range [k_begin, k_end) of
+// batch item `item`): loads it, repairs non-finite outputs (fix_nonfinite)
+// and writes C (store_chunk_regs). release: call on_release() once the chunk
+// is out of TMEM (the accumulator may be reused).
 template <bool VEC_C, class Release>
 __device__ __forceinline__ void epilogue_chunk_then(const Args &a, uint32_t taddr, float *crow, int64_t row, int64_t col0,
-                                               bool atomic, bool release, Release &&on_release) {
-    if (a.ep && !atomic) {
-        // Bias of this chunk: lane l holds column col0 + l's value (per
-        // column, one coalesced load issued before the TMEM loads) or the
-        // row's value (per row).
-        const int lane = static_cast<int>(threadIdx.x & 31);
-        float bl = 0.0f;
-        if (a.bias_kind == SGEMM_BIAS_PER_COL && col0 + lane < a.N) bl = __ldg(a.bias + col0 + lane);
-        if (a.bias_kind == SGEMM_BIAS_PER_ROW && row < a.M) bl = __ldg(a.bias + row);
-        float v[16];
-        tmem_load16(taddr, v);
-        store16_fused<VEC_C>(a, crow, row, col0, 0, bl, v);
-        tmem_load16(taddr + 16, v);
-        if (release) on_release();
-        store16_fused<VEC_C>(a, crow, row, col0 + 16, 16, bl, v);
-    } else {
-        float v[32];
-        tmem_load32(taddr, v);
-        if (release) on_release();
-        store_chunk<VEC_C>(a, crow, row, col0, v, atomic);
-    }
+                                               bool atomic, bool release, Release &&on_release, int item,
+                                               int64_t k_begin, int64_t k_end) {
+    float v[32];
+    tmem_load32(taddr, v);
+    if (release) on_release();
+    fix_nonfinite(a, item, row, col0, k_begin, k_end, v);
+    store_chunk_regs<VEC_C>(a, crow, row, col0, v, atomic);
 }
 
 // The same, arriving on the CTA's own mbarrier release_bar to free the
 // accumulator.
 template <bool VEC_C>
 __device__ __forceinline__ void epilogue_chunk(const Args &a, uint32_t taddr, float *crow, int64_t row, int64_t col0,
-                                               bool atomic, bool release, uint32_t release_bar) {
-    epilogue_chunk_then<VEC_C>(a, taddr, crow, row, col0, atomic, release, [&] {
-        tc_fence_before();
-        mbar_arrive(release_bar);
-    });
+                                               bool atomic, bool release, uint32_t release_bar, int item,
+                                               int64_t k_begin, int64_t k_end) {
+    epilogue_chunk_then<VEC_C>(
+        a, taddr, crow, row, col0, atomic, release,
+        [&] {
+            tc_fence_before();
+            mbar_arrive(release_bar);
+        },
+        item, k_begin, k_end);
 }
 
 // First split iteration of worker `index` (index = sk_ctas: the end). With
