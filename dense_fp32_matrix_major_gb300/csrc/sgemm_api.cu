@@ -365,7 +365,16 @@ int sgemm_f32_from_host(int64_t M, int64_t N, int64_t K, const float *A_host, in
     // last copy out, so the call keeps the one-stream semantics.
     std::lock_guard<std::mutex> guard(hp->lock);
     const size_t f = sizeof(float);
-    auto fail = [] { return cudaGetLastError(), SGEMM_ERR_LAUNCH; };
+    // On a failure after the fork, `stream` still waits for what the two
+    // library streams hold (best effort), so that, as on success, the
+    // buffers are free for reuse once `stream` has been synchronised.
+    auto fail = [&](int code = SGEMM_ERR_LAUNCH) {
+        cudaGetLastError();
+        if (cudaEventRecord(hp->fork, hp->compute) == cudaSuccess) cudaStreamWaitEvent(s, hp->fork, 0);
+        if (cudaEventRecord(hp->done, hp->d2h) == cudaSuccess) cudaStreamWaitEvent(s, hp->done, 0);
+        cudaGetLastError();
+        return code;
+    };
     if (cudaEventRecord(hp->fork, s) != cudaSuccess || cudaStreamWaitEvent(hp->compute, hp->fork, 0) != cudaSuccess ||
         cudaStreamWaitEvent(hp->d2h, hp->fork, 0) != cudaSuccess)
         return fail();
@@ -380,7 +389,7 @@ int sgemm_f32_from_host(int64_t M, int64_t N, int64_t K, const float *A_host, in
             return fail();
         Problem p{M, wj, K, dA, lda, dB + c0, ldb, dC + c0, ldc};
         rc = sgemm::enqueue(p, hp->compute);
-        if (rc != SGEMM_OK) return rc;
+        if (rc != SGEMM_OK) return fail(rc);
         if (cudaEventRecord(hp->c_out[j], hp->compute) != cudaSuccess ||
             cudaStreamWaitEvent(hp->d2h, hp->c_out[j], 0) != cudaSuccess ||
             cudaMemcpy2DAsync(C_host + c0, ldc * f, dC + c0, ldc * f, wj * f, M, cudaMemcpyDeviceToHost, hp->d2h) !=

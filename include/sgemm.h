@@ -76,10 +76,12 @@ enum sgemm_variant {
  * arithmetic in an order the library chooses; the acceptance bound is
  * max |C - C_exact| / sum_k |A[i][k]| |B[k][j]| <= 1e-5, and inputs whose
  * products and partial sums are integers below 2^24 give exact results.
- * Non-finite inputs: SGEMM_FFMA follows IEEE arithmetic; SGEMM_TF32X3 (what
- * SGEMM_AUTO runs from 2^14 multiply-adds on) gives NaN where IEEE gives
- * +-inf (its split multiplies an infinite high part by a zero low part).
- * NaN inputs give NaN in both.
+ * Non-finite inputs follow IEEE arithmetic on both variants: an infinity
+ * gives +-inf by the signs of the products it takes part in, inf * 0 and
+ * inf - inf give NaN, a NaN input gives NaN in every output that uses it.
+ * (SGEMM_TF32X3's split alone would turn an infinity into NaN: it finds
+ * every NaN it produced and recomputes that output over its k-range with
+ * fp32 fused multiply-adds, at no cost when no output is NaN.)
  * Returns SGEMM_OK or an sgemm_status code; on error nothing is enqueued.
  */
 int sgemm_f32(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, const float *B,
@@ -179,7 +181,10 @@ int sgemm_f32_fused(int transA, int transB, int64_t M, int64_t N, int64_t K, flo
  * strides as the host matrices (lda, ldb, ldc) and at least that many rows.
  * Host buffers should be page-locked (cudaHostAlloc) for the copies to be
  * asynchronous; the caller synchronises the stream before reading C_host.
- * Same sizes, strides, errors and results as sgemm_f32.
+ * Same sizes, strides, errors and results as sgemm_f32, except that an
+ * error may come back after part of the work was enqueued: the buffers are
+ * then in use until `stream` has been synchronised, as on success (`stream`
+ * still waits for whatever the call enqueued on the library streams).
  * Products of at least 2^30 multiply-adds with N >= 512 are pipelined over
  * up to eight column panels of B and C (widths in multiples of 256): A and
  * the B panels are copied in on `stream`, panel j's product runs on a

@@ -135,6 +135,32 @@ def test_forced_tensor_cores_on_unaligned_transposes(lib, tA, tB):
         assert lib.get_tuning(lib.SGEMM_TUNE_LAST_TC_KERNEL) == 4
 
 
+@pytest.mark.parametrize("sk", [0, 3])
+@pytest.mark.parametrize("tA,tB", FORMS)
+def test_forced_pair_kernel_on_tiny_and_ragged_shapes(lib, sk, tA, tB):
+    """The SM-pair kernel forced on products far smaller than its 256 x 128
+    tile (a single row or column of C, M or N below one tile) with K long
+    enough for several fold intervals and, under stream-K, several units per
+    tile: results match the oracle and nothing outside C's box is written, on
+    aligned and unaligned rows."""
+    lib.set_variant("tf32x3")
+    lib.set_tuning(lib.SGEMM_TUNE_TF32X3_KERNEL, 4)
+    lib.set_tuning(lib.SGEMM_TUNE_STREAM_K, sk)
+    try:
+        for i, (M, N, K) in enumerate([(1, 7, 1100), (129, 3, 1100), (3, 129, 700), (1, 1, 2049),
+                                       (17, 300, 2049), (257, 129, 600), (8, 8, 1024)]):
+            As, Bs = _stored(M, N, K, tA, tB, "normal", 40 + i)
+            C0 = np.random.default_rng(i).standard_normal((M, N)).astype(np.float32)
+            _check(lib, As, Bs, tA, tB, 1.25, -0.5, C0)
+            assert lib.get_tuning(lib.SGEMM_TUNE_LAST_TC_KERNEL) == 4, (M, N, K)
+            _check(lib, As, Bs, tA, tB, 1.0, 0.0, C0, lda=As.shape[1] + 1, ldb=Bs.shape[1] + 1, ldc=N + 2,
+                   offsets=(1, 1, 1))
+            assert lib.get_tuning(lib.SGEMM_TUNE_LAST_TC_KERNEL) == 4, (M, N, K)
+    finally:
+        lib.set_tuning(lib.SGEMM_TUNE_TF32X3_KERNEL, 0)
+        lib.set_tuning(lib.SGEMM_TUNE_STREAM_K, 0)
+
+
 @pytest.mark.parametrize("tA,tB", FORMS)
 def test_headline_shape_forms(lib, tA, tB):
     lib.set_variant("auto")
