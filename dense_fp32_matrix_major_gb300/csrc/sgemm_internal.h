@@ -123,10 +123,33 @@ int scale_launch(const Problem &p, const DeviceInfo &dev, cudaStream_t stream, i
 // cannot run the request.
 bool tf32x3_supports(const Problem &p, const DeviceInfo &dev);
 int tf32x3_launch(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStream_t stream, int *launches);
+// The part of tf32x3_launch for operands a tensor map cannot describe. With
+// `scratch` (16-byte aligned, scratch_bytes long) the aligned copies go
+// there instead of into pool memory; SGEMM_ERR_INVALID_ARG when it is too
+// small.
+int tf32x3_launch_unaligned(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStream_t stream,
+                            int *launches, float *scratch, size_t scratch_bytes);
 // The SM-pair kernel (every operand form; cpa: A and B rows not 16-byte
-// aligned, loaded with cp.async instead of TMA).
+// aligned, loaded with cp.async instead of TMA; after_copy: the last kernel
+// enqueued is the aligned copy of A and B, which this launch may overlap).
 int tf32x3_pair_launch(const Problem &p, const DeviceInfo &dev, int sk_mode, bool cpa, cudaStream_t stream,
-                       int *launches);
+                       int *launches, bool after_copy = false);
+
+// Operands whose rows TMA cannot address (repack.cu). tma_operand_ok: the
+// stored matrix X (rows x ld floats per item, items `stride` apart) can be
+// described by a tensor map. repack_bytes: scratch needed to copy every
+// operand of p that fails that test into rows of a multiple of 4 floats (0
+// when none does). repack_into: enqueue those copies on `stream` into
+// `scratch` (16-byte aligned, at least repack_bytes(p) bytes) and set *q to
+// p with the copied operands in place of the originals; nothing is enqueued
+// on error. scratch_alloc / scratch_free: stream-ordered scratch from a pool
+// the library keeps per device (nullptr when it cannot allocate).
+bool tma_operand_ok(const float *X, int64_t ld, int64_t stride, int64_t rows, int64_t batch);
+size_t repack_bytes(const Problem &p);
+int repack_into(const Problem &p, const DeviceInfo &dev, float *scratch, size_t bytes, cudaStream_t stream,
+                Problem *q, int *launches);
+float *scratch_alloc(const DeviceInfo &dev, size_t bytes, cudaStream_t stream);
+void scratch_free(float *ptr, cudaStream_t stream);
 
 // Watchdog flag shared by kernels with bounded waits (one per device, in the
 // tf32x3 translation unit). Read-and-clear; returns 0 or the first recorded code.

@@ -987,14 +987,15 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 
 // TMA requirements: 16-byte aligned bases and row strides, coordinates that
 // fit int32.
-bool tma_ok(const Problem &p) {
-    return (reinterpret_cast<uintptr_t>(p.A) % 16 == 0) && (reinterpret_cast<uintptr_t>(p.B) % 16 == 0) &&
-           (p.lda % 4 == 0) && (p.ldb % 4 == 0) && (p.strideA % 4 == 0) && (p.strideB % 4 == 0) &&
-           p.M < INT32_MAX / 2 && p.N < INT32_MAX / 2 && p.K < INT32_MAX / 2 && p.batch < INT32_MAX / 2 &&
-           // batch items of A and B that overlap cannot be described as a tensor
-           (p.batch == 1 || p.strideA == 0 || p.strideA >= (p.transA ? p.K : p.M) * p.lda) &&
-           (p.batch == 1 || p.strideB == 0 || p.strideB >= (p.transB ? p.N : p.K) * p.ldb) &&
+// Sizes a tensor map can describe, and the driver entry point that encodes one.
+bool tma_sizes_ok(const Problem &p) {
+    return p.M < INT32_MAX / 2 && p.N < INT32_MAX / 2 && p.K < INT32_MAX / 2 && p.batch < INT32_MAX / 2 &&
            tensor_map_encoder() != nullptr;
+}
+
+bool tma_ok(const Problem &p) {
+    return tma_operand_ok(p.A, p.lda, p.strideA, p.transA ? p.K : p.M, p.batch) &&
+           tma_operand_ok(p.B, p.ldb, p.strideB, p.transB ? p.N : p.K, p.batch) && tma_sizes_ok(p);
 }
 
 std::once_flag g_tma_attr_once[kMaxDevices][16];
@@ -1149,7 +1150,7 @@ int watchdog_selftest_launch(int64_t wait_ms, cudaStream_t stream) {
 }
 
 int tf32x3_set_kernel(int64_t mode) {
-    if (mode < 0 || mode > 4) return SGEMM_ERR_INVALID_ARG;
+    if (mode < 0 || mode > 5) return SGEMM_ERR_INVALID_ARG;
     g_use_tma.store(static_cast<int>(mode));
     return SGEMM_OK;
 }
@@ -1171,53 +1172,96 @@ bool tf32x3_supports(const Problem &p, const DeviceInfo &dev) {
            dev.smem_optin >= static_cast<size_t>(tma::SMEM_BYTES);
 }
 
+namespace {
+
+// The TMA kernels, for operands a tensor map can describe: the SM-pair
+// kernel from 2^20 multiply-adds on (or when forced), else the single-SM
+// kernels. Measured on GB300, L2 flushed, pair vs tensor-memory kernel:
+// 128^3 14.4 vs 15.7 us, 512^3 17.5 vs 22.2, 2048 x 128 x 512 17.2 vs 20.5,
+// 200 x 4096 x 4096 52.4 vs 68.6, 1024^3 27.5 vs 33.4; all four forms.
+int launch_aligned(const Problem &p, const DeviceInfo &dev, int sk_mode, int mode, cudaStream_t stream,
+                   int *launches, bool after_copy = false) {
+    const bool vc = (p.ldc % 4 == 0) && (p.strideC % 4 == 0) && (reinterpret_cast<uintptr_t>(p.C) % 16 == 0);
+    const double work = static_cast<double>(p.M) * static_cast<double>(p.N) * static_cast<double>(p.K) *
+                        static_cast<double>(p.batch);
+    const bool pair = mode == 4 || (mode == 0 && work >= 1048576.0);
+    if (pair) {
+        g_last_tc_kernel.store(4);
+        return tf32x3_pair_launch(p, dev, sk_mode, false, stream, launches, after_copy);
+    }
+    g_last_tc_kernel.store(mode == 2 && !p.transA && !p.transB ? 2 : 3);
+    if (p.transA && p.transB)
+        return vc ? launch_tma<true, true, true, true>(p, dev, sk_mode, stream, launches)
+                  : launch_tma<true, false, true, true>(p, dev, sk_mode, stream, launches);
+    if (p.transA)
+        return vc ? launch_tma<true, true, true, false>(p, dev, sk_mode, stream, launches)
+                  : launch_tma<true, false, true, false>(p, dev, sk_mode, stream, launches);
+    if (p.transB)
+        return vc ? launch_tma<true, true, false, true>(p, dev, sk_mode, stream, launches)
+                  : launch_tma<true, false, false, true>(p, dev, sk_mode, stream, launches);
+    if (mode == 2)
+        return vc ? launch_tma<false, true>(p, dev, sk_mode, stream, launches)
+                  : launch_tma<false, false>(p, dev, sk_mode, stream, launches);
+    return vc ? launch_tma<true, true>(p, dev, sk_mode, stream, launches)
+              : launch_tma<true, false>(p, dev, sk_mode, stream, launches);
+}
+
+// Smallest product (multiply-adds) for which copying operands with
+// unaligned rows into aligned scratch and running the TMA kernels beats the
+// per-thread-load kernel (measured on GB300, L2 flushed, rows of K + 1 and
+// N + 1 floats, copies + TMA kernels vs per-thread loads: 511 x 511 x 513
+// 37.9 vs 30.7 us, 1023 x 2049 x 1537 54.3 vs 86.0, 2047 x 3071 x 4095
+// 188 vs 376).
+constexpr double kRepackMinWork = 268435456.0;
+
+}  // namespace
+
 int tf32x3_launch(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStream_t stream, int *launches) {
     if (!tf32x3_supports(p, dev) || dev.device < 0 || dev.device >= kMaxDevices) return SGEMM_ERR_UNSUPPORTED;
-    const bool vc = (p.ldc % 4 == 0) && (p.strideC % 4 == 0) && (reinterpret_cast<uintptr_t>(p.C) % 16 == 0);
     const int mode = g_use_tma.load();
     // The transposed forms always take a TMA kernel (the per-thread-load
     // kernel serves op(A) = A, op(B) = B only).
-    if (tma_ok(p) && (mode != 1 || p.transA || p.transB)) {
-        // Automatic: the SM-pair kernel from 2^20 multiply-adds on, any
-        // shape (measured on GB300, L2 flushed, pair vs single-SM kernel:
-        // 64^3 11.3 vs 10.4 us, 128^3 12.3 vs 14.5, 512^3 16.4 vs 19.7,
-        // 2048 x 128 x 512 17.4 vs 20.2, 200 x 4096 x 4096 49.2 vs 67.6,
-        // 1024^3 25.6 vs 31.3); all four operand forms.
-        const double work = static_cast<double>(p.M) * static_cast<double>(p.N) * static_cast<double>(p.K) *
-                            static_cast<double>(p.batch);
-        const bool pair = mode == 4 || (mode == 0 && work >= 1048576.0);
-        if (pair) {
-            g_last_tc_kernel.store(4);
-            return tf32x3_pair_launch(p, dev, sk_mode, false, stream, launches);
+    if (tma_ok(p) && (mode != 1 || p.transA || p.transB))
+        return launch_aligned(p, dev, sk_mode, mode == 5 ? 0 : mode, stream, launches);
+    return tf32x3_launch_unaligned(p, dev, sk_mode, stream, launches, nullptr, 0);
+}
+
+int tf32x3_launch_unaligned(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStream_t stream,
+                            int *launches, float *scratch, size_t scratch_bytes) {
+    const int mode = g_use_tma.load();
+    const double work = static_cast<double>(p.M) * static_cast<double>(p.N) * static_cast<double>(p.K) *
+                        static_cast<double>(p.batch);
+    // Automatic (from kRepackMinWork on) or forced (5): copy the operands
+    // whose rows TMA cannot address into rows of a multiple of 4 floats (a
+    // memory-bound pass) and run the TMA kernels. Scratch: the caller's
+    // buffer, else the library's stream-ordered pool, freed on `stream`
+    // behind the product.
+    if (((mode == 0 && work >= kRepackMinWork) || mode == 5) && tma_sizes_ok(p)) {
+        const size_t bytes = repack_bytes(p);
+        float *buf = scratch;
+        if (!buf) buf = scratch_alloc(dev, bytes, stream);
+        if (buf && (scratch == nullptr || scratch_bytes >= bytes)) {
+            Problem q;
+            int rc = repack_into(p, dev, buf, bytes, stream, &q, launches);
+            if (rc == SGEMM_OK) rc = launch_aligned(q, dev, sk_mode, 0, stream, launches, true);
+            if (!scratch) scratch_free(buf, stream);
+            return rc;
         }
-        g_last_tc_kernel.store(mode == 2 && !p.transA && !p.transB ? 2 : 3);
-        if (p.transA && p.transB)
-            return vc ? launch_tma<true, true, true, true>(p, dev, sk_mode, stream, launches)
-                      : launch_tma<true, false, true, true>(p, dev, sk_mode, stream, launches);
-        if (p.transA)
-            return vc ? launch_tma<true, true, true, false>(p, dev, sk_mode, stream, launches)
-                      : launch_tma<true, false, true, false>(p, dev, sk_mode, stream, launches);
-        if (p.transB)
-            return vc ? launch_tma<true, true, false, true>(p, dev, sk_mode, stream, launches)
-                      : launch_tma<true, false, false, true>(p, dev, sk_mode, stream, launches);
-        if (mode == 2)
-            return vc ? launch_tma<false, true>(p, dev, sk_mode, stream, launches)
-                      : launch_tma<false, false>(p, dev, sk_mode, stream, launches);
-        return vc ? launch_tma<true, true>(p, dev, sk_mode, stream, launches)
-                  : launch_tma<true, false>(p, dev, sk_mode, stream, launches);
+        if (scratch) return SGEMM_ERR_INVALID_ARG;
     }
-    // Rows that TMA cannot address (or per-thread loads forced): the
-    // per-thread-load kernel for op(A) = A, op(B) = B; the SM-pair kernel with
-    // cp.async loaders for the transposed forms (which the per-thread-load
-    // kernel does not serve) or when forced (4). Its 4-byte copies are slow
-    // to issue (measured on GB300: ~5.5 us for one warp's half of a k-block,
-    // so 1023 x 2049 x 1537 with rows of 1537 and 2049 floats takes 309 us
-    // there against 131 us on the per-thread-load kernel).
+    // Per-thread loads: the per-thread-load kernel for op(A) = A, op(B) = B;
+    // the SM-pair kernel with cp.async loaders for the transposed forms
+    // (which the per-thread-load kernel does not serve) or when forced (4).
+    // Its 4-byte copies are slow to issue (measured on GB300: ~5.5 us for
+    // one warp's half of a k-block, so 1023 x 2049 x 1537 with rows of 1537
+    // and 2049 floats takes 309 us there against 86 us on the
+    // per-thread-load kernel).
     if (p.transA || p.transB || mode == 4) {
         g_last_tc_kernel.store(4);
         return tf32x3_pair_launch(p, dev, sk_mode, true, stream, launches);
     }
     g_last_tc_kernel.store(1);
+    const bool vc = (p.ldc % 4 == 0) && (p.strideC % 4 == 0) && (reinterpret_cast<uintptr_t>(p.C) % 16 == 0);
     const bool va = (p.lda % 4 == 0) && (p.strideA % 4 == 0) && (reinterpret_cast<uintptr_t>(p.A) % 16 == 0);
     const bool vb = (p.ldb % 4 == 0) && (p.strideB % 4 == 0) && (reinterpret_cast<uintptr_t>(p.B) % 16 == 0);
     const int idx = (va ? 4 : 0) + (vb ? 2 : 0) + (vc ? 1 : 0);

@@ -233,35 +233,28 @@ __device__ __forceinline__ void stage32_fused(int act, uint32_t buf, int lane, f
 }
 
 // The last fold of a unit for a chunk written with per-thread stores: the
-// unit's finished sum for this lane's row, columns col0 .. col0 + 31 (chunk
-// rc of shared memory, swizzled), repaired where it is NaN (fix_nonfinite,
-// over the unit's k-range [k_begin, k_end) of batch item `item`), then C =
-// alpha * v + beta * C (+ bias, activation) for a whole tile or C += alpha *
-// v with atomics for a tile split along K. Used for chunks that cross the
-// last row or column of C, for C that TMA cannot write and for chunks holding
-// a NaN; called by all 32 lanes (the bias shuffles and the NaN vote). Out of
-// line: it is rare, and inlined it would compete for registers with the
-// interior path.
+// unit's finished sum for rows row0 .. row0 + 31, columns col0 .. col0 + 31
+// (chunk rc of shared memory, swizzled, lane l holding row row0 + l),
+// repaired where it is NaN (recomputed over the unit's k-range [k_begin,
+// k_end) of batch item `item`), then written one row per step with the lanes
+// along the row (coalesced): C = act(alpha * v + beta * C + bias) for a
+// whole tile, C += alpha * v with atomics for a tile split along K. Used for
+// chunks that cross the last row or column of C, for C that TMA cannot
+// address and for chunks holding a NaN; called by all 32 lanes. Out of line:
+// it is rare, and inlined it would compete for registers with the interior
+// path.
 template <bool VEC_C>
-__device__ __noinline__ void edge_final_chunk(const Args &a, uint32_t rc, float *crow, int64_t row, int64_t col0,
+__device__ __noinline__ void edge_final_chunk(const Args &a, uint32_t rc, float *citem, int64_t row0, int64_t col0,
                                               bool atomic, int item, int64_t k_begin, int64_t k_end) {
     const int lane = static_cast<int>(threadIdx.x & 31);
     if (col0 >= a.N) return;  // uniform over the warp
-    float v[32];
-    auto load = [&] {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const float4 r = ld_shared_v4(rc + sw128_offset(lane, j));
-            v[4 * j] = r.x;
-            v[4 * j + 1] = r.y;
-            v[4 * j + 2] = r.z;
-            v[4 * j + 3] = r.w;
-        }
-    };
-    load();
+    const int64_t row = row0 + lane;
     bool nan = false;
 #pragma unroll
-    for (int j = 0; j < 32; ++j) nan |= v[j] != v[j];
+    for (int j = 0; j < 8; ++j) {
+        const float4 r = ld_shared_v4(rc + sw128_offset(lane, j));
+        nan |= r.x != r.x || r.y != r.y || r.z != r.z || r.w != r.w;
+    }
     if (nan && row < a.M) {
         // Repair in shared memory, one column at a time (few registers).
         const float *A = a.A + (a.a_shared ? 0 : item * a.strideA);
@@ -274,20 +267,51 @@ __device__ __noinline__ void edge_final_chunk(const Args &a, uint32_t rc, float 
             if (x != x) st_shared_f32(addr, dot_ieee(A, a.lda, a.ta, B, a.ldb, a.tb, row, col0 + j, k_begin, k_end));
         }
     }
-    if (nan) load();
-    if (a.ep && !atomic) {
-        float bl = 0.0f;
-        if (a.bias_kind == SGEMM_BIAS_PER_COL && col0 + lane < a.N) bl = __ldg(a.bias + col0 + lane);
-        if (a.bias_kind == SGEMM_BIAS_PER_ROW && row < a.M) bl = __ldg(a.bias + row);
-        float h[16];
+    __syncwarp();
+    // Parameters in registers: the shared-memory loads below are ordered
+    // against all memory, so fields read through `a` would be reloaded on
+    // every row.
+    const int64_t M = a.M, ldc = a.ldc, col = col0 + lane;
+    const bool col_ok = col < a.N;
+    const bool fused = a.ep && !atomic;
+    const int bias_kind = fused ? a.bias_kind : SGEMM_BIAS_NONE, act = a.act;
+    const float *bias = a.bias;
+    const float bcol = (bias_kind == SGEMM_BIAS_PER_COL && col_ok) ? __ldg(bias + col) : 0.0f;
+    const float alpha = a.alpha, beta = a.beta;
+    float *p = citem + row0 * ldc + col;
+    if (!fused) {
+        // All 32 values first (independent shared loads), then the stores.
+        float x[32];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) h[j] = v[j];
-        store16_fused<VEC_C>(a, crow, row, col0, 0, bl, h);
+        for (int r = 0; r < 32; ++r)
+            x[r] = ld_shared_f32(rc + sw128_offset(r, lane >> 2) + static_cast<uint32_t>((lane & 3) * 4));
+        if (!col_ok) return;
+        const int rows = M - row0 < 32 ? static_cast<int>(M - row0) : 32;
+        // Separate loops: with beta in the store expression the compiler
+        // loads C ahead of every store, beta or not.
+        if (atomic) {
 #pragma unroll
-        for (int j = 0; j < 16; ++j) h[j] = v[16 + j];
-        store16_fused<VEC_C>(a, crow, row, col0 + 16, 16, bl, h);
-    } else {
-        store_chunk<VEC_C>(a, crow, row, col0, v, atomic);
+            for (int r = 0; r < 32; ++r)
+                if (r < rows) atomicAdd(p + r * ldc, alpha * x[r]);
+        } else if (beta == 0.0f) {
+#pragma unroll
+            for (int r = 0; r < 32; ++r)
+                if (r < rows) p[r * ldc] = alpha * x[r];
+        } else {
+#pragma unroll
+            for (int r = 0; r < 32; ++r)
+                if (r < rows) p[r * ldc] = fmaf(beta, p[r * ldc], alpha * x[r]);
+        }
+        return;
+    }
+#pragma unroll 1
+    for (int r = 0; r < 32 && row0 + r < M; ++r, p += ldc) {  // the row bound is uniform over the warp
+        const float x = ld_shared_f32(rc + sw128_offset(r, lane >> 2) + static_cast<uint32_t>((lane & 3) * 4));
+        if (!col_ok) continue;
+        float y = alpha * x;
+        if (beta != 0.0f) y = fmaf(beta, *p, y);
+        y += bias_kind == SGEMM_BIAS_PER_COL ? bcol : (bias_kind == SGEMM_BIAS_PER_ROW ? __ldg(bias + row0 + r) : 0.0f);
+        *p = activate(y, act);
     }
 }
 
@@ -315,6 +339,7 @@ __global__ void __launch_bounds__(pr::THREADS, 1)
     // the k-blocks it = from .. to - 1 of its units, into the raw ring.
     const bool tma_warp = warp == 1 || warp == pr::TMA_B_WARP;
     auto tma_pass = [&](uint32_t from, uint32_t to) {
+        if (a.wait_inputs) asm volatile("griddepcontrol.wait;" ::: "memory");
         const bool is_a = warp == 1;
         uint32_t it = 0;
         bool ok = true;
@@ -364,6 +389,7 @@ __global__ void __launch_bounds__(pr::THREADS, 1)
     // K x N plain), zero outside the matrices. Every lane's copies for a slot
     // are tracked by one cp.async arrival on the slot's full barrier.
     auto load_pass = [&](uint32_t from, uint32_t to) {
+        if (a.wait_inputs) asm volatile("griddepcontrol.wait;" ::: "memory");
         const int half = warp == 1 ? 0 : 1;
         uint32_t it = 0;
         bool ok = true;
@@ -698,7 +724,6 @@ __global__ void __launch_bounds__(pr::THREADS, 1)
             const bool fused = a.ep && !atomic;
             const bool col_bias = a.bias_kind == SGEMM_BIAS_PER_COL;
             const float rb = (a.bias_kind == SGEMM_BIAS_PER_ROW && row < a.M) ? __ldg(a.bias + row) : 0.0f;
-            float *crow = a.C + at.item * a.strideC + row * a.ldc;
             // The previous unit's TMA stores read the running sum: wait until
             // they have, before this unit overwrites it.
             if (lane == 0) bulk_wait_read<0>();
@@ -743,7 +768,7 @@ __global__ void __launch_bounds__(pr::THREADS, 1)
                         for (int j = 0; j < 8; ++j)
                             st_shared_v4(rc + sw128_offset(lane, j), v[4 * j], v[4 * j + 1], v[4 * j + 2],
                                          v[4 * j + 3]);
-                        edge_final_chunk<VEC_C>(a, rc, crow, row, col0, atomic, at.item,
+                        edge_final_chunk<VEC_C>(a, rc, a.C + at.item * a.strideC, row0, col0, atomic, at.item,
                                                 static_cast<int64_t>(kb) * BK, static_cast<int64_t>(ke) * BK);
                         continue;
                     }
@@ -800,7 +825,8 @@ cudaError_t g_pair_err[kMaxDevices][8];
 int g_pair_clusters[kMaxDevices][8];
 
 template <bool VEC_C, bool TA, bool TB>
-int launch_pair(const Problem &p, const DeviceInfo &dev, int sk_mode, bool cpa, cudaStream_t stream, int *launches) {
+int launch_pair(const Problem &p, const DeviceInfo &dev, int sk_mode, bool cpa, bool after_copy, cudaStream_t stream,
+                int *launches) {
     auto kernel = tf32x3_pair_kernel<VEC_C, TA, TB>;
     constexpr int idx = (VEC_C ? 1 : 0) + (TA ? 2 : 0) + (TB ? 4 : 0);
     cudaLaunchAttribute attr[2];
@@ -903,7 +929,10 @@ int launch_pair(const Problem &p, const DeviceInfo &dev, int sk_mode, bool cpa, 
     // Behind our own beta pre-pass (which touches only C, and which started
     // after everything before it in the stream had finished) the main loop
     // may overlap it; the epilogue waits for it (griddepcontrol.wait).
-    cfg.numAttrs = split > 0 ? 2 : 1;
+    // Right behind the aligned copies of A and B the prologue overlaps them
+    // and the loaders wait.
+    a.wait_inputs = (after_copy && split == 0) ? 1 : 0;
+    cfg.numAttrs = (split > 0 || a.wait_inputs) ? 2 : 1;
     if (cudaLaunchKernelEx(&cfg, kernel, mapA, mapB, mapC, a) != cudaSuccess) {
         cudaGetLastError();
         return SGEMM_ERR_LAUNCH;
@@ -916,19 +945,19 @@ int launch_pair(const Problem &p, const DeviceInfo &dev, int sk_mode, bool cpa, 
 }  // namespace
 
 int tf32x3_pair_launch(const Problem &p, const DeviceInfo &dev, int sk_mode, bool cpa, cudaStream_t stream,
-                       int *launches) {
+                       int *launches, bool after_copy) {
     if (dev.device < 0 || dev.device >= kMaxDevices) return SGEMM_ERR_DEVICE;
     const bool vc = (p.ldc % 4 == 0) && (p.strideC % 4 == 0) && (reinterpret_cast<uintptr_t>(p.C) % 16 == 0);
     const int form = (vc ? 1 : 0) + (p.transA ? 2 : 0) + (p.transB ? 4 : 0);
     switch (form) {
-        case 0: return launch_pair<false, false, false>(p, dev, sk_mode, cpa, stream, launches);
-        case 1: return launch_pair<true, false, false>(p, dev, sk_mode, cpa, stream, launches);
-        case 2: return launch_pair<false, true, false>(p, dev, sk_mode, cpa, stream, launches);
-        case 3: return launch_pair<true, true, false>(p, dev, sk_mode, cpa, stream, launches);
-        case 4: return launch_pair<false, false, true>(p, dev, sk_mode, cpa, stream, launches);
-        case 5: return launch_pair<true, false, true>(p, dev, sk_mode, cpa, stream, launches);
-        case 6: return launch_pair<false, true, true>(p, dev, sk_mode, cpa, stream, launches);
-        default: return launch_pair<true, true, true>(p, dev, sk_mode, cpa, stream, launches);
+        case 0: return launch_pair<false, false, false>(p, dev, sk_mode, cpa, after_copy, stream, launches);
+        case 1: return launch_pair<true, false, false>(p, dev, sk_mode, cpa, after_copy, stream, launches);
+        case 2: return launch_pair<false, true, false>(p, dev, sk_mode, cpa, after_copy, stream, launches);
+        case 3: return launch_pair<true, true, false>(p, dev, sk_mode, cpa, after_copy, stream, launches);
+        case 4: return launch_pair<false, false, true>(p, dev, sk_mode, cpa, after_copy, stream, launches);
+        case 5: return launch_pair<true, false, true>(p, dev, sk_mode, cpa, after_copy, stream, launches);
+        case 6: return launch_pair<false, true, true>(p, dev, sk_mode, cpa, after_copy, stream, launches);
+        default: return launch_pair<true, true, true>(p, dev, sk_mode, cpa, after_copy, stream, launches);
     }
 }
 

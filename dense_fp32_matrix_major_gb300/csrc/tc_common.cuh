@@ -79,6 +79,10 @@ struct Args {
     // A pass (the activation of split tiles) follows as a programmatic
     // dependent: signal griddepcontrol.launch_dependents.
     int signal_dependents = 0;
+    // Launched as the programmatic dependent of the kernel that writes A and
+    // B (aligned copies): the loaders wait for it (griddepcontrol.wait)
+    // before their first read.
+    int wait_inputs = 0;
     // Cost, in k-blocks, of a switch from one split tile to the next inside
     // one worker's share (the next unit's MMAs wait for the accumulator to be
     // read out). With it the split iterations are shared so that k-blocks
@@ -568,10 +572,16 @@ __device__ __forceinline__ void store_chunk(const Args &a, float *crow, int64_t 
             }
             *p = o;
         }
+    } else if (beta == 0.0f) {
+        // Separate loops: with beta in the store expression the compiler
+        // loads C ahead of every store, beta or not.
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            if (col0 + j < N) crow[col0 + j] = alpha * v[j];
     } else {
 #pragma unroll
         for (int j = 0; j < 32; ++j)
-            if (col0 + j < N) crow[col0 + j] = beta != 0.0f ? fmaf(beta, crow[col0 + j], alpha * v[j]) : alpha * v[j];
+            if (col0 + j < N) crow[col0 + j] = fmaf(beta, crow[col0 + j], alpha * v[j]);
     }
 }
 

@@ -17,9 +17,16 @@
  *   - Sizes and strides are int64_t element counts.
  *   - Matrix pointers are device pointers (memory that the current CUDA
  *     device can read and write), except where an entry point says "host".
- *   - The caller owns every buffer. The library allocates no device or host
- *     memory in any call, keeps no pointer after a call returns, and never
- *     synchronises the stream.
+ *   - The caller owns every buffer. The library keeps no pointer after a
+ *     call returns and never synchronises the stream. It allocates device
+ *     memory in one case only: a tensor-core product whose A or B rows are
+ *     not 16-byte aligned (row stride or base address), from 2^28
+ *     multiply-adds on, copies those operands into aligned rows in scratch
+ *     taken from a stream-ordered pool the library creates per device on
+ *     first use (cudaMallocFromPoolAsync on `stream`, freed with
+ *     cudaFreeAsync on `stream` behind the product; the pool keeps up to
+ *     512 MiB between calls). If that allocation fails the product runs
+ *     without the copies. No host memory is allocated.
  *   - Calls are asynchronous: they enqueue work on `stream` and return. A
  *     NULL stream means the legacy default stream. Errors raised by a kernel
  *     while it runs surface on the stream (cudaStreamSynchronize), not here.
@@ -254,17 +261,22 @@ int sgemm_watchdog_selftest(int64_t wait_ms, sgemm_stream_t stream);
  *                            where A and B have 16-byte aligned bases and
  *                            row strides, the SM-pair kernel from 2^20
  *                            multiply-adds on and the TMA kernel with A in
- *                            tensor memory below; otherwise per-thread loads
- *                            (the SM-pair kernel for the transposed forms);
+ *                            tensor memory below; otherwise, from 2^28
+ *                            multiply-adds on, the unaligned operands are
+ *                            first copied into aligned rows (scratch from a
+ *                            stream-ordered pool, see sgemm_f32) and the TMA
+ *                            kernels run; below that per-thread loads (the
+ *                            SM-pair kernel for the transposed forms);
  *                            1 = per-thread loads, 2 = TMA, 3 = TMA with A's
  *                            operands in tensor memory, 4 = SM pairs (tcgen05
  *                            cta_group::2 on clusters of two CTAs; TMA loads
- *                            for 16-byte aligned rows, cp.async otherwise).
- *                            Kernels 2 and 3 need 16-byte aligned rows (else
- *                            kernel 1 runs, or kernel 4 for the transposed
- *                            forms); kernel 1 serves op(A) = A, op(B) = B
- *                            only (the transposed forms take kernel 3 when
- *                            the rows are aligned, else kernel 4).
+ *                            for 16-byte aligned rows, cp.async otherwise),
+ *                            5 = as 0, but unaligned operands are copied at
+ *                            any size. Kernels 2 and 3 need 16-byte aligned
+ *                            rows (else kernel 1 runs, or kernel 4 for the
+ *                            transposed forms); kernel 1 serves op(A) = A,
+ *                            op(B) = B only (the transposed forms take kernel
+ *                            3 when the rows are aligned, else kernel 4).
  * Returns SGEMM_OK or SGEMM_ERR_INVALID_ARG. sgemm_get_tuning returns the
  * value, or -1 for an unknown key.
  */
