@@ -176,6 +176,73 @@ int enqueue(const Problem &p, cudaStream_t stream) {
     return rc;
 }
 
+// sgemm_f32_noalloc's fixed scratch: one buffer per device (the copies of
+// operands whose rows TMA cannot address), looked up once per device.
+static __device__ __align__(256) float g_noalloc_scratch[SGEMM_NOALLOC_SCRATCH_BYTES / sizeof(float)];
+
+struct NoallocSlot {
+    std::once_flag once;
+    float *ptr = nullptr;
+};
+NoallocSlot g_noalloc[kMaxDevices];
+
+// The device address of the fixed buffer on the current device, or nullptr.
+float *noalloc_scratch(int device) {
+    std::call_once(g_noalloc[device].once, [device] {
+        void *ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess) {
+            cudaGetLastError();
+            return;
+        }
+        g_noalloc[device].ptr = static_cast<float *>(ptr);
+    });
+    return g_noalloc[device].ptr;
+}
+
+// enqueue() with the fixed buffer in place of pool memory; SGEMM_ERR_SCRATCH
+// when the copies do not fit (nothing enqueued).
+int enqueue_noalloc(const Problem &p, cudaStream_t stream) {
+    read_env();
+    DeviceInfo dev;
+    int rc = current_device(&dev);
+    if (rc != SGEMM_OK) return rc;
+    int launches = 0;
+    if (p.M == 0 || p.N == 0 || p.batch == 0) {
+        g_last_launches.store(0);
+        return SGEMM_OK;
+    }
+    if (p.K == 0 || p.alpha == 0.0f) {
+        rc = scale_launch(p, dev, stream, &launches);
+        if (rc == SGEMM_OK) {
+            g_last_variant.store(SGEMM_FFMA);
+            g_last_launches.store(launches);
+        }
+        return rc;
+    }
+    int variant = g_variant.load();
+    if (variant == SGEMM_AUTO) variant = auto_variant(p, dev);
+    if (variant == SGEMM_TF32X3) {
+        if (!tf32x3_supports(p, dev)) return SGEMM_ERR_UNSUPPORTED;
+        const size_t bytes = tf32x3_copy_bytes(p);
+        float *scratch = nullptr;
+        if (bytes > 0) {
+            if (bytes > SGEMM_NOALLOC_SCRATCH_BYTES) return SGEMM_ERR_SCRATCH;
+            scratch = noalloc_scratch(dev.device);
+            if (!scratch) return SGEMM_ERR_DEVICE;
+        }
+        rc = tf32x3_launch_with_scratch(p, dev, static_cast<int>(g_tune_sk.load()), stream, &launches, scratch,
+                                        scratch ? SGEMM_NOALLOC_SCRATCH_BYTES : 0);
+    } else {
+        rc = ffma_launch(p, dev, static_cast<int>(g_tune_tile.load()), static_cast<int>(g_tune_sk.load()),
+                         stream, &launches);
+    }
+    if (rc == SGEMM_OK) {
+        g_last_variant.store(variant);
+        g_last_launches.store(launches);
+    }
+    return rc;
+}
+
 }  // namespace
 
 int current_device(DeviceInfo *info) {
@@ -218,6 +285,14 @@ int sgemm_f32(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, cons
     if (rc != SGEMM_OK) return rc;
     Problem p{M, N, K, A, lda, B, ldb, C, ldc};
     return sgemm::enqueue(p, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int sgemm_f32_noalloc(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, const float *B, int64_t ldb,
+                      float *C, int64_t ldc, sgemm_stream_t stream) {
+    int rc = sgemm::check_args(SGEMM_OP_N, SGEMM_OP_N, M, N, K, A, lda, B, ldb, C, ldc);
+    if (rc != SGEMM_OK) return rc;
+    Problem p{M, N, K, A, lda, B, ldb, C, ldc};
+    return sgemm::enqueue_noalloc(p, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int sgemm_f32_ex(int transA, int transB, int64_t M, int64_t N, int64_t K, float alpha, const float *A,
@@ -434,6 +509,7 @@ const char *sgemm_strerror(int status) {
         case SGEMM_ERR_LAUNCH: return "CUDA launch or copy failed";
         case SGEMM_ERR_DEVICE: return "no usable sm_103a device";
         case SGEMM_ERR_TIMEOUT: return "a kernel gave up a bounded wait";
+        case SGEMM_ERR_SCRATCH: return "product needs more scratch than the fixed no-allocation buffer holds";
         default: return "unknown status";
     }
 }

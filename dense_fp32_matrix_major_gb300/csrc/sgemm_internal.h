@@ -129,6 +129,11 @@ int tf32x3_launch(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStre
 // small.
 int tf32x3_launch_unaligned(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStream_t stream,
                             int *launches, float *scratch, size_t scratch_bytes);
+// Scratch bytes tf32x3_launch would take from the pool for p (0: none), and
+// tf32x3_launch with the caller's scratch buffer in place of the pool.
+size_t tf32x3_copy_bytes(const Problem &p);
+int tf32x3_launch_with_scratch(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStream_t stream,
+                               int *launches, float *scratch, size_t scratch_bytes);
 // The SM-pair kernel (every operand form; cpa: A and B rows not 16-byte
 // aligned, loaded with cp.async instead of TMA; after_copy: the last kernel
 // enqueued is the aligned copy of A and B, which this launch may overlap).

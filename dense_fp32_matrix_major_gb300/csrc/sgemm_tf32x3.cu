@@ -1277,4 +1277,22 @@ int tf32x3_launch_unaligned(const Problem &p, const DeviceInfo &dev, int sk_mode
     }
 }
 
+size_t tf32x3_copy_bytes(const Problem &p) {
+    const int mode = g_use_tma.load();
+    if (tma_ok(p) && (mode != 1 || p.transA || p.transB)) return 0;
+    const double work = static_cast<double>(p.M) * static_cast<double>(p.N) * static_cast<double>(p.K) *
+                        static_cast<double>(p.batch);
+    if (((mode == 0 && work >= kRepackMinWork) || mode == 5) && tma_sizes_ok(p)) return repack_bytes(p);
+    return 0;
+}
+
+int tf32x3_launch_with_scratch(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStream_t stream,
+                               int *launches, float *scratch, size_t scratch_bytes) {
+    if (!tf32x3_supports(p, dev) || dev.device < 0 || dev.device >= kMaxDevices) return SGEMM_ERR_UNSUPPORTED;
+    const int mode = g_use_tma.load();
+    if (tma_ok(p) && (mode != 1 || p.transA || p.transB))
+        return launch_aligned(p, dev, sk_mode, mode == 5 ? 0 : mode, stream, launches);
+    return tf32x3_launch_unaligned(p, dev, sk_mode, stream, launches, scratch, scratch_bytes);
+}
+
 }  // namespace sgemm

@@ -20,6 +20,8 @@ SGEMM_ERR_UNSUPPORTED = 2
 SGEMM_ERR_LAUNCH = 3
 SGEMM_ERR_DEVICE = 4
 SGEMM_ERR_TIMEOUT = 5
+SGEMM_ERR_SCRATCH = 6
+SGEMM_NOALLOC_SCRATCH_BYTES = 64 << 20
 
 SGEMM_OP_N = 0
 SGEMM_OP_T = 1
@@ -52,6 +54,7 @@ SGEMM_TUNE_LAST_TC_KERNEL = 5
 _i64, _int, _vp, _cp = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_char_p
 SIGNATURES = {
     "sgemm_f32": (_int, [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _vp]),
+    "sgemm_f32_noalloc": (_int, [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _vp]),
     "sgemm_f32_ex": (_int, [_int, _int, _i64, _i64, _i64, ctypes.c_float, _vp, _i64, _vp, _i64,
                             ctypes.c_float, _vp, _i64, _vp]),
     "sgemm_f32_batched": (_int, [_int, _int, _i64, _i64, _i64, ctypes.c_float, _vp, _i64, _i64, _vp, _i64,
@@ -151,6 +154,11 @@ def version() -> str:
 def sgemm_f32_raw(M, N, K, A_ptr, lda, B_ptr, ldb, C_ptr, ldc, stream_handle=0) -> int:
     """Direct C-ABI call with integer device pointers; returns the status code."""
     return lib.sgemm_f32(M, N, K, A_ptr, lda, B_ptr, ldb, C_ptr, ldc, stream_handle)
+
+
+def sgemm_f32_noalloc_raw(M, N, K, A_ptr, lda, B_ptr, ldb, C_ptr, ldc, stream_handle=0) -> int:
+    """sgemm_f32_noalloc through the C ABI (integer device pointers); returns the status code."""
+    return lib.sgemm_f32_noalloc(M, N, K, A_ptr, lda, B_ptr, ldb, C_ptr, ldc, stream_handle)
 
 
 def _rowmajor_2d(t, name):

@@ -56,7 +56,9 @@ enum sgemm_status {
                                   alignment (SGEMM_AUTO never returns this) */
     SGEMM_ERR_LAUNCH = 3,      /* a CUDA call failed while enqueueing */
     SGEMM_ERR_DEVICE = 4,      /* no usable device, or not compute capability 10.3 */
-    SGEMM_ERR_TIMEOUT = 5      /* a kernel gave up a bounded wait (see sgemm_device_status) */
+    SGEMM_ERR_TIMEOUT = 5,     /* a kernel gave up a bounded wait (see sgemm_device_status) */
+    SGEMM_ERR_SCRATCH = 6      /* sgemm_f32_noalloc: the product needs more scratch than its
+                                  fixed buffer (SGEMM_NOALLOC_SCRATCH_BYTES) holds */
 };
 
 /* Kernel variants. */
@@ -207,6 +209,41 @@ int sgemm_f32_fused(int transA, int transB, int64_t M, int64_t N, int64_t K, flo
 int sgemm_f32_from_host(int64_t M, int64_t N, int64_t K, const float *A_host, int64_t lda,
                         const float *B_host, int64_t ldb, float *C_host, int64_t ldc, float *dA,
                         float *dB, float *dC, sgemm_stream_t stream);
+
+/*
+ * C = A * B like sgemm_f32 (same arguments, results and errors), without
+ * allocating memory. The pages define no such entry point; it exists because
+ * of sgemm_f32's one allocation (see the conventions above: the aligned
+ * copies of A or B whose rows are not 16-byte aligned, for tensor-core
+ * products of at least 2^28 multiply-adds).
+ * Some callers cannot let a library take device memory during a call: a
+ * program whose device memory is all reserved up front by its own allocator
+ * (a framework's caching allocator holding most of HBM), a service that must
+ * know before the first request how much memory the library uses, or code
+ * that may not risk an allocation failing in the middle of a step. This entry
+ * point puts those copies into one fixed buffer of SGEMM_NOALLOC_SCRATCH_BYTES
+ * per device instead: a file-scope __device__ array of the library, created
+ * with the library's device code when the module is loaded, not by this call.
+ *   - A product whose copies would need more than SGEMM_NOALLOC_SCRATCH_BYTES
+ *     is rejected with SGEMM_ERR_SCRATCH before anything is enqueued. The
+ *     copies take 4 * rows * round_up(columns, 4) bytes for each operand whose
+ *     rows are not aligned (A: M x K, B: K x N), each rounded up to 256 bytes;
+ *     products that make no copies (aligned rows, or fewer multiply-adds)
+ *     have no limit.
+ *   - Nothing in the buffer needs to start at zero: every value a product
+ *     reads from it was written by the copy pass of the same call.
+ *   - The buffer is shared by every call of this entry point on a device. Two
+ *     calls whose work may overlap on the GPU (different streams with no
+ *     ordering between them, or calls from several host threads) race on it
+ *     and give wrong results; order them (one stream, or events).
+ *   - The first call on each device looks up the buffer's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture begins. If the lookup fails the call returns
+ *     SGEMM_ERR_DEVICE.
+ */
+#define SGEMM_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+int sgemm_f32_noalloc(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, const float *B,
+                      int64_t ldb, float *C, int64_t ldc, sgemm_stream_t stream);
 
 /* Variant selection, process-wide (all threads, all devices). Returns SGEMM_OK
  * or SGEMM_ERR_INVALID_ARG for an unknown value. The initial value is
