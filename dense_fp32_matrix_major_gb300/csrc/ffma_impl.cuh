@@ -64,7 +64,7 @@ struct Cfg {
     static_assert(BK * BN / 4 % THREADS == 0, "B tile must split evenly over threads");
 };
 
-using CfgBig = Cfg<2, 4, 4, 4, 1, 8>;     // 128 x 256, 256 threads, 8 x 16 per thread
+using CfgBig = Cfg<2, 4, 4, 4, 1, 16>;    // 128 x 256, 256 threads, 8 x 16 per thread
 using CfgMid = Cfg<2, 4, 2, 4, 2, 16>;    // 128 x 128, 256 threads, 8 x 8 per thread
 using CfgSmall = Cfg<1, 2, 2, 3, 6, 16>;  // 64 x 64, 64 threads, 8 x 8 per thread
 
@@ -203,11 +203,14 @@ __device__ __forceinline__ void process_tile(const FfmaArgs &a, float *As, float
     float *Cb = a.C + item * a.strideC;
     const int nk = ke - kb;
 
-    float acc[8][TN];
+    // Accumulators in pairs of adjacent columns: each update is one packed
+    // fma.rn.f32x2 (two fp32 fused multiply-adds, each rounded to nearest as
+    // fmaf would), half the issue slots of scalar FFMAs.
+    unsigned long long acc2[8][TN / 2];
 #pragma unroll
     for (int i = 0; i < 8; ++i)
 #pragma unroll
-        for (int j = 0; j < TN; ++j) acc[i][j] = 0.0f;
+        for (int j = 0; j < TN / 2; ++j) acc2[i][j] = 0ull;
 
     __syncthreads();  // the previous tile of this CTA is done with the ring
 #pragma unroll
@@ -232,9 +235,9 @@ __device__ __forceinline__ void process_tile(const FfmaArgs &a, float *As, float
         }
         const float *as = As + (t % S) * C::A_STAGE;
         const float *bs = Bs + (t % S) * C::B_STAGE;
-        // Rolled passes of KU unrolled k-steps. With the 8 x 16 register tile a
-        // full unroll of BK = 16 overflows the instruction cache, so that
-        // configuration runs two passes of 8; the swizzle term
+        // Rolled passes of KU unrolled k-steps (KU = BK: one pass; with scalar
+        // FFMAs the 8 x 16 register tile's full unroll overflowed the
+        // instruction cache, with packed ones it fits); the swizzle term
         // ((k8 + kk) & 7 = kk & 7) stays a compile-time constant.
 #pragma unroll 1
         for (int k8 = 0; k8 < BK; k8 += C::KU)
@@ -260,13 +263,27 @@ __device__ __forceinline__ void process_tile(const FfmaArgs &a, float *As, float
                 bv[c * 4 + 2] = v.z;
                 bv[c * 4 + 3] = v.w;
             }
+            unsigned long long b2[TN / 2];
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
+            for (int j = 0; j < TN / 2; ++j)
+                asm("mov.b64 %0, {%1, %2};" : "=l"(b2[j]) : "f"(bv[2 * j]), "f"(bv[2 * j + 1]));
 #pragma unroll
-                for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+            for (int i = 0; i < 8; ++i) {
+                unsigned long long a2;  // av[i] in both halves
+                asm("mov.b64 %0, {%1, %1};" : "=l"(a2) : "f"(av[i]));
+#pragma unroll
+                for (int j = 0; j < TN / 2; ++j)
+                    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc2[i][j]) : "l"(a2), "l"(b2[j]));
+            }
         }
     }
     cp_async_wait<0>();
+    float acc[8][TN];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < TN / 2; ++j)
+            asm("mov.b64 {%0, %1}, %2;" : "=f"(acc[i][2 * j]), "=f"(acc[i][2 * j + 1]) : "l"(acc2[i][j]));
 
     // Epilogue: rows wm0 + g*32 + tm*4 + r, columns wn0 + c*16 + tn*4 + q.
     // Everything the stores need, read from the parameters before the first
@@ -317,7 +334,8 @@ __device__ __forceinline__ void process_tile(const FfmaArgs &a, float *As, float
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     if (col + q >= N) continue;
-                    float x = beta != 0.0f ? fmaf(beta, crow[col + q], v[q]) : v[q];
+                    float x = v[q];
+                    if (beta != 0.0f) x = fmaf(beta, crow[col + q], x);
                     if (ep) x = epilogue_value(x, bias, bias_kind, act, row, col + q);
                     crow[col + q] = x;
                 }
