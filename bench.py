@@ -613,7 +613,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--variant", default="auto", choices=["auto", "ffma", "tf32x3"])
     ap.add_argument("--workload", default=wl.C5_HEAD.name, choices=sorted(wl.BY_NAME))
-    ap.add_argument("--tc-kernel", type=int, default=None, choices=[0, 1, 2, 3, 4],
+    ap.add_argument("--tc-kernel", type=int, default=None, choices=[0, 1, 2, 3, 4, 5],
                     help="tensor-core kernel for 16-byte-aligned operands (library tuning key)")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)

@@ -15,13 +15,15 @@
 //     a thread 8*TN fused multiply-adds against 2 + TN/4 128-bit shared-memory
 //     loads. The multiply-adds are issued as packed fma.rn.f32x2 on pairs of
 //     adjacent columns (two IEEE fp32 FMAs each, the same results as fmaf):
-//     half the issue slots, measured 48.5 -> 53.3 TFLOP/s at 2048x3072x4096.
+//     half the issue slots (measured 48.5 -> 53.3 TFLOP/s at 2048x3072x4096;
+//     56.0 with a two-stage ring).
 //   * A and B move global -> shared with cp.async through a STAGES-deep ring
-//     (one __syncthreads per k-step). A is transposed on the way (4-byte
-//     copies into As[k][m]) so each thread reads four rows with one 128-bit
-//     load; As is XOR-swizzled on 16-byte groups by (k & 7) so the transposing
-//     stores spread over the banks. B keeps its layout (16-byte copies when
-//     its rows are 16-byte aligned, else 4-byte copies).
+//     (one __syncthreads per k-tile; two stages for the 128x256 tile). A is
+//     transposed on the way (4-byte copies into As[k][m]) so each thread
+//     reads four rows with one 128-bit load; As is XOR-swizzled on 16-byte
+//     groups by (k & 7) so the transposing stores spread over the banks. B
+//     keeps its layout (16-byte copies when its rows are 16-byte aligned,
+//     else 4-byte copies).
 //   * Out-of-range elements are copied as zeros (cp.async src-size 0), the
 //     store is guarded by row < M and col < N on both sides (the '&&' guard,
 //     not the '||' guard that writes out of bounds), and nothing is written
