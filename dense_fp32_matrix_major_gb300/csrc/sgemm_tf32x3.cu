@@ -78,7 +78,11 @@ constexpr int STAGE_BYTES = 2 * A_TILE + 2 * B_TILE;  // A_hi, A_lo, B_hi, B_lo
 constexpr int PRODUCER_WARPS = 8;
 constexpr int THREADS = 32 * (1 + PRODUCER_WARPS + EPILOGUE_WARPS);
 constexpr int PRODUCER_THREADS = 32 * PRODUCER_WARPS;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + BAR_BYTES + 1024;  // + slack to align to 1024
+// C rows that are not 16-byte aligned leave through one 32 x 32 staging
+// chunk per epilogue warp (coalesced row stores, store_staged_rows).
+constexpr int STAGE_C = STAGES * STAGE_BYTES;
+constexpr int C_CHUNK_BYTES = 32 * 32 * 4;
+constexpr int SMEM_BYTES = STAGE_C + EPILOGUE_WARPS * C_CHUNK_BYTES + BAR_BYTES + 1024;  // + slack to align to 1024
 constexpr int A_TASKS = BM * (BK / 4);  // 16-byte chunks per A tile
 constexpr int B_TASKS = BN * (BK / 4);
 static_assert(A_TASKS % PRODUCER_THREADS == 0 && B_TASKS % PRODUCER_THREADS == 0, "even producer split");
@@ -89,7 +93,7 @@ __global__ void __launch_bounds__(THREADS, 1) tf32x3_kernel(const Args a) {
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;  // 1024-aligned: the swizzle uses address bits 4-9
     uint8_t *smem = smem_raw + (base - raw);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_BYTES);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGE_C + EPILOGUE_WARPS * C_CHUNK_BYTES);
     // bars[0..1] full, [2..3] empty, [4] acc_full, [6] acc_empty, [8] drain
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + 9);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 10);
@@ -340,7 +344,19 @@ __global__ void __launch_bounds__(THREADS, 1) tf32x3_kernel(const Args a) {
                     if (last) {
                         fix_nonfinite(a, at.item, row, n0 + ch * 32, static_cast<int64_t>(kb) * BK,
                                       static_cast<int64_t>(ke) * BK, v);
-                        store_chunk_regs<VEC_C>(a, crow, row, n0 + ch * 32, v, atomic);
+                        if (VEC_C || (a.ep && !atomic)) {
+                            store_chunk_regs<VEC_C>(a, crow, row, n0 + ch * 32, v, atomic);
+                        } else if (n0 + ch * 32 < a.N) {
+                            // Unaligned C rows: through shared memory, one coalesced row per step.
+                            const uint32_t cs = base + static_cast<uint32_t>(STAGE_C + q * C_CHUNK_BYTES);
+#pragma unroll
+                            for (int j = 0; j < 8; ++j)
+                                st_shared_v4(cs + sw128_offset(lane, j), v[4 * j], v[4 * j + 1], v[4 * j + 2],
+                                             v[4 * j + 3]);
+                            __syncwarp();
+                            store_staged_rows(a, cs, a.C + at.item * a.strideC, m0 + q * 32, n0 + ch * 32, atomic);
+                            __syncwarp();  // the chunk is read before the next one is written
+                        }
                     } else {
                         float h[16];
 #pragma unroll

@@ -268,51 +268,7 @@ __device__ __noinline__ void edge_final_chunk(const Args &a, uint32_t rc, float 
         }
     }
     __syncwarp();
-    // Parameters in registers: the shared-memory loads below are ordered
-    // against all memory, so fields read through `a` would be reloaded on
-    // every row.
-    const int64_t M = a.M, ldc = a.ldc, col = col0 + lane;
-    const bool col_ok = col < a.N;
-    const bool fused = a.ep && !atomic;
-    const int bias_kind = fused ? a.bias_kind : SGEMM_BIAS_NONE, act = a.act;
-    const float *bias = a.bias;
-    const float bcol = (bias_kind == SGEMM_BIAS_PER_COL && col_ok) ? __ldg(bias + col) : 0.0f;
-    const float alpha = a.alpha, beta = a.beta;
-    float *p = citem + row0 * ldc + col;
-    if (!fused) {
-        // All 32 values first (independent shared loads), then the stores.
-        float x[32];
-#pragma unroll
-        for (int r = 0; r < 32; ++r)
-            x[r] = ld_shared_f32(rc + sw128_offset(r, lane >> 2) + static_cast<uint32_t>((lane & 3) * 4));
-        if (!col_ok) return;
-        const int rows = M - row0 < 32 ? static_cast<int>(M - row0) : 32;
-        // Separate loops: with beta in the store expression the compiler
-        // loads C ahead of every store, beta or not.
-        if (atomic) {
-#pragma unroll
-            for (int r = 0; r < 32; ++r)
-                if (r < rows) atomicAdd(p + r * ldc, alpha * x[r]);
-        } else if (beta == 0.0f) {
-#pragma unroll
-            for (int r = 0; r < 32; ++r)
-                if (r < rows) p[r * ldc] = alpha * x[r];
-        } else {
-#pragma unroll
-            for (int r = 0; r < 32; ++r)
-                if (r < rows) p[r * ldc] = fmaf(beta, p[r * ldc], alpha * x[r]);
-        }
-        return;
-    }
-#pragma unroll 1
-    for (int r = 0; r < 32 && row0 + r < M; ++r, p += ldc) {  // the row bound is uniform over the warp
-        const float x = ld_shared_f32(rc + sw128_offset(r, lane >> 2) + static_cast<uint32_t>((lane & 3) * 4));
-        if (!col_ok) continue;
-        float y = alpha * x;
-        if (beta != 0.0f) y = fmaf(beta, *p, y);
-        y += bias_kind == SGEMM_BIAS_PER_COL ? bcol : (bias_kind == SGEMM_BIAS_PER_ROW ? __ldg(bias + row0 + r) : 0.0f);
-        *p = activate(y, act);
-    }
+    store_staged_rows(a, rc, citem, row0, col0, atomic);
 }
 
 // TA: A stored K x M (op(A) = A^T); TB: B stored N x K (op(B) = B^T).

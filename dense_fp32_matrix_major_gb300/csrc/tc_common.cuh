@@ -661,6 +661,63 @@ __device__ __forceinline__ void store_chunk_regs(const Args &a, float *crow, int
     }
 }
 
+// Writes a 32 x 32 chunk of C held in shared memory (chunk rc, 128-byte
+// swizzled rows, row r = row row0 + r, the unit's finished sums) one row per
+// step with the lanes along the row, so that each warp store covers 128
+// contiguous bytes whatever C's alignment: C = act(alpha * v + beta * C +
+// bias) for a whole tile, C += alpha * v with atomics for a tile split along
+// K. Rows from M and columns from N on are skipped. Called by all 32 lanes
+// after the chunk is complete in shared memory (__syncwarp).
+__device__ __forceinline__ void store_staged_rows(const Args &a, uint32_t rc, float *citem, int64_t row0,
+                                                  int64_t col0, bool atomic) {
+    const int lane = static_cast<int>(threadIdx.x & 31);
+    // Parameters in registers: the shared-memory loads below are ordered
+    // against all memory, so fields read through `a` would be reloaded on
+    // every row.
+    const int64_t M = a.M, ldc = a.ldc, col = col0 + lane;
+    const bool col_ok = col < a.N;
+    const bool fused = a.ep && !atomic;
+    const int bias_kind = fused ? a.bias_kind : SGEMM_BIAS_NONE, act = a.act;
+    const float *bias = a.bias;
+    const float bcol = (bias_kind == SGEMM_BIAS_PER_COL && col_ok) ? __ldg(bias + col) : 0.0f;
+    const float alpha = a.alpha, beta = a.beta;
+    float *p = citem + row0 * ldc + col;
+    if (!fused) {
+        // All 32 values first (independent shared loads), then the stores.
+        float x[32];
+#pragma unroll
+        for (int r = 0; r < 32; ++r)
+            x[r] = ld_shared_f32(rc + sw128_offset(r, lane >> 2) + static_cast<uint32_t>((lane & 3) * 4));
+        if (!col_ok) return;
+        const int rows = M - row0 < 32 ? static_cast<int>(M - row0) : 32;
+        // Separate loops: with beta in the store expression the compiler
+        // loads C ahead of every store, beta or not.
+        if (atomic) {
+#pragma unroll
+            for (int r = 0; r < 32; ++r)
+                if (r < rows) atomicAdd(p + r * ldc, alpha * x[r]);
+        } else if (beta == 0.0f) {
+#pragma unroll
+            for (int r = 0; r < 32; ++r)
+                if (r < rows) p[r * ldc] = alpha * x[r];
+        } else {
+#pragma unroll
+            for (int r = 0; r < 32; ++r)
+                if (r < rows) p[r * ldc] = fmaf(beta, p[r * ldc], alpha * x[r]);
+        }
+        return;
+    }
+#pragma unroll 1
+    for (int r = 0; r < 32 && row0 + r < M; ++r, p += ldc) {  // the row bound is uniform over the warp
+        const float x = ld_shared_f32(rc + sw128_offset(r, lane >> 2) + static_cast<uint32_t>((lane & 3) * 4));
+        if (!col_ok) continue;
+        float y = alpha * x;
+        if (beta != 0.0f) y = fmaf(beta, *p, y);
+        y += bias_kind == SGEMM_BIAS_PER_COL ? bcol : (bias_kind == SGEMM_BIAS_PER_ROW ? __ldg(bias + row0 + r) : 0.0f);
+        *p = activate(y, act);
+    }
+}
+
 // Epilogue of one 32-column chunk of the accumulator at TMEM address taddr
 // (this thread's lane, the sum over the unit's k-range [k_begin, k_end) of
 // batch item `item`): loads it, repairs non-finite outputs (fix_nonfinite)
