@@ -422,7 +422,11 @@ int launch_cfg(const Problem &p, const DeviceInfo &dev, int sk_mode, cudaStream_
     const int tiles = static_cast<int>(tiles64);
     const int slots = dev.sm_count * per_sm;
     // A stream-K share below this many k-steps costs more in fix-up than it saves.
-    const Schedule sch = make_schedule(tiles, k_tiles, slots, sk_mode, 8, 0.10);
+    // A partial last wave: every tile split along K (stream-K over all) beats
+    // whole tiles plus a split remainder here (measured on GB300, 128 x 256
+    // tiles, L2 flushed: 2048 x 3072 x 4096 887.7 vs 920.6 us, 4096^3 2334
+    // vs 2392, 3072^3 1003 vs 1035, 4096 x 2048 x 1024 319.5 vs 350.4).
+    const Schedule sch = make_schedule(tiles, k_tiles, slots, sk_mode, 8, 0.10, true);
 
     FfmaArgs a;
     a.M = p.M;

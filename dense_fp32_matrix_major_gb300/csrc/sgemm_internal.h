@@ -64,12 +64,12 @@ struct Schedule {
 // pays for its atomic fix-up (measured per kernel family on GB300: 0.10 for
 // FFMA, 0.25 for the tensor-core kernels, whose k-steps are far shorter).
 inline Schedule make_schedule(int tiles, int64_t k_steps, int slots, int mode, int64_t min_share,
-                              double idle_for_split) {
+                              double idle_for_split, bool split_all_for_remainder = false) {
     if (mode == SK_AUTO) {
         const int rem = tiles % slots;
         if (tiles >= slots) {
-            mode = (rem != 0 && static_cast<int64_t>(rem) * k_steps >= min_share * slots) ? SK_HYBRID
-                                                                                              : SK_DP_ONLY;
+            const int split = split_all_for_remainder ? SK_ALL : SK_HYBRID;
+            mode = (rem != 0 && static_cast<int64_t>(rem) * k_steps >= min_share * slots) ? split : SK_DP_ONLY;
         } else {
             const double idle = 1.0 - static_cast<double>(tiles) / static_cast<double>(slots);
             mode = (idle >= idle_for_split && k_steps >= 2 * min_share) ? SK_ALL : SK_DP_ONLY;

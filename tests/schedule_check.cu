@@ -49,9 +49,10 @@ int main() {
             for (int slots : slots_list)
                 for (int mode : modes)
                     for (int cap : {0, 128})
-                        for (int p : {0, 6}) {
+                        for (int p : {0, 6})
+                        for (bool split_all : {false, true}) {  // the FFMA kernels' policy for a partial wave
                             ++cases;
-                            const Schedule s = make_schedule(tiles, kbs, slots, mode, 4, 0.25);
+                            const Schedule s = make_schedule(tiles, kbs, slots, mode, 4, 0.25, split_all);
                             tc::Args a{};
                             a.k_blocks = kbs;
                             a.dp_tiles = s.dp_tiles;
