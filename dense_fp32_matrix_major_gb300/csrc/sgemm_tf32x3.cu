@@ -1195,12 +1195,17 @@ namespace {
 // kernels. Measured on GB300, L2 flushed, pair vs tensor-memory kernel:
 // 128^3 14.4 vs 15.7 us, 512^3 17.5 vs 22.2, 2048 x 128 x 512 17.2 vs 20.5,
 // 200 x 4096 x 4096 52.4 vs 68.6, 1024^3 27.5 vs 33.4; all four forms.
+// Batches of short products (K <= 256: at most 8 k-blocks per tile) stay on
+// the tensor-memory kernel, whose tiles switch at less cost: 512 x 128^3
+// 43.0 vs 55.8 us, 64 x 256^3 24.6 vs 31.8, 256 x 64^3 17.9 vs 26.6 (but
+// 32 x 512^3 73.2 vs 51.2, and single products keep the pair kernel:
+// 8192 x 8192 x 256 201.7 vs 148.1).
 int launch_aligned(const Problem &p, const DeviceInfo &dev, int sk_mode, int mode, cudaStream_t stream,
                    int *launches, bool after_copy = false) {
     const bool vc = (p.ldc % 4 == 0) && (p.strideC % 4 == 0) && (reinterpret_cast<uintptr_t>(p.C) % 16 == 0);
     const double work = static_cast<double>(p.M) * static_cast<double>(p.N) * static_cast<double>(p.K) *
                         static_cast<double>(p.batch);
-    const bool pair = mode == 4 || (mode == 0 && work >= 1048576.0);
+    const bool pair = mode == 4 || (mode == 0 && work >= 1048576.0 && !(p.batch > 1 && p.K <= 256));
     if (pair) {
         g_last_tc_kernel.store(4);
         return tf32x3_pair_launch(p, dev, sk_mode, false, stream, launches, after_copy);

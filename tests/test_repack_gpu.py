@@ -97,7 +97,7 @@ def test_unaligned_batch(lib, share):
                                     strideB=None if share == "b" else K * N + 3, share_a=share == "a",
                                     share_b=share == "b")
     assert rc == 0
-    assert lib.get_tuning(lib.SGEMM_TUNE_LAST_TC_KERNEL) == 4
+    assert lib.get_tuning(lib.SGEMM_TUNE_LAST_TC_KERNEL) in (3, 4)  # a TMA kernel on the copies
     assert batched_outside_intact(flat, batch, M, N, sC)
     for b in range(batch):
         C64, S = oracle.sgemm_f64(Af[b], Bf[b])
