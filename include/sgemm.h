@@ -202,9 +202,9 @@ int sgemm_f32_fused(int transA, int transB, int64_t M, int64_t N, int64_t K, flo
  * overlap. `stream` waits for the last
  * copy out, so the call behaves as if everything ran in order on `stream`.
  * The two library streams and their events are created on the first
- * pipelined call on a device and kept for the process (no memory is
- * allocated); concurrent pipelined calls on one device are serialised while
- * they enqueue.
+ * pipelined call on a device and kept for the process (creating them takes
+ * no device memory); concurrent pipelined calls on one device are serialised
+ * while they enqueue.
  */
 int sgemm_f32_from_host(int64_t M, int64_t N, int64_t K, const float *A_host, int64_t lda,
                         const float *B_host, int64_t ldb, float *C_host, int64_t ldc, float *dA,
