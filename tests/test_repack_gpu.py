@@ -153,3 +153,48 @@ def test_automatic_copy_at_large_size(lib):
     finally:
         sgemm.set_variant("tf32x3")
         sgemm.set_tuning(sgemm.SGEMM_TUNE_TF32X3_KERNEL, 5)
+
+
+@pytest.mark.parametrize("tA,tB", FORMS)
+def test_unaligned_rows_fused_epilogue(lib, tA, tB):
+    """The fused epilogue (per-column bias + ReLU, and per-row bias + GELU with
+    beta) on the aligned copies, every form."""
+    from tests.gpu_harness import run_fused
+
+    M, N, K = 300, 270, 301
+    As, Bs = _stored(M, N, K, tA, tB, 17)
+    rng = np.random.default_rng(11)
+    C0 = rng.standard_normal((M, N)).astype(np.float32)
+    for bias_kind, act, kind_name, act_name, beta in [(1, 1, "col", "relu", 0.0), (2, 2, "row", "gelu", 0.5)]:
+        bias = rng.standard_normal(N if bias_kind == 1 else M).astype(np.float32)
+        C, flat, rc = run_fused(As, Bs, bias=bias, bias_kind=bias_kind, act=act, transA=tA, transB=tB, alpha=1.25,
+                                beta=beta, C_init=C0 if beta else None, lda=As.shape[1] + 1, ldb=Bs.shape[1] + 3,
+                                ldc=N + 1)
+        assert rc == 0
+        assert lib.get_tuning(lib.SGEMM_TUNE_LAST_TC_KERNEL) == 4
+        assert outside_box_intact(flat, M, N, N + 1, 0)
+        C64, S = oracle.gemm_f64(As, Bs, transA=bool(tA), transB=bool(tB), alpha=1.25, beta=beta,
+                                 C_in=C0 if beta else None)
+        E64, ES = oracle.epilogue_f64(C64, S, bias=bias, bias_kind=kind_name, act=act_name)
+        assert oracle.normalized_error(C, E64, ES) <= TOL, (bias_kind, act)
+
+
+@pytest.mark.parametrize("K", [1537, 4097])
+def test_unaligned_rows_same_sign_accuracy(lib, K):
+    """U[0,1] inputs (the pages' rand() / RAND_MAX) through the copies: the
+    copy is exact, so the bounded accumulation chains keep the bound."""
+    import torch
+    from dense_fp32_matrix_major_gb300 import sgemm
+
+    M, N = 300, 517
+    A, B = wl.make_mixed(M, N, K, "uniform01", "uniform01", K)
+    fa, vA = device_matrix(A, K + 1, 0)
+    fb, vB = device_matrix(B, N + 3, 0)
+    C = torch.full((M, N), float("nan"), device="cuda")
+    rc = sgemm.sgemm_f32_raw(M, N, K, vA.data_ptr(), K + 1, vB.data_ptr(), N + 3, C.data_ptr(), N,
+                             torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert rc == 0
+    assert sgemm.get_tuning(sgemm.SGEMM_TUNE_LAST_TC_KERNEL) == 4
+    C64, S = oracle.sgemm_f64_rows(A, B)
+    assert oracle.normalized_error(C.cpu().numpy(), C64, S) <= TOL
