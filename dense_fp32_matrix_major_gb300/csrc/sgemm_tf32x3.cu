@@ -66,8 +66,9 @@ namespace {
 std::atomic<int64_t> g_watchdog_ms{2000};
 // Tensor-core kernel (tuning key SGEMM_TUNE_TF32X3_KERNEL): 0 = automatic,
 // 1 = per-thread loads only, 2 = TMA kernel, 3 = TMA kernel with A in TMEM,
-// 4 = the SM-pair kernel of sgemm_tf32x3_pair.cu (op(A) = A, op(B) = B; the
-// transposed forms take kernel 3).
+// 4 = the SM-pair kernel of sgemm_tf32x3_pair.cu (every form; TMA for
+// aligned rows, cp.async otherwise), 5 = automatic, with operands whose rows
+// TMA cannot address copied into aligned scratch at any size.
 std::atomic<int> g_use_tma{0};
 std::atomic<int> g_last_tc_kernel{0};
 
