@@ -96,8 +96,15 @@ def test_tuning_keys(binding):
     ],
 )
 def test_invalid_arguments_rejected_without_device(binding, args):
-    # Argument checks run before any CUDA call, so these work on a CPU-only host.
+    # Argument checks run before any CUDA call, so these work on a CPU-only host;
+    # the fixed-scratch entry point takes the same arguments and checks.
     assert binding.sgemm_f32_raw(*args, 0) == binding.SGEMM_ERR_INVALID_ARG
+    assert binding.sgemm_f32_noalloc_raw(*args, 0) == binding.SGEMM_ERR_INVALID_ARG
+
+
+def test_noalloc_status_and_limit(binding):
+    assert "scratch" in binding.strerror(binding.SGEMM_ERR_SCRATCH)
+    assert binding.SGEMM_NOALLOC_SCRATCH_BYTES == 64 << 20
 
 
 def _header_enums():
