@@ -1231,10 +1231,11 @@ int launch_aligned(const Problem &p, const DeviceInfo &dev, int sk_mode, int mod
 // Smallest product (multiply-adds) for which copying operands with
 // unaligned rows into aligned scratch and running the TMA kernels beats the
 // per-thread-load kernel (measured on GB300, L2 flushed, rows of K + 1 and
-// N + 1 floats, copies + TMA kernels vs per-thread loads: 511 x 511 x 513
-// 37.9 vs 30.7 us, 1023 x 2049 x 1537 54.3 vs 86.0, 2047 x 3071 x 4095
-// 188 vs 376).
-constexpr double kRepackMinWork = 268435456.0;
+// N + 1 floats, per-thread loads vs copies + TMA kernels: 1023 x 1023 x 1025
+// 39.5 vs 44.1 us, 1151 x 1151 x 1153 47.9 vs 47.1, 1279 x 1279 x 1281 53.8
+// vs 52.5, 1407 x 1407 x 1409 66.1 vs 42.5, 511 x 4095 x 1025 53.8 vs 35.9,
+// 1023 x 2049 x 1537 72.4 vs 50.4): 1.25 * 2^30.
+constexpr double kRepackMinWork = 1342177280.0;
 
 }  // namespace
 

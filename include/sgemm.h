@@ -20,7 +20,7 @@
  *   - The caller owns every buffer. The library keeps no pointer after a
  *     call returns and never synchronises the stream. It allocates device
  *     memory in one case only: a tensor-core product whose A or B rows are
- *     not 16-byte aligned (row stride or base address), from 2^28
+ *     not 16-byte aligned (row stride or base address), from 1.25 * 2^30
  *     multiply-adds on, copies those operands into aligned rows in scratch
  *     taken from a stream-ordered pool the library creates per device on
  *     first use (cudaMallocFromPoolAsync on `stream`, freed with
@@ -215,7 +215,7 @@ int sgemm_f32_from_host(int64_t M, int64_t N, int64_t K, const float *A_host, in
  * allocating memory. The pages define no such entry point; it exists because
  * of sgemm_f32's one allocation (see the conventions above: the aligned
  * copies of A or B whose rows are not 16-byte aligned, for tensor-core
- * products of at least 2^28 multiply-adds).
+ * products of at least 1.25 * 2^30 multiply-adds).
  * Some callers cannot let a library take device memory during a call: a
  * program whose device memory is all reserved up front by its own allocator
  * (a framework's caching allocator holding most of HBM), a service that must
@@ -298,7 +298,7 @@ int sgemm_watchdog_selftest(int64_t wait_ms, sgemm_stream_t stream);
  *                            where A and B have 16-byte aligned bases and
  *                            row strides, the SM-pair kernel from 2^20
  *                            multiply-adds on and the TMA kernel with A in
- *                            tensor memory below; otherwise, from 2^28
+ *                            tensor memory below; otherwise, from 1.25 * 2^30
  *                            multiply-adds on, the unaligned operands are
  *                            first copied into aligned rows (scratch from a
  *                            stream-ordered pool, see sgemm_f32) and the TMA

@@ -359,7 +359,7 @@ def test_output_beyond_2_31_elements(lib, setting):
     (2048, 3072, 4096, 0, "tf32x3", 4),
     (200, 4096, 4096, 0, "tf32x3", 4),  # thin products too
     (300, 300, 301, 1, "tf32x3", 1),    # rows not 16-byte aligned, small: per-thread loads
-    (1023, 1025, 513, 1, "tf32x3", 4),  # from 2^28: aligned copies, then SM pairs
+    (1023, 1025, 1301, 1, "tf32x3", 4),  # from 1.25 * 2^30: aligned copies, then SM pairs
 ])
 def test_auto_dispatch(lib, M, N, K, lda_pad, variant, tc):
     """AUTO's choice of variant and tensor-core kernel (SGEMM_TUNE_LAST_TC_KERNEL)

@@ -1,7 +1,7 @@
 """Operands whose rows TMA cannot address (row strides or base addresses not
 16-byte aligned, "CUDA内存优化入门：从Naive到Tiled矩阵乘法" section 六's
 sizes that are not multiples of the tile): the tensor-core path copies them
-into aligned scratch rows and runs the TMA kernels (automatically from 2^28
+into aligned scratch rows and runs the TMA kernels (automatically from 1.25 * 2^30
 multiply-adds on; here forced at small sizes with tensor-core kernel mode 5,
 and automatically at one large size). Every output is compared with the
 oracle, the inputs are left untouched and nothing outside C's box is
