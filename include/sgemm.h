@@ -131,7 +131,8 @@ int sgemm_f32_ex(int transA, int transB, int64_t M, int64_t N, int64_t K, float 
  * be 0 (one matrix shared by every item); C items must not overlap one
  * another (strideC >= (M-1)*ldc + N) nor any A or B item. batch == 0:
  * nothing is enqueued. The whole batch runs as one persistent launch (plus a
- * small scaling launch when some tiles are split along K).
+ * small scaling launch when some tiles are split along K, and one copy launch
+ * when rows TMA cannot address are copied, see the conventions above).
  */
 int sgemm_f32_batched(int transA, int transB, int64_t M, int64_t N, int64_t K, float alpha, const float *A,
                       int64_t lda, int64_t strideA, const float *B, int64_t ldb, int64_t strideB, float beta,
